@@ -1,0 +1,97 @@
+// Internal declarations shared by the translation units of libbi (not installed).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <atomic>
+#include <mutex>
+#include <string>
+
+#include "bi.h"
+
+struct bi_engine_s {
+    int device = 0;
+    int sm_count = 0;
+    cudaMemPool_t pool = nullptr;
+    int* d_status = nullptr;               // device status word (0 = fine)
+    uint64_t wait_limit_ns = 2000000000ull; // bounded device-side waits
+    std::atomic<uint64_t> launches{0};
+    std::mutex mu;                          // guards last_error
+    std::string last_error;
+};
+
+namespace bi {
+
+// Status codes written by kernels into the engine's status word.
+enum DeviceStatus : int { DEV_OK = 0, DEV_TIMEOUT_PRODUCER = 1, DEV_TIMEOUT_MMA = 2,
+                          DEV_TIMEOUT_EPILOGUE = 3, DEV_TIMEOUT_SELFTEST = 4 };
+
+// Everything a kernel launcher needs from the engine.
+struct LaunchCtx {
+    bi_engine eng;
+    cudaStream_t stream;
+    int sm_count;
+    int* status;
+    uint64_t wait_limit_ns;
+    void count(uint64_t n = 1) const { eng->launches.fetch_add(n, std::memory_order_relaxed); }
+};
+
+// ---- scalar tier (scalar.cu) ---------------------------------------------
+// "rows" kernels: out[r, c] = down( chain_l A[r, l] * B(l, c) (+ bias[c]) ), A
+// contraction-contiguous [R, L]; B is [L, C] (b_contr_contig = 0) or [C, L] (1).
+// Grouped: rows come from expert segments (seg/perm), B advanced by expert.
+cudaError_t scalar_rows(const LaunchCtx& c, bi_dtype dt, void* out, const void* a, const void* b,
+                        const void* bias, int64_t R, int64_t L, int64_t C, int b_contr_contig);
+cudaError_t scalar_rows_grouped(const LaunchCtx& c, bi_dtype dt, void* out, const void* a,
+                                const void* b, int64_t M, int64_t L, int64_t C, int64_t E,
+                                int b_contr_contig, const uint32_t* seg, const uint32_t* perm);
+// dW kernels: out[r, c] = tree over chunks of chain over rows m of A[m, r] * B[m, c].
+// partials: workspace of J*R*C floats (may be null when J == 1).
+cudaError_t scalar_dw(const LaunchCtx& c, bi_dtype dt, void* out, int out_f32, const void* a,
+                      const void* b, int64_t M, int64_t R, int64_t C, float* partials);
+cudaError_t scalar_dw_grouped(const LaunchCtx& c, bi_dtype dt, float* out, const void* a,
+                              const void* b, int64_t M, int64_t R, int64_t C, int64_t E,
+                              const uint32_t* seg, const uint32_t* perm, float* partials,
+                              int64_t max_chunks);
+
+// ---- grouping (grouped.cu) ------------------------------------------------
+// Segment table layout (u32): [0, E+2) offsets of groups 0..E (group E =
+// padding) plus M; [E+2, 2E+3) padded starts of experts 0..E (rows rounded up
+// to 128 per expert); then tc_rows (1 entry).
+inline int64_t seg_table_len(int64_t E) { return 2 * E + 4; }
+int64_t segment_scratch_bytes(int64_t M, int64_t E);
+cudaError_t segment(const LaunchCtx& c, const uint32_t* ids, int64_t M, int64_t E, uint32_t* seg,
+                    uint32_t* perm, void* scratch);
+// Copy rows of src [M, L] into dst [Mp, L] in padded expert order (zeros in the gaps).
+cudaError_t gather_padded(const LaunchCtx& c, const void* src, int64_t M, int64_t L, int64_t E,
+                          const uint32_t* seg, const uint32_t* perm, void* dst, int64_t Mp_max);
+// Zero the rows of out [M, C] (element size esize) whose ids are padding.
+cudaError_t zero_padding_rows(const LaunchCtx& c, void* out, int64_t C, int esize, int64_t E,
+                              const uint32_t* seg, const uint32_t* perm);
+cudaError_t selftest_wait(const LaunchCtx& c);
+
+// ---- tensor-core tier (tc.cu) ----------------------------------------------
+cudaError_t tc_forward(const LaunchCtx& c, bi_dtype dt, void* y, const void* x, const void* w,
+                       const void* bias, int64_t M, int64_t K, int64_t N);
+cudaError_t tc_dx(const LaunchCtx& c, bi_dtype dt, void* dx, const void* dy, const void* w,
+                  int64_t M, int64_t K, int64_t N);
+cudaError_t tc_dw(const LaunchCtx& c, bi_dtype dt, void* dw, int dw_f32, const void* x,
+                  const void* dy, int64_t M, int64_t K, int64_t N);
+// Grouped, on padded gathered operands (rows of expert g start at pstart[g]).
+cudaError_t tc_grouped_rows(const LaunchCtx& c, bi_dtype dt, int pass_dinput, void* out,
+                            const void* a_padded, int64_t Mp_max, const void* w, int64_t M,
+                            int64_t K, int64_t N, int64_t E, const uint32_t* seg,
+                            const uint32_t* perm);
+cudaError_t tc_grouped_dw(const LaunchCtx& c, bi_dtype dt, float* dw, const void* dy_padded,
+                          const void* x_padded, int64_t Mp_max, int64_t M, int64_t K, int64_t N,
+                          int64_t E, const uint32_t* seg);
+// Upper bound on padded rows for M rows over E experts (multiples of 128 per expert).
+inline int64_t padded_rows_max(int64_t M, int64_t E) { return ((M + 127) / 128) * 128 + E * 128; }
+
+}  // namespace bi
+
+namespace bi {
+__host__ __device__ __forceinline__ int64_t lmin(int64_t a, int64_t b) { return a < b ? a : b; }
+__host__ __device__ __forceinline__ int64_t lmax(int64_t a, int64_t b) { return a > b ? a : b; }
+}  // namespace bi

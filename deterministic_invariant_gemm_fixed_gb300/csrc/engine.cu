@@ -1,0 +1,368 @@
+// C ABI of libbi: argument validation, shape-only dispatch, scratch memory and
+// kernel orchestration.  See include/bi.h for the contract of every entry point.
+#include <cstdio>
+#include <cstring>
+#include <new>
+#include <string>
+
+#include "bi_internal.h"
+
+namespace {
+
+thread_local std::string tl_error;
+
+// Record an error on the engine (or on the calling thread) and return `st`.
+bi_status fail(bi_engine eng, bi_status st, const std::string& msg) {
+    if (eng) {
+        std::lock_guard<std::mutex> g(eng->mu);
+        eng->last_error = msg;
+    } else {
+        tl_error = msg;
+    }
+    return st;
+}
+
+bi_status cuda_fail(bi_engine eng, cudaError_t e, const char* where) {
+    return fail(eng, e == cudaErrorMemoryAllocation ? BI_ERR_OOM : BI_ERR_CUDA,
+                std::string(where) + ": " + cudaGetErrorName(e) + " (" + cudaGetErrorString(e) + ")");
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int64_t dsize(bi_dtype dt) { return dt == BI_F32 ? 4 : 2; }
+
+// Makes the engine's device current for the duration of a call, then restores.
+struct DeviceGuard {
+    int prev = -1;
+    bool ok = true;
+    explicit DeviceGuard(int dev) {
+        if (cudaGetDevice(&prev) != cudaSuccess) prev = -1;
+        if (prev != dev) ok = cudaSetDevice(dev) == cudaSuccess;
+    }
+    ~DeviceGuard() {
+        int cur = -1;
+        if (prev >= 0 && cudaGetDevice(&cur) == cudaSuccess && cur != prev) cudaSetDevice(prev);
+    }
+};
+
+// Stream-ordered scratch from the engine's pool, released in stream order.
+struct Scratch {
+    bi_engine eng;
+    cudaStream_t stream;
+    void* ptr = nullptr;
+    cudaError_t err = cudaSuccess;
+    Scratch(bi_engine e, cudaStream_t s, size_t bytes) : eng(e), stream(s) {
+        if (bytes) err = cudaMallocFromPoolAsync(&ptr, bytes, e->pool, s);
+    }
+    ~Scratch() {
+        if (ptr) cudaFreeAsync(ptr, stream);
+    }
+};
+
+const int64_t kMaxDim = (int64_t(1) << 31) - 1;
+
+bi_status check_common(bi_engine eng, bi_dtype dt, int64_t m, int64_t k, int64_t n) {
+    if (!eng) return fail(nullptr, BI_ERR_INVALID_ARG, "engine is NULL");
+    if (dt != BI_F32 && dt != BI_BF16 && dt != BI_F16)
+        return fail(eng, BI_ERR_INVALID_ARG, "dtype must be BI_F32, BI_BF16 or BI_F16");
+    if (m < 0) return fail(eng, BI_ERR_INVALID_ARG, "m must be >= 0");
+    if (k <= 0 || n <= 0) return fail(eng, BI_ERR_INVALID_ARG, "k and n must be > 0");
+    if (m > kMaxDim || k > kMaxDim || n > kMaxDim)
+        return fail(eng, BI_ERR_UNSUPPORTED, "a dimension exceeds 2^31 - 1");
+    if (n > int64_t(65535) * 128 || k > int64_t(65535) * 128)
+        return fail(eng, BI_ERR_UNSUPPORTED, "k and n are limited to 8388480");
+    return BI_OK;
+}
+
+bi::LaunchCtx ctx(bi_engine eng, void* stream) {
+    return bi::LaunchCtx{eng, static_cast<cudaStream_t>(stream), eng->sm_count, eng->d_status,
+                         eng->wait_limit_ns};
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* bi_version(void) { return "bi 0.1.0 (sm_103a)"; }
+
+int bi_dispatch_tier(int pass, bi_dtype dtype, int tensor_cores, int64_t k, int64_t n) {
+    if (!tensor_cores) return 0;
+    if (dtype != BI_BF16 && dtype != BI_F16) return 0;  // f32 operands: scalar tier
+    if (k <= 0 || n <= 0 || k % 8 != 0 || n % 8 != 0) return 0;  // 16-byte rows for TMA
+    switch (pass) {
+        case BI_PASS_FORWARD:
+        case BI_PASS_GROUPED_FORWARD: return n >= 64 ? 1 : 0;
+        case BI_PASS_DX:
+        case BI_PASS_GROUPED_DINPUT: return k >= 64 ? 1 : 0;
+        case BI_PASS_DW:
+        case BI_PASS_GROUPED_DWEIGHTS: return (k >= 64 && n >= 64) ? 1 : 0;
+        default: return 0;
+    }
+}
+
+bi_status bi_engine_create(int device, bi_engine* out) {
+    if (!out) return fail(nullptr, BI_ERR_INVALID_ARG, "out is NULL");
+    *out = nullptr;
+    int count = 0;
+    cudaError_t e = cudaGetDeviceCount(&count);
+    if (e != cudaSuccess) return cuda_fail(nullptr, e, "cudaGetDeviceCount");
+    if (device < 0 || device >= count) return fail(nullptr, BI_ERR_CUDA, "no such CUDA device");
+    bi_engine eng = new (std::nothrow) bi_engine_s();
+    if (!eng) return fail(nullptr, BI_ERR_OOM, "engine allocation failed");
+    eng->device = device;
+    DeviceGuard g(device);
+    if (!g.ok) { delete eng; return fail(nullptr, BI_ERR_CUDA, "cudaSetDevice failed"); }
+    if ((e = cudaDeviceGetAttribute(&eng->sm_count, cudaDevAttrMultiProcessorCount, device)) != cudaSuccess) {
+        delete eng;
+        return cuda_fail(nullptr, e, "cudaDeviceGetAttribute");
+    }
+    cudaMemPoolProps props{};
+    props.allocType = cudaMemAllocationTypePinned;
+    props.location.type = cudaMemLocationTypeDevice;
+    props.location.id = device;
+    if ((e = cudaMemPoolCreate(&eng->pool, &props)) != cudaSuccess) {
+        delete eng;
+        return cuda_fail(nullptr, e, "cudaMemPoolCreate");
+    }
+    uint64_t keep = ~uint64_t(0);  // keep freed scratch cached in the pool
+    cudaMemPoolSetAttribute(eng->pool, cudaMemPoolAttrReleaseThreshold, &keep);
+    if ((e = cudaMalloc(&eng->d_status, 16)) != cudaSuccess ||
+        (e = cudaMemset(eng->d_status, 0, 16)) != cudaSuccess) {
+        cudaMemPoolDestroy(eng->pool);
+        delete eng;
+        return cuda_fail(nullptr, e, "status word");
+    }
+    *out = eng;
+    return BI_OK;
+}
+
+void bi_engine_destroy(bi_engine eng) {
+    if (!eng) return;
+    {
+        DeviceGuard g(eng->device);
+        cudaFree(eng->d_status);
+        cudaMemPoolDestroy(eng->pool);
+    }
+    delete eng;
+}
+
+const char* bi_last_error(bi_engine eng) {
+    if (!eng) return tl_error.c_str();
+    std::lock_guard<std::mutex> g(eng->mu);
+    return eng->last_error.c_str();
+}
+
+uint64_t bi_launch_count(bi_engine eng) { return eng ? eng->launches.load() : 0; }
+
+bi_status bi_engine_set_wait_limit(bi_engine eng, uint64_t ns) {
+    if (!eng) return fail(nullptr, BI_ERR_INVALID_ARG, "engine is NULL");
+    eng->wait_limit_ns = ns ? ns : 2000000000ull;
+    return BI_OK;
+}
+
+bi_status bi_engine_check(bi_engine eng, void* stream) {
+    if (!eng) return fail(nullptr, BI_ERR_INVALID_ARG, "engine is NULL");
+    DeviceGuard g(eng->device);
+    cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(eng, e, "cudaStreamSynchronize");
+    int v = 0;
+    if ((e = cudaMemcpy(&v, eng->d_status, sizeof(int), cudaMemcpyDeviceToHost)) != cudaSuccess)
+        return cuda_fail(eng, e, "reading the status word");
+    if (v != 0) {
+        cudaMemset(eng->d_status, 0, sizeof(int));
+        static const char* who[] = {"", "TMA producer", "MMA issuer", "epilogue", "self-test"};
+        return fail(eng, BI_ERR_TIMEOUT,
+                    std::string("a device pipeline wait ran out (") + (v > 0 && v < 5 ? who[v] : "unknown") + ")");
+    }
+    return BI_OK;
+}
+
+bi_status bi_selftest_wait_timeout(bi_engine eng, void* stream) {
+    if (!eng) return fail(nullptr, BI_ERR_INVALID_ARG, "engine is NULL");
+    DeviceGuard g(eng->device);
+    cudaError_t e = bi::selftest_wait(ctx(eng, stream));
+    return e == cudaSuccess ? BI_OK : cuda_fail(eng, e, "self-test launch");
+}
+
+bi_status bi_forward(bi_engine eng, void* y, const void* x, const void* w, const void* bias,
+                     int64_t m, int64_t k, int64_t n, bi_dtype dtype, void* stream, int tensor_cores) {
+    bi_status st = check_common(eng, dtype, m, k, n);
+    if (st != BI_OK) return st;
+    if (m == 0) return BI_OK;
+    if (!y || !x || !w) return fail(eng, BI_ERR_INVALID_ARG, "y, x and w must not be NULL");
+    const int tier = bi_dispatch_tier(BI_PASS_FORWARD, dtype, tensor_cores, k, n);
+    if (tier && (!aligned16(y) || !aligned16(x) || !aligned16(w)))
+        return fail(eng, BI_ERR_MISALIGNED, "tensor-core tier needs 16-byte aligned y, x, w");
+    DeviceGuard g(eng->device);
+    if (!g.ok) return fail(eng, BI_ERR_CUDA, "cudaSetDevice failed");
+    const bi::LaunchCtx c = ctx(eng, stream);
+    cudaError_t e = tier ? bi::tc_forward(c, dtype, y, x, w, bias, m, k, n)
+                         : bi::scalar_rows(c, dtype, y, x, w, bias, m, k, n, 0);
+    return e == cudaSuccess ? BI_OK : cuda_fail(eng, e, "bi_forward");
+}
+
+bi_status bi_backward_dx(bi_engine eng, void* dx, const void* dy, const void* w, int64_t m,
+                         int64_t k, int64_t n, bi_dtype dtype, void* stream, int tensor_cores) {
+    bi_status st = check_common(eng, dtype, m, k, n);
+    if (st != BI_OK) return st;
+    if (m == 0) return BI_OK;
+    if (!dx || !dy || !w) return fail(eng, BI_ERR_INVALID_ARG, "dx, dy and w must not be NULL");
+    const int tier = bi_dispatch_tier(BI_PASS_DX, dtype, tensor_cores, k, n);
+    if (tier && (!aligned16(dx) || !aligned16(dy) || !aligned16(w)))
+        return fail(eng, BI_ERR_MISALIGNED, "tensor-core tier needs 16-byte aligned dx, dy, w");
+    DeviceGuard g(eng->device);
+    if (!g.ok) return fail(eng, BI_ERR_CUDA, "cudaSetDevice failed");
+    const bi::LaunchCtx c = ctx(eng, stream);
+    cudaError_t e = tier ? bi::tc_dx(c, dtype, dx, dy, w, m, k, n)
+                         : bi::scalar_rows(c, dtype, dx, dy, w, nullptr, m, n, k, 1);
+    return e == cudaSuccess ? BI_OK : cuda_fail(eng, e, "bi_backward_dx");
+}
+
+bi_status bi_backward_dw(bi_engine eng, void* dw, int dw_f32, const void* x, const void* dy,
+                         int64_t m, int64_t k, int64_t n, bi_dtype dtype, void* stream, int tensor_cores) {
+    bi_status st = check_common(eng, dtype, m, k, n);
+    if (st != BI_OK) return st;
+    if (!dw) return fail(eng, BI_ERR_INVALID_ARG, "dw must not be NULL");
+    if (m > 0 && (!x || !dy)) return fail(eng, BI_ERR_INVALID_ARG, "x and dy must not be NULL");
+    const int64_t J = (m + BI_DW_CHUNK - 1) / BI_DW_CHUNK;
+    if (J > 65535) return fail(eng, BI_ERR_UNSUPPORTED, "m is limited to 65535 * 256 rows for dW");
+    const int out_f32 = dw_f32 || dtype == BI_F32;
+    const int tier = bi_dispatch_tier(BI_PASS_DW, dtype, tensor_cores, k, n);
+    if (tier && m > 0 && (!aligned16(dw) || !aligned16(x) || !aligned16(dy)))
+        return fail(eng, BI_ERR_MISALIGNED, "tensor-core tier needs 16-byte aligned dw, x, dy");
+    DeviceGuard g(eng->device);
+    if (!g.ok) return fail(eng, BI_ERR_CUDA, "cudaSetDevice failed");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (m == 0) {  // empty sum: +0
+        cudaError_t e = cudaMemsetAsync(dw, 0, static_cast<size_t>(k * n * (out_f32 ? 4 : dsize(dtype))), s);
+        return e == cudaSuccess ? BI_OK : cuda_fail(eng, e, "bi_backward_dw");
+    }
+    const bi::LaunchCtx c = ctx(eng, stream);
+    if (tier) {
+        cudaError_t e = bi::tc_dw(c, dtype, dw, out_f32, x, dy, m, k, n);
+        return e == cudaSuccess ? BI_OK : cuda_fail(eng, e, "bi_backward_dw");
+    }
+    Scratch part(eng, s, J > 1 ? static_cast<size_t>(J * k * n * 4) : 0);
+    if (part.err != cudaSuccess) return cuda_fail(eng, part.err, "dW scratch");
+    cudaError_t e = bi::scalar_dw(c, dtype, dw, out_f32, x, dy, m, k, n, static_cast<float*>(part.ptr));
+    return e == cudaSuccess ? BI_OK : cuda_fail(eng, e, "bi_backward_dw");
+}
+
+namespace {
+
+bi_status check_grouped(bi_engine eng, bi_dtype dt, int64_t m, int64_t k, int64_t n, int64_t e) {
+    bi_status st = check_common(eng, dt, m, k, n);
+    if (st != BI_OK) return st;
+    if (e <= 0) return fail(eng, BI_ERR_INVALID_ARG, "e must be > 0");
+    if (e > 65535) return fail(eng, BI_ERR_UNSUPPORTED, "e is limited to 65535 experts");
+    // the same U32 indexing limits as the grouped matmul of rublas (GroupedMatmulError)
+    const uint64_t lim = 0xffffffffull;
+    if (uint64_t(m) * uint64_t(k) > lim || uint64_t(m) * uint64_t(n) > lim ||
+        uint64_t(e) * uint64_t(n) * uint64_t(k) > lim)
+        return fail(eng, BI_ERR_UNSUPPORTED, "grouped matmul exceeds U32 indexing");
+    return BI_OK;
+}
+
+}  // namespace
+
+bi_status bi_grouped_forward(bi_engine eng, void* y, const void* x, const void* w,
+                             const uint32_t* row_experts, int64_t m, int64_t k, int64_t n, int64_t e,
+                             bi_dtype dtype, void* stream, int tensor_cores) {
+    bi_status st = check_grouped(eng, dtype, m, k, n, e);
+    if (st != BI_OK) return st;
+    if (m == 0) return BI_OK;
+    if (!y || !x || !w || !row_experts)
+        return fail(eng, BI_ERR_INVALID_ARG, "y, x, w and row_experts must not be NULL");
+    const int tier = bi_dispatch_tier(BI_PASS_GROUPED_FORWARD, dtype, tensor_cores, k, n);
+    if (tier && (!aligned16(y) || !aligned16(x) || !aligned16(w)))
+        return fail(eng, BI_ERR_MISALIGNED, "tensor-core tier needs 16-byte aligned y, x, w");
+    DeviceGuard g(eng->device);
+    if (!g.ok) return fail(eng, BI_ERR_CUDA, "cudaSetDevice failed");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const bi::LaunchCtx c = ctx(eng, stream);
+    // scratch: seg table | perm | histogram | (padded X)
+    const int64_t seg_b = ((bi::seg_table_len(e) * 4 + 255) / 256) * 256;
+    const int64_t perm_b = ((m * 4 + 255) / 256) * 256;
+    const int64_t hist_b = ((bi::segment_scratch_bytes(m, e) + 255) / 256) * 256;
+    const int64_t mp = bi::padded_rows_max(m, e);
+    const int64_t pad_b = tier ? mp * k * 2 : 0;
+    Scratch sc(eng, s, static_cast<size_t>(seg_b + perm_b + hist_b + pad_b));
+    if (sc.err != cudaSuccess) return cuda_fail(eng, sc.err, "grouped scratch");
+    uint8_t* base = static_cast<uint8_t*>(sc.ptr);
+    uint32_t* seg = reinterpret_cast<uint32_t*>(base);
+    uint32_t* perm = reinterpret_cast<uint32_t*>(base + seg_b);
+    void* hist = base + seg_b + perm_b;
+    void* xpad = base + seg_b + perm_b + hist_b;
+    cudaError_t err = bi::segment(c, row_experts, m, e, seg, perm, hist);
+    if (err == cudaSuccess) {
+        if (tier) {
+            err = bi::gather_padded(c, x, m, k, e, seg, perm, xpad, mp);
+            if (err == cudaSuccess)
+                err = bi::tc_grouped_rows(c, dtype, 0, y, xpad, mp, w, m, k, n, e, seg, perm);
+        } else {
+            err = bi::scalar_rows_grouped(c, dtype, y, x, w, m, k, n, e, 1, seg, perm);
+        }
+    }
+    if (err == cudaSuccess) err = bi::zero_padding_rows(c, y, n, static_cast<int>(dsize(dtype)), e, seg, perm);
+    return err == cudaSuccess ? BI_OK : cuda_fail(eng, err, "bi_grouped_forward");
+}
+
+bi_status bi_grouped_backward(bi_engine eng, void* dx, float* dw, const void* x, const void* w,
+                              const void* dy, const uint32_t* row_experts, int64_t m, int64_t k,
+                              int64_t n, int64_t e, bi_dtype dtype, void* stream, int tensor_cores) {
+    bi_status st = check_grouped(eng, dtype, m, k, n, e);
+    if (st != BI_OK) return st;
+    if (!dw) return fail(eng, BI_ERR_INVALID_ARG, "dw must not be NULL");
+    DeviceGuard g(eng->device);
+    if (!g.ok) return fail(eng, BI_ERR_CUDA, "cudaSetDevice failed");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (m == 0) {
+        cudaError_t err = cudaMemsetAsync(dw, 0, static_cast<size_t>(e * n * k * 4), s);
+        return err == cudaSuccess ? BI_OK : cuda_fail(eng, err, "bi_grouped_backward");
+    }
+    if (!x || !w || !dy || !row_experts)
+        return fail(eng, BI_ERR_INVALID_ARG, "x, w, dy and row_experts must not be NULL");
+    const int tier_dx = dx ? bi_dispatch_tier(BI_PASS_GROUPED_DINPUT, dtype, tensor_cores, k, n) : 0;
+    const int tier_dw = bi_dispatch_tier(BI_PASS_GROUPED_DWEIGHTS, dtype, tensor_cores, k, n);
+    if ((tier_dx || tier_dw) &&
+        (!aligned16(x) || !aligned16(w) || !aligned16(dy) || !aligned16(dw) || (dx && !aligned16(dx))))
+        return fail(eng, BI_ERR_MISALIGNED, "tensor-core tier needs 16-byte aligned operands");
+    const bi::LaunchCtx c = ctx(eng, stream);
+    const int64_t seg_b = ((bi::seg_table_len(e) * 4 + 255) / 256) * 256;
+    const int64_t perm_b = ((m * 4 + 255) / 256) * 256;
+    const int64_t hist_b = ((bi::segment_scratch_bytes(m, e) + 255) / 256) * 256;
+    const int64_t mp = bi::padded_rows_max(m, e);
+    const bool need_dy_pad = tier_dx || tier_dw;
+    const int64_t dypad_b = need_dy_pad ? ((mp * n * 2 + 255) / 256) * 256 : 0;
+    const int64_t xpad_b = tier_dw ? ((mp * k * 2 + 255) / 256) * 256 : 0;
+    const int64_t max_chunks = (m + BI_DW_CHUNK - 1) / BI_DW_CHUNK + e;
+    const int64_t part_b = tier_dw ? 0 : max_chunks * n * k * 4;
+    Scratch sc(eng, s, static_cast<size_t>(seg_b + perm_b + hist_b + dypad_b + xpad_b + part_b));
+    if (sc.err != cudaSuccess) return cuda_fail(eng, sc.err, "grouped scratch");
+    uint8_t* base = static_cast<uint8_t*>(sc.ptr);
+    uint32_t* seg = reinterpret_cast<uint32_t*>(base);
+    uint32_t* perm = reinterpret_cast<uint32_t*>(base + seg_b);
+    void* hist = base + seg_b + perm_b;
+    void* dypad = base + seg_b + perm_b + hist_b;
+    void* xpad = static_cast<uint8_t*>(dypad) + dypad_b;
+    float* part = reinterpret_cast<float*>(static_cast<uint8_t*>(xpad) + xpad_b);
+    cudaError_t err = bi::segment(c, row_experts, m, e, seg, perm, hist);
+    if (err == cudaSuccess && need_dy_pad) err = bi::gather_padded(c, dy, m, n, e, seg, perm, dypad, mp);
+    if (err == cudaSuccess && dx) {
+        err = tier_dx ? bi::tc_grouped_rows(c, dtype, 1, dx, dypad, mp, w, m, k, n, e, seg, perm)
+                      : bi::scalar_rows_grouped(c, dtype, dx, dy, w, m, n, k, e, 0, seg, perm);
+        if (err == cudaSuccess)
+            err = bi::zero_padding_rows(c, dx, k, static_cast<int>(dsize(dtype)), e, seg, perm);
+    }
+    if (err == cudaSuccess) {
+        if (tier_dw) {
+            err = bi::gather_padded(c, x, m, k, e, seg, perm, xpad, mp);
+            if (err == cudaSuccess) err = bi::tc_grouped_dw(c, dtype, dw, dypad, xpad, mp, m, k, n, e, seg);
+        } else {
+            err = bi::scalar_dw_grouped(c, dtype, dw, dy, x, m, n, k, e, seg, perm, part, max_chunks);
+        }
+    }
+    return err == cudaSuccess ? BI_OK : cuda_fail(eng, err, "bi_grouped_backward");
+}
+
+}  // extern "C"

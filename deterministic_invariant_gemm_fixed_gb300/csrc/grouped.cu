@@ -1,0 +1,260 @@
+// Grouping of rows by expert id for the grouped matmul.
+//
+// Source: rublas 0.1.45 src/tensor_grouped/mod.rs -- ids outside [0,E) are
+// padding and produce zero rows (fn grouped_matmul_nt); the segmented backward
+// takes `offsets` [E+1] that describe the same grouping as `row_experts`
+// (fn grouped_matmul_nt_backward_segmented_with_strategy).  Here the library
+// builds that grouping itself, on the device, as a stable counting sort:
+//
+//   1. count:   each block counts the ids of its slice of rows per bucket
+//               (bucket = id for id < E, bucket E = padding);
+//   2. scan:    exclusive prefix over (bucket, block) in bucket-major order gives
+//               every block its first output position per bucket, the group
+//               offsets, and the padded starts used by the tensor-core tier;
+//   3. scatter: each block walks its slice in row order, 256 rows at a time; a
+//               row's position is its block's running base for its bucket plus
+//               the number of earlier rows of that bucket in the same 256-row
+//               step.  No atomics anywhere: positions are a pure function of the
+//               ids, so the permutation is stable and run-to-run identical.
+#include "bi_internal.h"
+
+namespace bi {
+namespace {
+
+constexpr int SEG_THREADS = 256;
+constexpr int SEG_ROWS_PER_BLOCK = 4096;
+constexpr uint32_t NONE = 0xffffffffu;
+
+__device__ __forceinline__ uint32_t bucket_of(uint32_t id, uint32_t E) { return id < E ? id : E; }
+
+// For the row held by thread `tid` in a 256-row step staged in sb[]: number of
+// earlier rows with the same bucket, and whether no later row shares it.
+__device__ __forceinline__ void rank_in_step(const uint32_t* sb, int tid, uint32_t g, uint32_t& rank,
+                                             bool& last) {
+    rank = 0;
+    for (int j = 0; j < tid; ++j) rank += sb[j] == g;
+    last = true;
+    for (int j = tid + 1; j < SEG_THREADS; ++j)
+        if (sb[j] == g) { last = false; break; }
+}
+
+__global__ void __launch_bounds__(SEG_THREADS)
+    seg_count_kernel(const uint32_t* ids, int64_t M, uint32_t E, uint32_t* hist, int64_t NB) {
+    __shared__ uint32_t sb[SEG_THREADS];
+    const int64_t b = blockIdx.x;
+    const int64_t begin = b * SEG_ROWS_PER_BLOCK;
+    const int64_t end = lmin(M, begin + SEG_ROWS_PER_BLOCK);
+    for (int64_t g = threadIdx.x; g <= E; g += SEG_THREADS) hist[g * NB + b] = 0;
+    __syncthreads();
+    for (int64_t base = begin; base < end; base += SEG_THREADS) {
+        const int64_t r = base + threadIdx.x;
+        sb[threadIdx.x] = r < end ? bucket_of(ids[r], E) : NONE;
+        __syncthreads();
+        const uint32_t g = sb[threadIdx.x];
+        if (g != NONE) {
+            uint32_t rank;
+            bool last;
+            rank_in_step(sb, threadIdx.x, g, rank, last);
+            if (last) hist[g * NB + b] += rank + 1;  // the only writer of this entry in this step
+        }
+        __syncthreads();
+    }
+}
+
+// One block.  hist (bucket-major, (E+1)*NB entries) becomes its exclusive
+// prefix sum; seg receives offsets[0..E+1], padded starts pstart[0..E] and the
+// total padded row count.
+__global__ void __launch_bounds__(1024)
+    seg_scan_kernel(uint32_t* hist, int64_t NB, uint32_t E, int64_t M, uint32_t* seg) {
+    __shared__ uint32_t warp_sums[32];
+    __shared__ uint32_t carry;
+    const int64_t total = (static_cast<int64_t>(E) + 1) * NB;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    if (threadIdx.x == 0) carry = 0;
+    __syncthreads();
+    for (int64_t base = 0; base < total; base += 1024) {
+        const int64_t i = base + threadIdx.x;
+        const uint32_t v = i < total ? hist[i] : 0;
+        uint32_t x = v;  // inclusive scan within the warp
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
+            if (lane >= o) x += y;
+        }
+        if (lane == 31) warp_sums[warp] = x;
+        __syncthreads();
+        if (warp == 0) {
+            uint32_t s = warp_sums[lane];
+            for (int o = 1; o < 32; o <<= 1) {
+                const uint32_t y = __shfl_up_sync(0xffffffffu, s, o);
+                if (lane >= o) s += y;
+            }
+            warp_sums[lane] = s;  // inclusive over warps
+        }
+        __syncthreads();
+        const uint32_t before = carry + (warp ? warp_sums[warp - 1] : 0) + x - v;
+        if (i < total) hist[i] = before;
+        __syncthreads();
+        if (threadIdx.x == 1023) carry = before + v;
+        __syncthreads();
+    }
+    if (threadIdx.x == 0) {
+        for (uint32_t g = 0; g <= E; ++g) seg[g] = hist[static_cast<int64_t>(g) * NB];
+        seg[E + 1] = static_cast<uint32_t>(M);
+        uint32_t ps = 0;
+        for (uint32_t g = 0; g < E; ++g) {
+            seg[E + 2 + g] = ps;
+            const uint32_t cnt = seg[g + 1] - seg[g];
+            ps += (cnt + 127u) / 128u * 128u;
+        }
+        seg[E + 2 + E] = ps;
+        seg[2 * E + 3] = ps;
+    }
+}
+
+__global__ void __launch_bounds__(SEG_THREADS)
+    seg_scatter_kernel(const uint32_t* ids, int64_t M, uint32_t E, uint32_t* base_pos, int64_t NB,
+                       uint32_t* perm) {
+    __shared__ uint32_t sb[SEG_THREADS];
+    const int64_t b = blockIdx.x;
+    const int64_t begin = b * SEG_ROWS_PER_BLOCK;
+    const int64_t end = lmin(M, begin + SEG_ROWS_PER_BLOCK);
+    for (int64_t base = begin; base < end; base += SEG_THREADS) {
+        const int64_t r = base + threadIdx.x;
+        sb[threadIdx.x] = r < end ? bucket_of(ids[r], E) : NONE;
+        __syncthreads();
+        const uint32_t g = sb[threadIdx.x];
+        uint32_t rank = 0;
+        bool last = false;
+        if (g != NONE) {
+            rank_in_step(sb, threadIdx.x, g, rank, last);
+            perm[base_pos[g * NB + b] + rank] = static_cast<uint32_t>(r);
+        }
+        __syncthreads();  // every row of this step has read the old base
+        if (g != NONE && last) base_pos[g * NB + b] += rank + 1;
+        __syncthreads();
+    }
+}
+
+// dst row p (padded order): expert g with pstart[g] <= p < pstart[g+1];
+// rows past the expert's count are zero.
+__global__ void gather_padded_kernel(const uint4* src, int64_t L16, uint32_t E, const uint32_t* seg,
+                                     const uint32_t* perm, uint4* dst, int64_t Mp_max) {
+    const uint32_t* off = seg;
+    const uint32_t* pst = seg + E + 2;
+    const int64_t total = pst[E];
+    for (int64_t p = blockIdx.x; p < total && p < Mp_max; p += gridDim.x) {
+        uint32_t lo = 0, hi = E;  // largest g with pst[g] <= p
+        while (hi - lo > 1) {
+            const uint32_t mid = (lo + hi) / 2;
+            if (pst[mid] <= p) lo = mid; else hi = mid;
+        }
+        const uint32_t g = lo;
+        const int64_t l = p - pst[g];
+        const int64_t cnt = off[g + 1] - off[g];
+        uint4* d = dst + p * L16;
+        if (l < cnt) {
+            const uint4* s = src + static_cast<int64_t>(perm[off[g] + l]) * L16;
+            for (int64_t i = threadIdx.x; i < L16; i += blockDim.x) d[i] = __ldg(s + i);
+        } else {
+            const uint4 z = make_uint4(0, 0, 0, 0);
+            for (int64_t i = threadIdx.x; i < L16; i += blockDim.x) d[i] = z;
+        }
+    }
+}
+
+__global__ void zero_rows_kernel(uint8_t* out, int64_t row_bytes, uint32_t E, const uint32_t* seg,
+                                 const uint32_t* perm) {
+    const int64_t first = seg[E], end = seg[E + 1];
+    for (int64_t s = first + blockIdx.x; s < end; s += gridDim.x) {
+        uint8_t* d = out + static_cast<int64_t>(perm[s]) * row_bytes;
+        for (int64_t i = threadIdx.x; i < row_bytes; i += blockDim.x) d[i] = 0;
+    }
+}
+
+__device__ __forceinline__ unsigned long long gtimer() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Waits on an mbarrier that nothing ever completes, bounded by `limit`, then
+// records the timeout the same way the GEMM pipeline does.
+__global__ void selftest_wait_kernel(int* status, unsigned long long limit) {
+    __shared__ __align__(8) uint64_t bar;
+    const uint32_t a = static_cast<uint32_t>(__cvta_generic_to_shared(&bar));
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(a) : "memory");
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    const unsigned long long t0 = gtimer();
+    for (;;) {
+        uint32_t ok;
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], 0;\n\t"
+            "selp.b32 %0, 1, 0, p;\n\t}\n"
+            : "=r"(ok)
+            : "r"(a)
+            : "memory");
+        if (ok) return;
+        if (gtimer() - t0 > limit) {
+            *reinterpret_cast<volatile int*>(status) = DEV_TIMEOUT_SELFTEST;
+            return;
+        }
+    }
+}
+
+int64_t num_seg_blocks(int64_t M) { return (M + SEG_ROWS_PER_BLOCK - 1) / SEG_ROWS_PER_BLOCK; }
+
+}  // namespace
+
+int64_t segment_scratch_bytes(int64_t M, int64_t E) {
+    return (E + 1) * (num_seg_blocks(M) > 0 ? num_seg_blocks(M) : 1) * 4;
+}
+
+cudaError_t segment(const LaunchCtx& c, const uint32_t* ids, int64_t M, int64_t E, uint32_t* seg,
+                    uint32_t* perm, void* scratch) {
+    const int64_t NB = num_seg_blocks(M) > 0 ? num_seg_blocks(M) : 1;
+    uint32_t* hist = static_cast<uint32_t*>(scratch);
+    if (M > 0) {
+        seg_count_kernel<<<static_cast<unsigned>(NB), SEG_THREADS, 0, c.stream>>>(ids, M, static_cast<uint32_t>(E), hist, NB);
+        c.count();
+    } else {
+        cudaError_t e = cudaMemsetAsync(hist, 0, (E + 1) * NB * 4, c.stream);
+        if (e != cudaSuccess) return e;
+    }
+    seg_scan_kernel<<<1, 1024, 0, c.stream>>>(hist, NB, static_cast<uint32_t>(E), M, seg);
+    c.count();
+    if (M > 0) {
+        seg_scatter_kernel<<<static_cast<unsigned>(NB), SEG_THREADS, 0, c.stream>>>(ids, M, static_cast<uint32_t>(E), hist, NB, perm);
+        c.count();
+    }
+    return cudaGetLastError();
+}
+
+cudaError_t gather_padded(const LaunchCtx& c, const void* src, int64_t M, int64_t L, int64_t E,
+                          const uint32_t* seg, const uint32_t* perm, void* dst, int64_t Mp_max) {
+    (void)M;
+    const int64_t L16 = L * 2 / 16;  // 16-bit data, L a multiple of 8
+    int64_t blocks = Mp_max < static_cast<int64_t>(c.sm_count) * 16 ? Mp_max : static_cast<int64_t>(c.sm_count) * 16;
+    if (blocks < 1) blocks = 1;
+    gather_padded_kernel<<<static_cast<unsigned>(blocks), 256, 0, c.stream>>>(
+        static_cast<const uint4*>(src), L16, static_cast<uint32_t>(E), seg, perm, static_cast<uint4*>(dst), Mp_max);
+    c.count();
+    return cudaGetLastError();
+}
+
+cudaError_t zero_padding_rows(const LaunchCtx& c, void* out, int64_t C, int esize, int64_t E,
+                              const uint32_t* seg, const uint32_t* perm) {
+    const unsigned blocks = static_cast<unsigned>(c.sm_count * 4);
+    zero_rows_kernel<<<blocks, 256, 0, c.stream>>>(static_cast<uint8_t*>(out), C * esize,
+                                                  static_cast<uint32_t>(E), seg, perm);
+    c.count();
+    return cudaGetLastError();
+}
+
+cudaError_t selftest_wait(const LaunchCtx& c) {
+    selftest_wait_kernel<<<1, 1, 0, c.stream>>>(c.status, c.wait_limit_ns);
+    c.count();
+    return cudaGetLastError();
+}
+
+}  // namespace bi

@@ -1,0 +1,477 @@
+// Scalar tier: fixed-order f32 fmaf chains, one output element per accumulator.
+//
+// Contract (sgemm-bi 0.1.1.post2, "Determinism contracts", row "f32 / typed
+// scalar"): bf16/f16 operands are widened exactly to f32, the f32 kernel runs,
+// and the result is rounded once to nearest-even.  Each output's chain is
+//     acc = +0.0f;  for l = 0, 1, ..., L-1:  acc = fmaf(a_l, b_l, acc)
+// and the forward adds the bias to acc in f32 before the single rounding
+// (ViperLLM ffma.py, _FFMAAddmm.forward).  Elements past the end of the
+// contraction are staged as zeros on both operands; fmaf(0, 0, acc) returns acc
+// exactly because acc is never -0 (it starts at +0 and a rounded sum is -0 only
+// when both addends are -0), so padding does not change a bit.
+//
+// Tiling: a 256-thread CTA computes a 128 x 128 output tile; each thread owns
+// 8 x 8 outputs (rows {4ty..4ty+3, 64+4ty..}, cols {4tx.., 64+4tx..}) and keeps
+// their accumulators in registers.  Operands are loaded with 16-byte vector
+// loads (when sizes and alignment allow), widened, and staged through a double
+// buffer in shared memory, 16 contraction steps at a time.
+//
+// dW reduction over rows (the weight gradient): rows are cut into chunks of
+// BI_DW_CHUNK rows from row 0 (per expert, from the expert's first row, for the
+// grouped dweights).  One CTA computes one chunk's chain for its tile; a second
+// kernel adds the chunk partials with the fixed pairwise tree (adjacent pairs,
+// odd last partial carried), evaluated as a binary counter, which performs the
+// same additions on the same operands.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "bi_internal.h"
+
+namespace bi {
+namespace {
+
+constexpr int TM = 128, TN = 128, TK = 16, NT = 256, PAD = 4;
+
+template <typename T> struct Elem;
+template <> struct Elem<float> {
+    static __device__ __forceinline__ float up(float v) { return v; }
+    static __device__ __forceinline__ float down(float v) { return v; }
+};
+template <> struct Elem<__nv_bfloat16> {
+    static __device__ __forceinline__ float up(__nv_bfloat16 v) { return __bfloat162float(v); }
+    static __device__ __forceinline__ __nv_bfloat16 down(float v) { return __float2bfloat16_rn(v); }
+};
+template <> struct Elem<__half> {
+    static __device__ __forceinline__ float up(__half v) { return __half2float(v); }
+    static __device__ __forceinline__ __half down(float v) { return __float2half_rn(v); }
+};
+
+// Load 8 consecutive elements starting at p (widened to f32).  VEC: p is
+// 16-byte aligned and all 8 are in range; otherwise `avail` of them are valid.
+template <typename T, bool VEC>
+__device__ __forceinline__ void load8(const T* p, int avail, float (&v)[8]) {
+    if (VEC && avail >= 8) {
+        if (sizeof(T) == 4) {
+            const float4 a = __ldg(reinterpret_cast<const float4*>(p));
+            const float4 b = __ldg(reinterpret_cast<const float4*>(p) + 1);
+            v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+            v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+        } else {
+            const uint4 a = __ldg(reinterpret_cast<const uint4*>(p));
+            const T* h = reinterpret_cast<const T*>(&a);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) v[i] = Elem<T>::up(h[i]);
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) v[i] = i < avail ? Elem<T>::up(p[i]) : 0.0f;
+    }
+}
+
+// Shared tile: s[l][i] with l the contraction step, i the row or column.
+struct Smem {
+    float a[2][TK][TM + PAD];
+    float b[2][TK][TN + PAD];
+};
+
+// 8x8 micro-tile product over one staged block: acc[i][j] chains over l ascending.
+__device__ __forceinline__ void mma_block(const float (*as)[TM + PAD], const float (*bs)[TN + PAD],
+                                          int ty, int tx, float (&acc)[8][8]) {
+#pragma unroll
+    for (int l = 0; l < TK; ++l) {
+        float a[8], b[8];
+        const float4 a0 = *reinterpret_cast<const float4*>(&as[l][ty * 4]);
+        const float4 a1 = *reinterpret_cast<const float4*>(&as[l][64 + ty * 4]);
+        const float4 b0 = *reinterpret_cast<const float4*>(&bs[l][tx * 4]);
+        const float4 b1 = *reinterpret_cast<const float4*>(&bs[l][64 + tx * 4]);
+        a[0] = a0.x; a[1] = a0.y; a[2] = a0.z; a[3] = a0.w;
+        a[4] = a1.x; a[5] = a1.y; a[6] = a1.z; a[7] = a1.w;
+        b[0] = b0.x; b[1] = b0.y; b[2] = b0.z; b[3] = b0.w;
+        b[4] = b1.x; b[5] = b1.y; b[6] = b1.z; b[7] = b1.w;
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+#pragma unroll
+            for (int j = 0; j < 8; ++j) acc[i][j] = __fmaf_rn(a[i], b[j], acc[i][j]);
+    }
+}
+
+__device__ __forceinline__ int mrow(int ty, int i) { return i < 4 ? ty * 4 + i : 64 + ty * 4 + (i - 4); }
+
+// ------------------------------------------------------------------ rows kernels
+
+struct RowsArgs {
+    void* out;
+    const void* a;      // [R or M, L], contraction contiguous
+    const void* b;      // [L, C] or [C, L] (per expert when grouped)
+    const void* bias;   // [C] or null
+    int64_t R, L, C;
+    int64_t E;
+    const uint32_t* seg;
+    const uint32_t* perm;
+};
+
+// out[r, c] = down( chain_l a[r, l] * b(l, c) (+ bias[c]) )
+template <typename T, bool BT, bool GROUPED, bool VEC>
+__global__ void __launch_bounds__(NT) scalar_rows_kernel(const RowsArgs p) {
+    __shared__ __align__(16) Smem sm;
+    const int tid = threadIdx.x, ty = tid / 16, tx = tid % 16;
+    const T* A = static_cast<const T*>(p.a);
+    const T* B = static_cast<const T*>(p.b);
+    const int64_t L = p.L, C = p.C;
+    const int64_t c0 = static_cast<int64_t>(blockIdx.y) * TN;
+
+    // rows of this tile: r0 + i (dense) or sorted positions of one expert
+    int64_t r0 = static_cast<int64_t>(blockIdx.x) * TM;
+    int64_t rvalid = p.R - r0;
+    uint32_t sbase = 0;
+    if (GROUPED) {
+        int64_t t = blockIdx.x;
+        int g = 0;
+        bool found = false;
+        for (; g < p.E; ++g) {
+            const int64_t cnt = p.seg[g + 1] - p.seg[g];
+            const int64_t tiles = (cnt + TM - 1) / TM;
+            if (t < tiles) { found = true; break; }
+            t -= tiles;
+        }
+        if (!found) return;
+        const int64_t cnt = p.seg[g + 1] - p.seg[g];
+        sbase = p.seg[g] + static_cast<uint32_t>(t * TM);
+        rvalid = cnt - t * TM;
+        B += static_cast<int64_t>(g) * C * L;
+    }
+    if (rvalid > TM) rvalid = TM;
+
+    // global -> register staging of one TK block
+    const int a_row = tid / 2, a_seg = (tid % 2) * 8;          // A: 128 rows x 16 steps
+    int64_t a_src_row = -1;
+    if (a_row < rvalid) a_src_row = GROUPED ? static_cast<int64_t>(p.perm[sbase + a_row]) : r0 + a_row;
+    float ra[8], rb[8];
+    auto load_a = [&](int64_t l0) {
+        const int64_t l = l0 + a_seg;
+        const int avail = a_src_row < 0 ? 0 : static_cast<int>(lmin(8, lmax(0, L - l)));
+        load8<T, VEC>(A + (a_src_row < 0 ? 0 : a_src_row * L + l), avail, ra);
+    };
+    auto load_b = [&](int64_t l0) {
+        if (BT) {  // b(l, c) = B[c * L + l]: 128 cols x 16 steps
+            const int c = tid / 2, s = (tid % 2) * 8;
+            const int64_t gc = c0 + c, l = l0 + s;
+            const int avail = gc < C ? static_cast<int>(lmin(8, lmax(0, L - l))) : 0;
+            load8<T, VEC>(B + (avail ? gc * L + l : 0), avail, rb);
+        } else {   // b(l, c) = B[l * C + c]: 16 steps x 128 cols
+            const int l = tid / 16, s = (tid % 16) * 8;
+            const int64_t gl = l0 + l, gc = c0 + s;
+            const int avail = gl < L ? static_cast<int>(lmin(8, lmax(0, C - gc))) : 0;
+            load8<T, VEC>(B + (avail ? gl * C + gc : 0), avail, rb);
+        }
+    };
+    auto store = [&](int buf) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) sm.a[buf][a_seg + i][a_row] = ra[i];
+        if (BT) {
+            const int c = tid / 2, s = (tid % 2) * 8;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) sm.b[buf][s + i][c] = rb[i];
+        } else {
+            const int l = tid / 16, s = (tid % 16) * 8;
+            *reinterpret_cast<float4*>(&sm.b[buf][l][s]) = make_float4(rb[0], rb[1], rb[2], rb[3]);
+            *reinterpret_cast<float4*>(&sm.b[buf][l][s + 4]) = make_float4(rb[4], rb[5], rb[6], rb[7]);
+        }
+    };
+
+    float acc[8][8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc[i][j] = 0.0f;
+
+    const int64_t nkb = (L + TK - 1) / TK;
+    load_a(0); load_b(0); store(0);
+    __syncthreads();
+    int buf = 0;
+    for (int64_t kb = 0; kb < nkb; ++kb) {
+        const bool more = kb + 1 < nkb;
+        if (more) { load_a((kb + 1) * TK); load_b((kb + 1) * TK); }
+        mma_block(sm.a[buf], sm.b[buf], ty, tx, acc);
+        if (more) store(buf ^ 1);
+        __syncthreads();
+        buf ^= 1;
+    }
+
+    // epilogue: (+ bias), one rounding, store
+    T* out = static_cast<T*>(p.out);
+    const T* bias = static_cast<const T*>(p.bias);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int lr = mrow(ty, i);
+        if (lr >= rvalid) continue;
+        const int64_t orow = GROUPED ? static_cast<int64_t>(p.perm[sbase + lr]) : r0 + lr;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const int64_t c = c0 + mrow(tx, j);
+            if (c >= C) continue;
+            float v = acc[i][j];
+            if (bias) v = v + Elem<T>::up(bias[c]);
+            out[orow * C + c] = Elem<T>::down(v);
+        }
+    }
+}
+
+// ------------------------------------------------------------------ dW kernels
+
+struct DwArgs {
+    void* out;          // final output (direct mode) [R, C]
+    int out_f32;
+    float* partials;    // [chunks, R, C] or null for direct mode
+    const void* a;      // [M, R] (row-major over m, r contiguous)
+    const void* b;      // [M, C]
+    int64_t M, R, C;
+    int64_t E;
+    const uint32_t* seg;
+    const uint32_t* perm;
+};
+
+// partial[z][r][c] = chain over the rows of chunk z of a[m, r] * b[m, c]
+template <typename T, bool GROUPED, bool VEC>
+__global__ void __launch_bounds__(NT) scalar_dw_chunk_kernel(const DwArgs p) {
+    __shared__ __align__(16) Smem sm;
+    const int tid = threadIdx.x, ty = tid / 16, tx = tid % 16;
+    const T* A = static_cast<const T*>(p.a);
+    const T* Bm = static_cast<const T*>(p.b);
+    const int64_t R = p.R, C = p.C;
+    const int64_t r0 = static_cast<int64_t>(blockIdx.y) * TM;
+    const int64_t c0 = static_cast<int64_t>(blockIdx.x) * TN;
+    const int64_t z = blockIdx.z;
+
+    // rows of this chunk: positions [pos0, pos0 + cnt) (dense: rows; grouped: sorted positions)
+    int64_t pos0, cnt;
+    if (GROUPED) {
+        int64_t t = z;
+        int g = 0;
+        bool found = false;
+        for (; g < p.E; ++g) {
+            const int64_t n_g = p.seg[g + 1] - p.seg[g];
+            const int64_t j_g = (n_g + BI_DW_CHUNK - 1) / BI_DW_CHUNK;
+            if (t < j_g) { found = true; break; }
+            t -= j_g;
+        }
+        if (!found) return;
+        const int64_t n_g = p.seg[g + 1] - p.seg[g];
+        pos0 = p.seg[g] + t * BI_DW_CHUNK;
+        cnt = lmin(BI_DW_CHUNK, n_g - t * BI_DW_CHUNK);
+    } else {
+        pos0 = z * BI_DW_CHUNK;
+        cnt = lmin(BI_DW_CHUNK, p.M - pos0);
+    }
+
+    // both operands are [rows, out] with out contiguous: 16 rows x 128 outs each
+    const int l_ld = tid / 16, s_ld = (tid % 16) * 8;
+    float ra[8], rb[8];
+    auto load = [&](int64_t l0) {
+        const int64_t l = l0 + l_ld;
+        int64_t row = -1;
+        if (l < cnt) row = GROUPED ? static_cast<int64_t>(p.perm[pos0 + l]) : pos0 + l;
+        const int av_a = row < 0 ? 0 : static_cast<int>(lmin(8, lmax(0, R - (r0 + s_ld))));
+        const int av_b = row < 0 ? 0 : static_cast<int>(lmin(8, lmax(0, C - (c0 + s_ld))));
+        load8<T, VEC>(A + (av_a ? row * R + r0 + s_ld : 0), av_a, ra);
+        load8<T, VEC>(Bm + (av_b ? row * C + c0 + s_ld : 0), av_b, rb);
+    };
+    auto store = [&](int buf) {
+        *reinterpret_cast<float4*>(&sm.a[buf][l_ld][s_ld]) = make_float4(ra[0], ra[1], ra[2], ra[3]);
+        *reinterpret_cast<float4*>(&sm.a[buf][l_ld][s_ld + 4]) = make_float4(ra[4], ra[5], ra[6], ra[7]);
+        *reinterpret_cast<float4*>(&sm.b[buf][l_ld][s_ld]) = make_float4(rb[0], rb[1], rb[2], rb[3]);
+        *reinterpret_cast<float4*>(&sm.b[buf][l_ld][s_ld + 4]) = make_float4(rb[4], rb[5], rb[6], rb[7]);
+    };
+
+    float acc[8][8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc[i][j] = 0.0f;
+
+    const int64_t nkb = (cnt + TK - 1) / TK;
+    if (nkb > 0) {
+        load(0); store(0);
+        __syncthreads();
+        int buf = 0;
+        for (int64_t kb = 0; kb < nkb; ++kb) {
+            const bool more = kb + 1 < nkb;
+            if (more) load((kb + 1) * TK);
+            mma_block(sm.a[buf], sm.b[buf], ty, tx, acc);
+            if (more) store(buf ^ 1);
+            __syncthreads();
+            buf ^= 1;
+        }
+    }
+
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int64_t r = r0 + mrow(ty, i);
+        if (r >= R) continue;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const int64_t c = c0 + mrow(tx, j);
+            if (c >= C) continue;
+            if (p.partials) {
+                p.partials[(z * R + r) * C + c] = acc[i][j];
+            } else if (p.out_f32) {
+                static_cast<float*>(p.out)[r * C + c] = acc[i][j];
+            } else {
+                static_cast<T*>(p.out)[r * C + c] = Elem<T>::down(acc[i][j]);
+            }
+        }
+    }
+}
+
+// The fixed tree over J chunk partials of one output, as a binary counter:
+// after chunk j the counter merges the two newest entries once per trailing
+// zero bit of j+1 (pairs of equal, aligned blocks), and at the end folds the
+// remaining entries from the newest down.  Same pairs, same operands as the
+// level-by-level pairwise tree with the odd last entry carried.
+__device__ __forceinline__ float tree_from(const float* part, int64_t stride, int64_t J) {
+    float st[32];
+    int sp = 0;
+    for (int64_t j = 0; j < J; ++j) {
+        st[sp++] = part[j * stride];
+        for (uint64_t c = static_cast<uint64_t>(j) + 1; (c & 1u) == 0; c >>= 1) {
+            st[sp - 2] = st[sp - 2] + st[sp - 1];
+            --sp;
+        }
+    }
+    float v = sp ? st[sp - 1] : 0.0f;
+    for (int i = sp - 2; i >= 0; --i) v = st[i] + v;
+    return v;
+}
+
+template <typename T>
+__global__ void dw_tree_kernel(const float* partials, int64_t RC, int64_t J, void* out, int out_f32) {
+    for (int64_t e = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; e < RC;
+         e += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const float v = tree_from(partials + e, RC, J);
+        if (out_f32) static_cast<float*>(out)[e] = v;
+        else static_cast<T*>(out)[e] = Elem<T>::down(v);
+    }
+}
+
+// grouped: blockIdx.y = expert; chunk range of expert g follows experts 0..g-1
+__global__ void dw_tree_grouped_kernel(const float* partials, int64_t RC, const uint32_t* seg,
+                                       float* out) {
+    const int g = blockIdx.y;
+    int64_t cstart = 0;
+    for (int q = 0; q < g; ++q) cstart += (static_cast<int64_t>(seg[q + 1] - seg[q]) + BI_DW_CHUNK - 1) / BI_DW_CHUNK;
+    const int64_t J = (static_cast<int64_t>(seg[g + 1] - seg[g]) + BI_DW_CHUNK - 1) / BI_DW_CHUNK;
+    for (int64_t e = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; e < RC;
+         e += static_cast<int64_t>(gridDim.x) * blockDim.x)
+        out[g * RC + e] = tree_from(partials + cstart * RC + e, RC, J);
+}
+
+// ------------------------------------------------------------------ host helpers
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+template <typename T, bool BT, bool G>
+cudaError_t rows_t(const LaunchCtx& c, const RowsArgs& a, int64_t row_tiles) {
+    // 8-element loads need rows of whole 16-byte units and aligned bases
+    const int64_t unit = 16 / sizeof(T);
+    bool vec = aligned16(a.a) && aligned16(a.b) && a.L % unit == 0 && (BT || a.C % unit == 0);
+    if (sizeof(T) == 4) vec = vec && a.L % 4 == 0 && (BT || a.C % 4 == 0);
+    dim3 grid(static_cast<unsigned>(row_tiles), static_cast<unsigned>((a.C + TN - 1) / TN));
+    if (vec) scalar_rows_kernel<T, BT, G, true><<<grid, NT, 0, c.stream>>>(a);
+    else scalar_rows_kernel<T, BT, G, false><<<grid, NT, 0, c.stream>>>(a);
+    c.count();
+    return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t rows_dispatch(const LaunchCtx& c, const RowsArgs& a, int bt, bool grouped, int64_t tiles) {
+    if (grouped) return bt ? rows_t<T, true, true>(c, a, tiles) : rows_t<T, false, true>(c, a, tiles);
+    return bt ? rows_t<T, true, false>(c, a, tiles) : rows_t<T, false, false>(c, a, tiles);
+}
+
+template <typename T, bool G>
+cudaError_t dw_chunks_t(const LaunchCtx& c, const DwArgs& a, int64_t chunks) {
+    const int64_t unit = 16 / sizeof(T);
+    const bool vec = aligned16(a.a) && aligned16(a.b) && a.R % unit == 0 && a.C % unit == 0;
+    dim3 grid(static_cast<unsigned>((a.C + TN - 1) / TN), static_cast<unsigned>((a.R + TM - 1) / TM),
+              static_cast<unsigned>(chunks));
+    if (vec) scalar_dw_chunk_kernel<T, G, true><<<grid, NT, 0, c.stream>>>(a);
+    else scalar_dw_chunk_kernel<T, G, false><<<grid, NT, 0, c.stream>>>(a);
+    c.count();
+    return cudaGetLastError();
+}
+
+unsigned tree_grid(int64_t n, int sm) {
+    int64_t b = (n + 255) / 256;
+    const int64_t cap = static_cast<int64_t>(sm) * 8;
+    return static_cast<unsigned>(b < cap ? (b > 0 ? b : 1) : cap);
+}
+
+}  // namespace
+
+cudaError_t scalar_rows(const LaunchCtx& c, bi_dtype dt, void* out, const void* a, const void* b,
+                        const void* bias, int64_t R, int64_t L, int64_t C, int b_contr_contig) {
+    RowsArgs args{out, a, b, bias, R, L, C, 0, nullptr, nullptr};
+    const int64_t tiles = (R + TM - 1) / TM;
+    switch (dt) {
+        case BI_F32: return rows_dispatch<float>(c, args, b_contr_contig, false, tiles);
+        case BI_BF16: return rows_dispatch<__nv_bfloat16>(c, args, b_contr_contig, false, tiles);
+        default: return rows_dispatch<__half>(c, args, b_contr_contig, false, tiles);
+    }
+}
+
+cudaError_t scalar_rows_grouped(const LaunchCtx& c, bi_dtype dt, void* out, const void* a,
+                                const void* b, int64_t M, int64_t L, int64_t C, int64_t E,
+                                int b_contr_contig, const uint32_t* seg, const uint32_t* perm) {
+    RowsArgs args{out, a, b, nullptr, M, L, C, E, seg, perm};
+    const int64_t tiles = (M + TM - 1) / TM + E;  // upper bound over per-expert tiles
+    switch (dt) {
+        case BI_F32: return rows_dispatch<float>(c, args, b_contr_contig, true, tiles);
+        case BI_BF16: return rows_dispatch<__nv_bfloat16>(c, args, b_contr_contig, true, tiles);
+        default: return rows_dispatch<__half>(c, args, b_contr_contig, true, tiles);
+    }
+}
+
+cudaError_t scalar_dw(const LaunchCtx& c, bi_dtype dt, void* out, int out_f32, const void* a,
+                      const void* b, int64_t M, int64_t R, int64_t C, float* partials) {
+    const int64_t J = (M + BI_DW_CHUNK - 1) / BI_DW_CHUNK;
+    DwArgs args{out, out_f32, J > 1 ? partials : nullptr, a, b, M, R, C, 0, nullptr, nullptr};
+    cudaError_t e;
+    switch (dt) {
+        case BI_F32: e = dw_chunks_t<float, false>(c, args, J); break;
+        case BI_BF16: e = dw_chunks_t<__nv_bfloat16, false>(c, args, J); break;
+        default: e = dw_chunks_t<__half, false>(c, args, J); break;
+    }
+    if (e != cudaSuccess || J <= 1) return e;
+    const int64_t RC = R * C;
+    const unsigned grid = tree_grid(RC, c.sm_count);
+    switch (dt) {
+        case BI_F32: dw_tree_kernel<float><<<grid, 256, 0, c.stream>>>(partials, RC, J, out, out_f32); break;
+        case BI_BF16: dw_tree_kernel<__nv_bfloat16><<<grid, 256, 0, c.stream>>>(partials, RC, J, out, out_f32); break;
+        default: dw_tree_kernel<__half><<<grid, 256, 0, c.stream>>>(partials, RC, J, out, out_f32); break;
+    }
+    c.count();
+    return cudaGetLastError();
+}
+
+cudaError_t scalar_dw_grouped(const LaunchCtx& c, bi_dtype dt, float* out, const void* a,
+                              const void* b, int64_t M, int64_t R, int64_t C, int64_t E,
+                              const uint32_t* seg, const uint32_t* perm, float* partials,
+                              int64_t max_chunks) {
+    DwArgs args{out, 1, partials, a, b, M, R, C, E, seg, perm};
+    cudaError_t e;
+    if (max_chunks > 0) {
+        switch (dt) {
+            case BI_F32: e = dw_chunks_t<float, true>(c, args, max_chunks); break;
+            case BI_BF16: e = dw_chunks_t<__nv_bfloat16, true>(c, args, max_chunks); break;
+            default: e = dw_chunks_t<__half, true>(c, args, max_chunks); break;
+        }
+        if (e != cudaSuccess) return e;
+    }
+    const int64_t RC = R * C;
+    dim3 grid(tree_grid(RC, c.sm_count) / (E > 8 ? 8 : 1) + 1, static_cast<unsigned>(E));
+    dw_tree_grouped_kernel<<<grid, 256, 0, c.stream>>>(partials, RC, seg, out);
+    c.count();
+    return cudaGetLastError();
+}
+
+}  // namespace bi

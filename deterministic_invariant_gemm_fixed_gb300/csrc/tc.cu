@@ -1,0 +1,715 @@
+// Tensor-core tier: one persistent, warp-specialised tcgen05 GEMM kernel for sm_103a.
+//
+// Contract (sgemm-bi 0.1.1.post2, "Determinism contracts", row "tensor cores"):
+// f32 accumulation, bit-identical across runs, each output row independent of M.
+// The kernel keeps every arithmetic choice fixed by (pass, dtype, K, N):
+//   - one MMA shape, M128 x N256 x K16 (tcgen05.mma.cta_group::1.kind::f16),
+//     f32 accumulator in tensor memory;
+//   - the contracted index is walked in 64-wide blocks in ascending order, four
+//     K16 instructions per block, accumulating into the same TMEM tile;
+//   - no split of the contraction, no atomics, no stream-K;
+//   - M only decides how many tiles exist and which CTA runs which tile, which
+//     cannot change the arithmetic of any output element.
+//
+// Roles (192 threads):
+//   warp 0 lane 0  TMA producer: cp.async.bulk.tensor loads into a 4-stage ring
+//   warp 1 lane 0  MMA issuer (warp 1 also owns the TMEM allocation)
+//   warps 2..5     epilogue: tcgen05.ld -> (+bias) -> one rounding -> st.global
+// The accumulator is double-buffered (2 x 256 TMEM columns) so the epilogue of
+// one tile overlaps the main loop of the next.  Every mbarrier wait is bounded
+// by a %globaltimer limit; on expiry the kernel records a status code, stops all
+// roles, drains its own copies and MMAs, frees TMEM and returns.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "bi_internal.h"
+
+namespace bi {
+namespace {
+
+constexpr int BM = 128;        // tile rows = MMA M
+constexpr int BN = 256;        // tile cols = MMA N
+constexpr int BK = 64;         // contraction block = one 128-byte swizzle row of 16-bit data
+constexpr int UK = 16;         // contraction per MMA instruction
+constexpr int STAGES = 4;
+constexpr int A_BYTES = BM * BK * 2;
+constexpr int B_BYTES = BN * BK * 2;
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int THREADS = 192;
+constexpr int TMEM_COLS = 2 * BN;
+constexpr int BAR_BYTES = 256;
+constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + BAR_BYTES;
+constexpr int GROUP_M = 16;    // raster: 16 row-tiles share the column sweep (L2 reuse)
+
+enum Mode { DENSE = 0, GROUPED_ROWS = 1, GROUPED_DW = 2 };
+
+struct Params {
+    void* out;
+    int64_t ldo;             // row stride of out, elements
+    int64_t rows, cols;      // output extent of one problem (for masking)
+    const void* bias;        // dense forward only (nullable)
+    int num_m, num_n, num_kb;
+    const uint32_t* seg;     // grouped: segment table
+    const uint32_t* perm;    // grouped rows: sorted position -> original row
+    int E;
+    int* status;
+    unsigned long long wait_limit;
+};
+
+// ---------------------------------------------------------------- PTX helpers
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ unsigned long long globaltimer() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.b32 %0, 1, 0, p;\n\t}\n"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Bounded wait.  Returns false if this CTA is aborting or the limit ran out
+// (then the status word is written and the CTA-wide abort flag raised).
+__device__ __noinline__ bool mbar_wait_impl(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                            int* status, unsigned long long limit, int code) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const unsigned long long t0 = globaltimer();
+    for (uint32_t i = 1;; ++i) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((i & 15u) == 0) {
+            if (*abort_flag) return false;
+            if (globaltimer() - t0 > limit) {
+                *abort_flag = 1;
+                if (status) *reinterpret_cast<volatile int*>(status) = code;
+                return false;
+            }
+        }
+    }
+}
+#define mbar_wait(bar, parity, abort_flag, p, code) \
+    mbar_wait_impl((bar), (parity), (abort_flag), (p).status, (p).wait_limit, (code))
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y,
+                                            uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int x, int y,
+                                            int z, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor (tcgen05 format): start address, leading and
+// stride byte offsets (>> 4), version 1 at bit 46, 128-byte swizzle (2) at bit 61.
+__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+    d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;
+    d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
+    d |= 1ull << 46;
+    d |= 2ull << 61;
+    return d;
+}
+
+// Instruction descriptor for kind::f16: D f32 (bit 4), A/B format (bits 7, 10),
+// A/B major (bits 15, 16: 1 = MN-major), N >> 3 (bits 17..22), M >> 4 (bits 24..28).
+template <int FMT, bool A_MN, bool B_MN>
+__device__ __forceinline__ constexpr uint32_t instr_desc() {
+    return (1u << 4) | (static_cast<uint32_t>(FMT) << 7) | (static_cast<uint32_t>(FMT) << 10) |
+           (static_cast<uint32_t>(A_MN) << 15) | (static_cast<uint32_t>(B_MN) << 16) |
+           (static_cast<uint32_t>(BN >> 3) << 17) | (static_cast<uint32_t>(BM >> 4) << 24);
+}
+
+__device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                        uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&v)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32"
+        " {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+        : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
+          "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]),
+          "=r"(v[13]), "=r"(v[14]), "=r"(v[15])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// ---------------------------------------------------------------- output types
+
+template <int FMT> struct OutT;
+template <> struct OutT<0> {
+    using T = __half;
+    static __device__ __forceinline__ uint32_t pack(float a, float b) {
+        __half2 h = __floats2half2_rn(a, b);
+        return *reinterpret_cast<uint32_t*>(&h);
+    }
+    static __device__ __forceinline__ float load(const void* p, int64_t i) {
+        return __half2float(reinterpret_cast<const __half*>(p)[i]);
+    }
+    static __device__ __forceinline__ void store1(void* p, int64_t i, float v) {
+        reinterpret_cast<__half*>(p)[i] = __float2half_rn(v);
+    }
+};
+template <> struct OutT<1> {
+    using T = __nv_bfloat16;
+    static __device__ __forceinline__ uint32_t pack(float a, float b) {
+        __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+        return *reinterpret_cast<uint32_t*>(&h);
+    }
+    static __device__ __forceinline__ float load(const void* p, int64_t i) {
+        return __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(p)[i]);
+    }
+    static __device__ __forceinline__ void store1(void* p, int64_t i, float v) {
+        reinterpret_cast<__nv_bfloat16*>(p)[i] = __float2bfloat16_rn(v);
+    }
+};
+
+// ---------------------------------------------------------------- tile schedule
+
+struct Tile {
+    int m_blk, n_blk, g, nkb;
+    int row0;       // grouped: first padded row of the A tile / of the expert
+    int valid;      // grouped rows: rows of this tile that belong to the expert
+    uint32_t sbase; // grouped rows: sorted position of the tile's first row
+};
+
+template <int MODE>
+__device__ __forceinline__ bool get_tile(const Params& p, int t, Tile& ti) {
+    if (MODE == DENSE) {
+        const int total = p.num_m * p.num_n;
+        if (t >= total) return false;
+        const int span = GROUP_M * p.num_n;
+        const int grp = t / span;
+        const int first_m = grp * GROUP_M;
+        const int gsize = min(p.num_m - first_m, GROUP_M);
+        const int r = t - grp * span;
+        ti.m_blk = first_m + r % gsize;
+        ti.n_blk = r / gsize;
+        ti.g = 0;
+        ti.nkb = p.num_kb;
+        ti.row0 = ti.m_blk * BM;
+        ti.valid = BM;
+        ti.sbase = 0;
+        return true;
+    } else if (MODE == GROUPED_ROWS) {
+        const uint32_t* off = p.seg;
+        const uint32_t* pst = p.seg + p.E + 2;
+        for (int g = 0; g < p.E; ++g) {
+            const int cnt = static_cast<int>(off[g + 1] - off[g]);
+            const int mt = (cnt + BM - 1) / BM;
+            const int tiles = mt * p.num_n;
+            if (t < tiles) {
+                ti.m_blk = t / p.num_n;
+                ti.n_blk = t % p.num_n;
+                ti.g = g;
+                ti.nkb = p.num_kb;
+                ti.row0 = static_cast<int>(pst[g]) + ti.m_blk * BM;
+                ti.valid = min(BM, cnt - ti.m_blk * BM);
+                ti.sbase = off[g] + static_cast<uint32_t>(ti.m_blk * BM);
+                return true;
+            }
+            t -= tiles;
+        }
+        return false;
+    } else {
+        const int per = p.num_m * p.num_n;
+        const int g = t / per;
+        if (g >= p.E) return false;
+        const int r = t - g * per;
+        const uint32_t* off = p.seg;
+        const uint32_t* pst = p.seg + p.E + 2;
+        const int cnt = static_cast<int>(off[g + 1] - off[g]);
+        ti.m_blk = r / p.num_n;
+        ti.n_blk = r % p.num_n;
+        ti.g = g;
+        ti.nkb = 2 * ((cnt + BM - 1) / BM);  // padded rows / BK
+        ti.row0 = static_cast<int>(pst[g]);
+        ti.valid = BM;
+        ti.sbase = 0;
+        return true;
+    }
+}
+
+// ---------------------------------------------------------------- the kernel
+
+template <int FMT, bool A_MN, bool B_MN, bool B3D, int MODE, bool OUT_F32>
+__global__ void __launch_bounds__(THREADS, 1)
+    tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   const Params p) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    uint8_t* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
+    const uint32_t sbase = smem_u32(smem);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
+    const uint32_t bar0 = smem_u32(bars);
+    auto full_bar = [&](int s) { return bar0 + 8u * s; };
+    auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
+    auto tfull_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + b); };
+    auto tempty_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + 2 + b); };
+    const uint32_t drain_bar = bar0 + 8u * (2 * STAGES + 4);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 5);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(full_bar(s), 1);
+            mbar_init(empty_bar(s), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(tfull_bar(b), 1);
+            mbar_init(tempty_bar(b), 4);  // one arrival per epilogue warp
+        }
+        mbar_init(drain_bar, 1);
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         smem_u32(tmem_slot)),
+                     "r"(TMEM_COLS)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
+
+    if (warp == 0 && lane == 0) {
+        // ------------------------------------------------------------ producer
+        int s = 0;
+        uint32_t ph = 0;
+        uint32_t used = 0, last_par = 0;  // per stage: ever issued / parity of the last issue
+        Tile ti;
+        for (int t = blockIdx.x; get_tile<MODE>(p, t, ti); t += gridDim.x) {
+            if (ti.nkb == 0) continue;
+            for (int kb = 0; kb < ti.nkb; ++kb) {
+                if (!mbar_wait(empty_bar(s), ph ^ 1u, abort_flag, p, DEV_TIMEOUT_PRODUCER)) goto drain;
+                const uint32_t fb = full_bar(s);
+                mbar_expect_tx(fb, STAGE_BYTES);
+                const uint32_t a_dst = sbase + s * STAGE_BYTES;
+                const uint32_t b_dst = a_dst + A_BYTES;
+                const int kofs = kb * BK;
+                // A operand
+                if (MODE == GROUPED_DW) {
+                    // dY rows of the expert, MN-major: out index n contiguous
+                    for (int a = 0; a < BM / 64; ++a)
+                        tma_load_2d(a_dst + a * (BK * 128), &tmA, ti.m_blk * BM + a * 64,
+                                    ti.row0 + kofs, fb);
+                } else if (A_MN) {
+                    for (int a = 0; a < BM / 64; ++a)
+                        tma_load_2d(a_dst + a * (BK * 128), &tmA, ti.m_blk * BM + a * 64, kofs, fb);
+                } else {
+                    tma_load_2d(a_dst, &tmA, kofs, ti.row0, fb);
+                }
+                // B operand
+                if (MODE == GROUPED_DW) {
+                    for (int b = 0; b < BN / 64; ++b)
+                        tma_load_2d(b_dst + b * (BK * 128), &tmB, ti.n_blk * BN + b * 64,
+                                    ti.row0 + kofs, fb);
+                } else if (B3D) {
+                    if (B_MN) {
+                        for (int b = 0; b < BN / 64; ++b)
+                            tma_load_3d(b_dst + b * (BK * 128), &tmB, ti.n_blk * BN + b * 64, kofs,
+                                        ti.g, fb);
+                    } else {
+                        tma_load_3d(b_dst, &tmB, kofs, ti.n_blk * BN, ti.g, fb);
+                    }
+                } else if (B_MN) {
+                    for (int b = 0; b < BN / 64; ++b)
+                        tma_load_2d(b_dst + b * (BK * 128), &tmB, ti.n_blk * BN + b * 64, kofs, fb);
+                } else {
+                    tma_load_2d(b_dst, &tmB, kofs, ti.n_blk * BN, fb);
+                }
+                used |= 1u << s;
+                last_par = (last_par & ~(1u << s)) | (ph << s);
+                if (++s == STAGES) { s = 0; ph ^= 1u; }
+            }
+        }
+    drain:
+        // make sure no copy into this CTA's shared memory is still in flight
+        for (int q = 0; q < STAGES; ++q)
+            if (used & (1u << q))
+                mbar_wait(full_bar(q), (last_par >> q) & 1u, abort_flag, p, DEV_TIMEOUT_PRODUCER);
+    } else if (warp == 1 && lane == 0) {
+        // ------------------------------------------------------------ MMA issuer
+        constexpr uint32_t idesc = instr_desc<FMT, A_MN || MODE == GROUPED_DW,
+                                              B_MN || MODE == GROUPED_DW>();
+        constexpr bool AM = A_MN || MODE == GROUPED_DW;
+        constexpr bool BMN = B_MN || MODE == GROUPED_DW;
+        int s = 0;
+        uint32_t ph = 0;
+        int ab = 0;
+        uint32_t aph = 0;
+        Tile ti;
+        for (int t = blockIdx.x; get_tile<MODE>(p, t, ti); t += gridDim.x) {
+            if (ti.nkb == 0) continue;
+            if (!mbar_wait(tempty_bar(ab), aph ^ 1u, abort_flag, p, DEV_TIMEOUT_MMA)) break;
+            tc_fence_after();
+            const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(ab * BN);
+            bool ok = true;
+            for (int kb = 0; kb < ti.nkb; ++kb) {
+                if (!mbar_wait(full_bar(s), ph, abort_flag, p, DEV_TIMEOUT_MMA)) { ok = false; break; }
+                tc_fence_after();
+                const uint32_t a_s = sbase + s * STAGE_BYTES;
+                const uint32_t b_s = a_s + A_BYTES;
+#pragma unroll
+                for (int kk = 0; kk < BK / UK; ++kk) {
+                    // K-major: step 32 bytes along the swizzled 128-byte row;
+                    // MN-major: step 16 rows = 2048 bytes (2 swizzle atoms of 8 rows).
+                    const uint64_t ad = AM ? smem_desc(a_s + kk * 2048, BK * 128, 1024)
+                                           : smem_desc(a_s + kk * 32, 16, 1024);
+                    const uint64_t bd = BMN ? smem_desc(b_s + kk * 2048, BK * 128, 1024)
+                                            : smem_desc(b_s + kk * 32, 16, 1024);
+                    mma_f16(d_tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+                }
+                mma_commit(empty_bar(s));  // frees the stage once these MMAs have read it
+                if (++s == STAGES) { s = 0; ph ^= 1u; }
+            }
+            if (!ok) break;
+            mma_commit(tfull_bar(ab));
+            if (++ab == 2) { ab = 0; aph ^= 1u; }
+        }
+        // wait for every MMA this thread issued before TMEM can be released
+        mma_commit(drain_bar);
+        mbar_wait(drain_bar, 0, abort_flag, p, DEV_TIMEOUT_MMA);
+    } else if (warp >= 2) {
+        // ------------------------------------------------------------ epilogue
+        const int q = warp & 3;              // TMEM lane quarter this warp may access
+        const int r = q * 32 + lane;         // tile row owned by this thread
+        int ab = 0;
+        uint32_t aph = 0;
+        Tile ti;
+        for (int t = blockIdx.x; get_tile<MODE>(p, t, ti); t += gridDim.x) {
+            // output row of this thread (or -1)
+            int64_t orow = -1;
+            void* out = p.out;
+            if (MODE == DENSE) {
+                const int64_t gr = static_cast<int64_t>(ti.m_blk) * BM + r;
+                if (gr < p.rows) orow = gr;
+            } else if (MODE == GROUPED_ROWS) {
+                if (r < ti.valid) orow = p.perm[ti.sbase + r];
+            } else {
+                const int64_t gr = static_cast<int64_t>(ti.m_blk) * BM + r;
+                if (gr < p.rows) orow = gr;
+                out = static_cast<float*>(p.out) + static_cast<int64_t>(ti.g) * p.rows * p.ldo;
+            }
+            const int64_t col0 = static_cast<int64_t>(ti.n_blk) * BN;
+            if (ti.nkb == 0) {  // empty expert: +0 everywhere, no accumulator involved
+                if (orow >= 0)
+                    for (int64_t c = col0; c < col0 + BN && c < p.cols; ++c)
+                        static_cast<float*>(out)[orow * p.ldo + c] = 0.0f;
+                continue;
+            }
+            bool ok = mbar_wait(tfull_bar(ab), aph, abort_flag, p, DEV_TIMEOUT_EPILOGUE);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) break;
+            tc_fence_after();
+            const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
+                                   static_cast<uint32_t>(ab * BN);
+            for (int c0 = 0; c0 < BN; c0 += 16) {
+                if (col0 + c0 >= p.cols) break;  // uniform across the warp
+                uint32_t v[16];
+                tmem_ld16(tbase + c0, v);
+                if (orow < 0) continue;
+                float f[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) f[i] = __uint_as_float(v[i]);
+                const int64_t cb = col0 + c0;
+                if (MODE == DENSE && p.bias != nullptr) {
+#pragma unroll
+                    for (int i = 0; i < 16; ++i)
+                        if (cb + i < p.cols) f[i] = f[i] + OutT<FMT>::load(p.bias, cb + i);
+                }
+                const bool full = cb + 16 <= p.cols;
+                if (OUT_F32) {
+                    float* dst = static_cast<float*>(out) + orow * p.ldo + cb;
+                    if (full) {
+#pragma unroll
+                        for (int i = 0; i < 16; i += 4)
+                            *reinterpret_cast<float4*>(dst + i) = make_float4(f[i], f[i + 1], f[i + 2], f[i + 3]);
+                    } else {
+                        for (int i = 0; i < 16; ++i)
+                            if (cb + i < p.cols) dst[i] = f[i];
+                    }
+                } else {
+                    using T = typename OutT<FMT>::T;
+                    T* dst = static_cast<T*>(out) + orow * p.ldo + cb;
+                    if (full) {
+                        uint4 w0, w1;
+                        w0.x = OutT<FMT>::pack(f[0], f[1]);
+                        w0.y = OutT<FMT>::pack(f[2], f[3]);
+                        w0.z = OutT<FMT>::pack(f[4], f[5]);
+                        w0.w = OutT<FMT>::pack(f[6], f[7]);
+                        w1.x = OutT<FMT>::pack(f[8], f[9]);
+                        w1.y = OutT<FMT>::pack(f[10], f[11]);
+                        w1.z = OutT<FMT>::pack(f[12], f[13]);
+                        w1.w = OutT<FMT>::pack(f[14], f[15]);
+                        reinterpret_cast<uint4*>(dst)[0] = w0;
+                        reinterpret_cast<uint4*>(dst)[1] = w1;
+                    } else {
+                        for (int i = 0; i < 16; ++i)
+                            if (cb + i < p.cols) OutT<FMT>::store1(dst, i, f[i]);
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(tempty_bar(ab));
+            if (++ab == 2) { ab = 0; aph ^= 1u; }
+        }
+    }
+
+    // ---------------------------------------------------------------- teardown
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
+                     "r"(TMEM_COLS)
+                     : "memory");
+    }
+}
+
+// ---------------------------------------------------------------- host side
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// 16-bit row-major tensor [outer][inner] (optionally [depth][outer][inner]),
+// box {64, box_outer(, 1)}, 128-byte swizzle, zero fill out of bounds.
+cudaError_t make_map(CUtensorMap* m, bi_dtype dt, const void* ptr, uint64_t inner, uint64_t outer,
+                     uint64_t depth, uint32_t box_outer, bool rank3 = false) {
+    auto enc = encode_fn();
+    if (!enc) return cudaErrorNotSupported;
+    const CUtensorMapDataType t =
+        dt == BI_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    cuuint64_t dims[3] = {inner, outer, depth};
+    cuuint64_t strides[2] = {inner * 2, inner * outer * 2};
+    cuuint32_t box[3] = {64, box_outer, 1};
+    cuuint32_t es[3] = {1, 1, 1};
+    const cuuint32_t rank = rank3 ? 3 : 2;
+    CUresult r = enc(m, t, rank, const_cast<void*>(ptr), dims, strides, box, es,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+template <int FMT, bool A_MN, bool B_MN, bool B3D, int MODE, bool OUT_F32>
+cudaError_t launch(const LaunchCtx& c, const CUtensorMap& a, const CUtensorMap& b, Params p,
+                   int64_t tiles_upper) {
+    auto kern = tc_gemm_kernel<FMT, A_MN, B_MN, B3D, MODE, OUT_F32>;
+    static std::once_flag once;
+    static cudaError_t attr_err = cudaSuccess;
+    std::call_once(once, [&] {
+        attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    });
+    if (attr_err != cudaSuccess) return attr_err;
+    if (tiles_upper <= 0) return cudaSuccess;
+    const int grid = static_cast<int>(tiles_upper < c.sm_count ? tiles_upper : c.sm_count);
+    p.status = c.status;
+    p.wait_limit = c.wait_limit_ns;
+    kern<<<grid, THREADS, SMEM_BYTES, c.stream>>>(a, b, p);
+    c.count();
+    return cudaGetLastError();
+}
+
+template <int FMT>
+cudaError_t forward_t(const LaunchCtx& c, bi_dtype dt, void* y, const void* x, const void* w,
+                      const void* bias, int64_t M, int64_t K, int64_t N) {
+    CUtensorMap a, b;
+    cudaError_t e;
+    if ((e = make_map(&a, dt, x, K, M, 1, BM)) != cudaSuccess) return e;   // X [M,K], K-major
+    if ((e = make_map(&b, dt, w, N, K, 1, BK)) != cudaSuccess) return e;   // W [K,N], MN-major
+    Params p{};
+    p.out = y; p.ldo = N; p.rows = M; p.cols = N; p.bias = bias;
+    p.num_m = static_cast<int>((M + BM - 1) / BM);
+    p.num_n = static_cast<int>((N + BN - 1) / BN);
+    p.num_kb = static_cast<int>((K + BK - 1) / BK);
+    return launch<FMT, false, true, false, DENSE, false>(c, a, b, p, int64_t(p.num_m) * p.num_n);
+}
+
+template <int FMT>
+cudaError_t dx_t(const LaunchCtx& c, bi_dtype dt, void* dx, const void* dy, const void* w,
+                 int64_t M, int64_t K, int64_t N) {
+    CUtensorMap a, b;
+    cudaError_t e;
+    if ((e = make_map(&a, dt, dy, N, M, 1, BM)) != cudaSuccess) return e;  // dY [M,N], K-major
+    if ((e = make_map(&b, dt, w, N, K, 1, BN)) != cudaSuccess) return e;   // W [K,N]: rows k, contraction n
+    Params p{};
+    p.out = dx; p.ldo = K; p.rows = M; p.cols = K;
+    p.num_m = static_cast<int>((M + BM - 1) / BM);
+    p.num_n = static_cast<int>((K + BN - 1) / BN);
+    p.num_kb = static_cast<int>((N + BK - 1) / BK);
+    return launch<FMT, false, false, false, DENSE, false>(c, a, b, p, int64_t(p.num_m) * p.num_n);
+}
+
+template <int FMT, bool F32>
+cudaError_t dw_t(const LaunchCtx& c, bi_dtype dt, void* dw, const void* x, const void* dy,
+                 int64_t M, int64_t K, int64_t N) {
+    CUtensorMap a, b;
+    cudaError_t e;
+    if ((e = make_map(&a, dt, x, K, M, 1, BK)) != cudaSuccess) return e;   // X [M,K]: out k, contraction m
+    if ((e = make_map(&b, dt, dy, N, M, 1, BK)) != cudaSuccess) return e;  // dY [M,N]: out n, contraction m
+    Params p{};
+    p.out = dw; p.ldo = N; p.rows = K; p.cols = N;
+    p.num_m = static_cast<int>((K + BM - 1) / BM);
+    p.num_n = static_cast<int>((N + BN - 1) / BN);
+    p.num_kb = static_cast<int>((M + BK - 1) / BK);
+    return launch<FMT, true, true, false, DENSE, F32>(c, a, b, p, int64_t(p.num_m) * p.num_n);
+}
+
+template <int FMT>
+cudaError_t grouped_rows_t(const LaunchCtx& c, bi_dtype dt, int dinput, void* out,
+                           const void* a_pad, int64_t Mp, const void* w, int64_t M, int64_t K,
+                           int64_t N, int64_t E, const uint32_t* seg, const uint32_t* perm) {
+    CUtensorMap a, b;
+    cudaError_t e;
+    Params p{};
+    p.seg = seg; p.perm = perm; p.E = static_cast<int>(E);
+    if (!dinput) {
+        // Y = X W[g]^T: A = padded X [Mp,K] K-major; B = W[g] [N,K] K-major (3-D map)
+        if ((e = make_map(&a, dt, a_pad, K, Mp, 1, BM)) != cudaSuccess) return e;
+        if ((e = make_map(&b, dt, w, K, N, E, BN, true)) != cudaSuccess) return e;
+        p.out = out; p.ldo = N; p.rows = M; p.cols = N;
+        p.num_n = static_cast<int>((N + BN - 1) / BN);
+        p.num_kb = static_cast<int>((K + BK - 1) / BK);
+        const int64_t up = ((M + BM - 1) / BM + E) * p.num_n;
+        return launch<FMT, false, false, true, GROUPED_ROWS, false>(c, a, b, p, up);
+    }
+    // dX = dY W[g]: A = padded dY [Mp,N] K-major; B = W[g] [N,K]: out k contiguous, contraction n
+    if ((e = make_map(&a, dt, a_pad, N, Mp, 1, BM)) != cudaSuccess) return e;
+    if ((e = make_map(&b, dt, w, K, N, E, BK, true)) != cudaSuccess) return e;
+    p.out = out; p.ldo = K; p.rows = M; p.cols = K;
+    p.num_n = static_cast<int>((K + BN - 1) / BN);
+    p.num_kb = static_cast<int>((N + BK - 1) / BK);
+    const int64_t up = ((M + BM - 1) / BM + E) * p.num_n;
+    return launch<FMT, false, true, true, GROUPED_ROWS, false>(c, a, b, p, up);
+}
+
+template <int FMT>
+cudaError_t grouped_dw_t(const LaunchCtx& c, bi_dtype dt, float* dw, const void* dy_pad,
+                         const void* x_pad, int64_t Mp, int64_t K, int64_t N, int64_t E,
+                         const uint32_t* seg) {
+    CUtensorMap a, b;
+    cudaError_t e;
+    if ((e = make_map(&a, dt, dy_pad, N, Mp, 1, BK)) != cudaSuccess) return e;
+    if ((e = make_map(&b, dt, x_pad, K, Mp, 1, BK)) != cudaSuccess) return e;
+    Params p{};
+    p.out = dw; p.ldo = K; p.rows = N; p.cols = K;
+    p.seg = seg; p.E = static_cast<int>(E);
+    p.num_m = static_cast<int>((N + BM - 1) / BM);
+    p.num_n = static_cast<int>((K + BN - 1) / BN);
+    p.num_kb = 0;
+    return launch<FMT, true, true, false, GROUPED_DW, true>(c, a, b, p,
+                                                            E * int64_t(p.num_m) * p.num_n);
+}
+
+}  // namespace
+
+cudaError_t tc_forward(const LaunchCtx& c, bi_dtype dt, void* y, const void* x, const void* w,
+                       const void* bias, int64_t M, int64_t K, int64_t N) {
+    return dt == BI_BF16 ? forward_t<1>(c, dt, y, x, w, bias, M, K, N)
+                         : forward_t<0>(c, dt, y, x, w, bias, M, K, N);
+}
+
+cudaError_t tc_dx(const LaunchCtx& c, bi_dtype dt, void* dx, const void* dy, const void* w,
+                  int64_t M, int64_t K, int64_t N) {
+    return dt == BI_BF16 ? dx_t<1>(c, dt, dx, dy, w, M, K, N) : dx_t<0>(c, dt, dx, dy, w, M, K, N);
+}
+
+cudaError_t tc_dw(const LaunchCtx& c, bi_dtype dt, void* dw, int dw_f32, const void* x,
+                  const void* dy, int64_t M, int64_t K, int64_t N) {
+    if (dt == BI_BF16)
+        return dw_f32 ? dw_t<1, true>(c, dt, dw, x, dy, M, K, N) : dw_t<1, false>(c, dt, dw, x, dy, M, K, N);
+    return dw_f32 ? dw_t<0, true>(c, dt, dw, x, dy, M, K, N) : dw_t<0, false>(c, dt, dw, x, dy, M, K, N);
+}
+
+cudaError_t tc_grouped_rows(const LaunchCtx& c, bi_dtype dt, int pass_dinput, void* out,
+                            const void* a_padded, int64_t Mp_max, const void* w, int64_t M,
+                            int64_t K, int64_t N, int64_t E, const uint32_t* seg,
+                            const uint32_t* perm) {
+    return dt == BI_BF16
+               ? grouped_rows_t<1>(c, dt, pass_dinput, out, a_padded, Mp_max, w, M, K, N, E, seg, perm)
+               : grouped_rows_t<0>(c, dt, pass_dinput, out, a_padded, Mp_max, w, M, K, N, E, seg, perm);
+}
+
+cudaError_t tc_grouped_dw(const LaunchCtx& c, bi_dtype dt, float* dw, const void* dy_padded,
+                          const void* x_padded, int64_t Mp_max, int64_t M, int64_t K, int64_t N,
+                          int64_t E, const uint32_t* seg) {
+    (void)M;
+    return dt == BI_BF16 ? grouped_dw_t<1>(c, dt, dw, dy_padded, x_padded, Mp_max, K, N, E, seg)
+                         : grouped_dw_t<0>(c, dt, dw, dy_padded, x_padded, Mp_max, K, N, E, seg);
+}
+
+}  // namespace bi

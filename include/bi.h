@@ -1,0 +1,189 @@
+/*
+ * bi.h - C ABI of the deterministic, batch-invariant training matmul (GB300, sm_103a).
+ *
+ * The three matmuls of a linear layer and a grouped per-row-expert variant:
+ *
+ *   forward   Y  = X * W (+ b)       X [M,K], W [K,N] ("[in, out]"), b [N], Y [M,N]
+ *   dX        dX = dY * W^T          dY [M,N], dX [M,K]
+ *   dW        dW = X^T * dY          dW [K,N]
+ *   grouped   Y[m,:] = X[m,:] * W[e(m)]^T        W [E,N,K], row_experts [M] (u32)
+ *             dX[m,:] = dY[m,:] * W[e(m)]        dW[e] = sum over rows of expert e
+ *                                                 of dY[m,:]^T X[m,:] (always f32)
+ *
+ * Sources: sgemm-bi 0.1.1.post2 (PyPI page), sections "Use" (weight stored
+ * [in, out]; the raw-pointer Engine.forward call with m, k, n, a dtype string,
+ * a stream and a tensor-core flag) and "Determinism contracts" (the two tiers);
+ * ViperLLM ffma.py, _FFMAAddmm (bias added in f32 before the single downcast;
+ * gx = gy W^T, gW = x^T gy); rublas 0.1.45 src/tensor_grouped/mod.rs
+ * (fn grouped_matmul_nt, struct GroupedBackward, GroupedMatmulError).
+ *
+ * ------------------------------------------------------------------------
+ * Arithmetic contract
+ * ------------------------------------------------------------------------
+ * Scalar tier (tensor_cores = 0, or any f32 call, or a shape below the
+ * tensor-core threshold): every output is one chain
+ *      acc = +0.0f;  for i ascending: acc = fmaf(up(a_i), up(b_i), acc)
+ * over the contracted index, where up() is the exact widening to f32.  The
+ * forward adds up(b[n]) to acc in f32, then rounds once (round to nearest
+ * even) to the operand type.  dW cuts the rows into chunks of BI_DW_CHUNK rows
+ * counted from row 0, runs a chain per chunk, and adds the chunk partials by a
+ * fixed pairwise tree over adjacent partials (an odd last partial is carried up
+ * unchanged); then one rounding (or none, with dw_f32 = 1).  Grouped dweights
+ * do the same per expert over that expert's rows in ascending row index.
+ * Results are bit-identical to the reference CPU definition above, across
+ * runs, and row m of Y / dX does not depend on M.
+ *
+ * Tensor-core tier (tensor_cores = 1, bf16/f16, non-M output dims >= 64, K and
+ * N multiples of 8, 16-byte aligned pointers): tcgen05 MMA, f32 accumulation
+ * in tensor memory, contracted index processed in fixed 64-wide blocks in
+ * ascending order, no split of the contraction, no atomics, and no tile,
+ * order or instruction choice that depends on M.  Results are bit-identical
+ * across runs and per row for any M, and within the published tolerance of the
+ * scalar tier (they are not bit-equal to it).  dW and grouped dweights chain
+ * the row blocks in ascending order inside the accumulator (the degenerate,
+ * single-chunk case of the fixed tree).
+ *
+ * Dispatch looks only at (pass, dtype, tensor_cores, K, N): never at M.
+ *
+ * ------------------------------------------------------------------------
+ * Conventions
+ * ------------------------------------------------------------------------
+ * - Every tensor is dense, row-major, contiguous, on the engine's device, and
+ *   owned by the caller.  Pointers are device pointers.  bf16/f16 data are
+ *   the IEEE encodings; f32 is binary32.
+ * - `stream` is a cudaStream_t (NULL = the legacy default stream).  Calls only
+ *   enqueue work; none of them synchronises with the host.
+ * - Calls return a status and never throw or abort.  Arguments are checked on
+ *   the host before anything is enqueued.  On error nothing is enqueued and
+ *   bi_last_error() describes the cause.
+ * - M = 0 is a successful no-op (the grouped backward still zeroes dW).
+ * - Row ids >= E are padding: they give +0 rows in Y and dX and add nothing
+ *   to dW.  They are not an error.
+ * - Scratch memory is taken from an engine-owned, stream-ordered memory pool
+ *   and returned in stream order, so calls on different streams do not share
+ *   scratch.
+ * - A device-side wait that does not finish within the engine's limit stops
+ *   the kernel, which records BI_ERR_TIMEOUT in the engine's status word;
+ *   bi_engine_check() reports it.
+ */
+#ifndef BI_H
+#define BI_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct bi_engine_s* bi_engine;
+
+typedef enum { BI_F32 = 0, BI_BF16 = 1, BI_F16 = 2 } bi_dtype;
+
+typedef enum {
+    BI_OK = 0,
+    BI_ERR_INVALID_ARG = 1, /* null pointer, K/N/E = 0, bad dtype, negative size */
+    BI_ERR_MISALIGNED = 2,  /* tensor-core tier chosen but a pointer is not 16-byte aligned */
+    BI_ERR_UNSUPPORTED = 3, /* sizes beyond the library's indexing limits */
+    BI_ERR_CUDA = 4,        /* a CUDA runtime or launch error (never turned into a fallback) */
+    BI_ERR_OOM = 5,         /* scratch allocation failed */
+    BI_ERR_TIMEOUT = 6      /* a device-side pipeline wait ran out (see bi_engine_check) */
+} bi_status;
+
+/* Passes, as seen by the dispatcher. */
+typedef enum {
+    BI_PASS_FORWARD = 0, BI_PASS_DX = 1, BI_PASS_DW = 2,
+    BI_PASS_GROUPED_FORWARD = 3, BI_PASS_GROUPED_DINPUT = 4, BI_PASS_GROUPED_DWEIGHTS = 5
+} bi_pass;
+
+/* Rows per chunk of the dW reduction tree (scalar tier). */
+#define BI_DW_CHUNK 256
+
+/* Create an engine bound to CUDA device `device`.  Source: sgemm-bi 0.1.1.post2,
+ * "Use" (Engine(0) is created once and owns the compiled kernels).  The engine
+ * owns a memory pool for scratch, a device status word and an error string.
+ * Errors: BI_ERR_INVALID_ARG (out == NULL), BI_ERR_CUDA (no such device). */
+bi_status bi_engine_create(int device, bi_engine* out);
+
+/* Destroy an engine.  The caller must make sure no work enqueued through it is
+ * still running (synchronise its streams first).  NULL is a no-op. */
+void bi_engine_destroy(bi_engine engine);
+
+/* Text of the last error on this engine (engine != NULL) or of the last error
+ * on this thread for calls made with engine == NULL.  Owned by the library,
+ * valid until the next call on the same engine / thread. */
+const char* bi_last_error(bi_engine engine);
+
+/* Wait for `stream`, then read and clear the engine's device status word.
+ * Returns BI_ERR_TIMEOUT if a kernel gave up a pipeline wait since the last
+ * check, BI_ERR_CUDA on a CUDA error, BI_OK otherwise. */
+bi_status bi_engine_check(bi_engine engine, void* stream);
+
+/* Forward: y[M,N] = round( X[M,K] * W[K,N] + bias[N] ), bias nullable.
+ * Source: sgemm-bi 0.1.1.post2, "Use" (Engine.forward(y, x, w, bias|None, m, k,
+ * n, dtype, stream, tensor_cores)); ViperLLM ffma.py, _FFMAAddmm.forward (bias in
+ * f32, then one cast).  y must not overlap x, w or bias. */
+bi_status bi_forward(bi_engine engine, void* y, const void* x, const void* w, const void* bias,
+                     int64_t m, int64_t k, int64_t n, bi_dtype dtype, void* stream, int tensor_cores);
+
+/* Input gradient: dx[M,K] = round( dY[M,N] * W[K,N]^T ).
+ * Source: ViperLLM ffma.py, _FFMAAddmm.backward (gx = gy W^T); sgemm-bi
+ * 0.1.1.post2 intro (deterministic dX). */
+bi_status bi_backward_dx(bi_engine engine, void* dx, const void* dy, const void* w,
+                         int64_t m, int64_t k, int64_t n, bi_dtype dtype, void* stream, int tensor_cores);
+
+/* Weight gradient: dw[K,N] = X[M,K]^T * dY[M,N], reduced over M by the fixed
+ * chunk tree.  dw_f32 = 1 writes f32 (no rounding), 0 writes the operand type.
+ * Source: ViperLLM ffma.py, _FFMAAddmm.backward (gW = x^T gy, cast back);
+ * sgemm-bi 0.1.1.post2 "Use" ("deterministic dW (f32-accumulated)"). */
+bi_status bi_backward_dw(bi_engine engine, void* dw, int dw_f32, const void* x, const void* dy,
+                         int64_t m, int64_t k, int64_t n, bi_dtype dtype, void* stream, int tensor_cores);
+
+/* Grouped forward: y[m,:] = round( X[m,:] * W[e(m)]^T ) with W [E,N,K] and
+ * e(m) = row_experts[m]; rows with e(m) >= E are +0.  Rows need not be sorted.
+ * Source: rublas 0.1.45 src/tensor_grouped/mod.rs, fn grouped_matmul_nt
+ * ("Group IDs outside [0,E) denote padding and produce zero rows"; FP32
+ * accumulation, one output rounding). */
+bi_status bi_grouped_forward(bi_engine engine, void* y, const void* x, const void* w,
+                             const uint32_t* row_experts, int64_t m, int64_t k, int64_t n, int64_t e,
+                             bi_dtype dtype, void* stream, int tensor_cores);
+
+/* Grouped backward: dx[m,:] = round( dY[m,:] * W[e(m)] ) (+0 for padding rows)
+ * and dw[e] (f32, [E,N,K]) = sum over the rows of expert e, in ascending row
+ * index, of dY[m,:]^T X[m,:]; an expert with no rows gets +0.  dx may be NULL
+ * to compute dw only.  Source: rublas 0.1.45 src/tensor_grouped/mod.rs,
+ * struct GroupedBackward ("dweights is always FP32") and fn
+ * grouped_matmul_nt_backward_segmented_with_strategy (the segment offsets are
+ * built inside the library here, from row_experts). */
+bi_status bi_grouped_backward(bi_engine engine, void* dx, float* dw, const void* x, const void* w,
+                              const void* dy, const uint32_t* row_experts,
+                              int64_t m, int64_t k, int64_t n, int64_t e,
+                              bi_dtype dtype, void* stream, int tensor_cores);
+
+/* ---- introspection ---------------------------------------------------- */
+
+/* The dispatcher's choice for a call: 0 = scalar tier, 1 = tensor-core tier.
+ * A pure function of its arguments (M is not one of them).  Source:
+ * sgemm-bi 0.1.1.post2, "Determinism contracts" ("falls back to the scalar
+ * tier when an output dim is < 64 (shape-only dispatch)"). */
+int bi_dispatch_tier(int pass, bi_dtype dtype, int tensor_cores, int64_t k, int64_t n);
+
+/* Number of kernels this engine has launched since it was created. */
+uint64_t bi_launch_count(bi_engine engine);
+
+/* Set the limit (nanoseconds) after which a device-side pipeline wait gives up
+ * and records BI_ERR_TIMEOUT.  Default 2e9 (2 s); 0 restores the default. */
+bi_status bi_engine_set_wait_limit(bi_engine engine, uint64_t nanoseconds);
+
+/* Self-test of the timeout path: launches one kernel that waits on a barrier
+ * nothing completes, bounded by the engine's wait limit.  Afterwards
+ * bi_engine_check() must report BI_ERR_TIMEOUT.  Faults nothing. */
+bi_status bi_selftest_wait_timeout(bi_engine engine, void* stream);
+
+/* Library version string. */
+const char* bi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* BI_H */

@@ -1,0 +1,294 @@
+"""GPU parity of the dense passes (forward, dX, dW) through the C ABI.
+
+Scalar tier: bit-exact against the oracle.  Tensor-core tier: within the
+tolerance in helpers.py, and bit-exact on exact small-integer problems.  Both
+tiers: bit-identical over 10 runs, and row m of Y / dX independent of M.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import deterministic_invariant_gemm_fixed_gb300 as bi
+from deterministic_invariant_gemm_fixed_gb300 import synth
+from helpers import abs_sum, check_tc, dev, f64, out_np, sample_rows
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def eng():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    e = bi.Engine(0)
+    yield e
+    e.close()
+
+
+def run_dense(eng, x, w, dy, b, m, k, n, dtype, tc, dw_f32=True, passes=("y", "dx", "dw")):
+    tdt = synth.TORCH_DTYPES[dtype]
+    X, W, DY, B = dev(x), dev(w), dev(dy), dev(b)
+    out = {}
+    if "y" in passes:
+        y = torch.empty(m, n, dtype=tdt, device="cuda")
+        eng.forward(y, X, W, B, m, k, n, dtype, None, tc)
+        out["y"] = y
+    if "dx" in passes:
+        dx = torch.empty(m, k, dtype=tdt, device="cuda")
+        eng.backward_dx(dx, DY, W, m, k, n, dtype, None, tc)
+        out["dx"] = dx
+    if "dw" in passes:
+        dw = torch.empty(k, n, dtype=torch.float32 if (dw_f32 or dtype == "f32") else tdt, device="cuda")
+        eng.backward_dw(dw, int(dw_f32), X, DY, m, k, n, dtype, None, tc)
+        out["dw"] = dw
+    eng.check()
+    return {kk: out_np(v) for kk, v in out.items()}
+
+
+def np_in(*ts):
+    return [synth.to_np(t) if t is not None else None for t in ts]
+
+
+SCALAR_CASES = [
+    # name, dtype, M, K, N, value spec
+    ("linear_f32", "f32", 64, 256, 512, ("normal", 1.0)),
+    ("ragged_f16", "f16", 300, 200, 130, ("uniform", 1.0)),
+    ("odd_bf16", "bf16", 257, 77, 131, ("normal", 1.0)),     # unaligned rows: scalar loads
+    ("n48_fallback_f16", "f16", 2048, 1024, 48, ("uniform", 1.0)),
+    ("gemv_f16", "f16", 1, 4096, 4096, ("uniform", 1.0)),
+    ("ragged_1000_f16", "f16", 1000, 1000, 1000, ("uniform", 1.0)),
+    ("long_dw_chunks_bf16", "bf16", 1500, 64, 72, ("normal", 1.0)),  # 6 chunks, odd tree
+]
+
+
+@pytest.mark.parametrize("case", SCALAR_CASES, ids=lambda c: c[0])
+def test_scalar_tier_bit_exact(eng, case):
+    _, dtype, m, k, n, spec = case
+    x, w, dy, b = synth.dense_inputs(m, k, n, dtype, x=spec, w=spec, dy=spec, b=("normal", 0.1))
+    got = run_dense(eng, x, w, dy, b, m, k, n, dtype, tc=0)
+    xn, wn, dyn, bn = np_in(x, w, dy, b)
+    assert np.array_equal(got["y"], oracle.forward(xn, wn, bn, m, k, n, dtype))
+    assert np.array_equal(got["dx"], oracle.backward_dx(dyn, wn, m, k, n, dtype))
+    assert np.array_equal(got["dw"], oracle.backward_dw(xn, dyn, m, k, n, dtype, dw_f32=True))
+    # rounded dW as well
+    got2 = run_dense(eng, x, w, dy, b, m, k, n, dtype, tc=0, dw_f32=False, passes=("dw",))
+    assert np.array_equal(got2["dw"], oracle.backward_dw(xn, dyn, m, k, n, dtype, dw_f32=False))
+
+
+@pytest.mark.parametrize("case", SCALAR_CASES, ids=lambda c: c[0])
+def test_tc_flag_on_scalar_shapes_is_scalar(eng, case):
+    """With tensor_cores=1, passes whose shape the dispatcher keeps on the scalar
+    tier (f32 operands, an output dim < 64, rows not multiples of 8) give the
+    scalar results bit for bit."""
+    _, dtype, m, k, n, spec = case
+    x, w, dy, b = synth.dense_inputs(m, k, n, dtype, x=spec, w=spec, dy=spec, b=("normal", 0.1))
+    a = run_dense(eng, x, w, dy, b, m, k, n, dtype, tc=0)
+    t = run_dense(eng, x, w, dy, b, m, k, n, dtype, tc=1)
+    for key, p in (("y", bi.BI_PASS_FORWARD), ("dx", bi.BI_PASS_DX), ("dw", bi.BI_PASS_DW)):
+        if bi.bi_dispatch_tier(p, dtype, 1, k, n) == 0:
+            assert np.array_equal(a[key], t[key]), key
+
+
+def test_scalar_gpt2_up_sampled(eng):
+    c = synth.GPT2_UP
+    m, k, n, dtype = c["m"], c["k"], c["n"], c["dtype"]
+    x, w, dy, b = synth.dense_inputs(m, k, n, dtype, x=c["x"], w=c["w"], dy=c["dy"], b=c["b"])
+    got = run_dense(eng, x, w, dy, b, m, k, n, dtype, tc=0)
+    xn, wn, dyn, bn = np_in(x, w, dy, b)
+    rows = sample_rows(m, 96)
+    cols = sample_rows(n, 24, seed=1)
+    assert np.array_equal(got["y"][rows], oracle.forward(xn, wn, bn, m, k, n, dtype, rows=rows))
+    assert np.array_equal(got["dx"][rows], oracle.backward_dx(dyn, wn, m, k, n, dtype, rows=rows))
+    assert np.array_equal(got["dw"][:, cols], oracle.backward_dw(xn, dyn, m, k, n, dtype, dw_f32=True, cols=cols))
+
+
+TC_CASES = [
+    ("ragged_bf16", "bf16", 300, 200, 520),
+    ("multi_tile_bf16", "bf16", 520, 264, 776),
+    ("ragged_1000_f16", "f16", 1000, 1000, 1000),
+    ("gemv_f16", "f16", 1, 4096, 4096),
+    ("small_k_f16", "f16", 130, 8, 72),
+]
+
+
+@pytest.mark.parametrize("case", TC_CASES, ids=lambda c: c[0])
+def test_tc_tier_within_tolerance(eng, case):
+    _, dtype, m, k, n = case
+    spec = ("uniform", 1.0) if dtype == "f16" else ("normal", 1.0)
+    x, w, dy, b = synth.dense_inputs(m, k, n, dtype, x=spec, w=spec, dy=spec, b=("normal", 0.1))
+    for p in (bi.BI_PASS_FORWARD, bi.BI_PASS_DX, bi.BI_PASS_DW):
+        assert bi.bi_dispatch_tier(p, dtype, 1, k, n) == (0 if (p != bi.BI_PASS_FORWARD and k < 64) else 1)
+    got = run_dense(eng, x, w, dy, b, m, k, n, dtype, tc=1)
+    got_r = run_dense(eng, x, w, dy, b, m, k, n, dtype, tc=1, dw_f32=False, passes=("dw",))
+    xn, wn, dyn, bn = np_in(x, w, dy, b)
+    x64, w64, dy64, b64 = (f64(a, dtype) for a in (xn, wn, dyn, bn))
+    r = oracle.forward(xn, wn, bn, m, k, n, dtype, out_f32=True)
+    ok, st = check_tc(got["y"], r, abs_sum(x64, w64, b64), dtype)
+    assert ok, ("y", st)
+    r = oracle.backward_dx(dyn, wn, m, k, n, dtype, out_f32=True)
+    ok, st = check_tc(got["dx"], r, abs_sum(dy64, w64.T), dtype)
+    assert ok, ("dx", st)
+    r = oracle.backward_dw(xn, dyn, m, k, n, dtype, dw_f32=True)
+    S = abs_sum(x64.T, dy64)
+    ok, st = check_tc(got["dw"], r, S, "f32")
+    assert ok, ("dw f32", st)
+    ok, st = check_tc(got_r["dw"], r, S, dtype)
+    assert ok, ("dw rounded", st)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+def test_tc_tier_exact_on_small_integers(eng, dtype):
+    """Integer operands in [-8, 8] (f16: [-16, 16]) make every partial sum exact in
+    f32, so the tensor-core result must equal the oracle bit for bit, bias and
+    the single rounding included."""
+    m, k, n = 333, 320, 392
+    hi = 16 if dtype == "f16" else 8
+    x = synth.small_ints((m, k), -hi, hi, dtype, 11)
+    w = synth.small_ints((k, n), -hi, hi, dtype, 12)
+    dy = synth.small_ints((m, n), -hi, hi, dtype, 13)
+    b = (synth.small_ints((n,), -128, 127, "f32", 14) / 2).to(synth.TORCH_DTYPES[dtype])
+    got = run_dense(eng, x, w, dy, b, m, k, n, dtype, tc=1)
+    got_r = run_dense(eng, x, w, dy, b, m, k, n, dtype, tc=1, dw_f32=False, passes=("dw",))
+    xn, wn, dyn, bn = np_in(x, w, dy, b)
+    assert np.array_equal(got["y"], oracle.forward(xn, wn, bn, m, k, n, dtype))
+    assert np.array_equal(got["dx"], oracle.backward_dx(dyn, wn, m, k, n, dtype))
+    assert np.array_equal(got["dw"], oracle.backward_dw(xn, dyn, m, k, n, dtype, dw_f32=True))
+    assert np.array_equal(got_r["dw"], oracle.backward_dw(xn, dyn, m, k, n, dtype, dw_f32=False))
+
+
+def test_tc_gpt2_up_sampled(eng):
+    c = synth.GPT2_UP
+    m, k, n, dtype = c["m"], c["k"], c["n"], c["dtype"]
+    x, w, dy, b = synth.dense_inputs(m, k, n, dtype, x=c["x"], w=c["w"], dy=c["dy"], b=c["b"])
+    got = run_dense(eng, x, w, dy, b, m, k, n, dtype, tc=1)
+    xn, wn, dyn, bn = np_in(x, w, dy, b)
+    x64, w64, dy64, b64 = (f64(a, dtype) for a in (xn, wn, dyn, bn))
+    rows = sample_rows(m, 64)
+    cols = sample_rows(n, 16, seed=1)
+    r = oracle.forward(xn, wn, bn, m, k, n, dtype, rows=rows, out_f32=True)
+    ok, st = check_tc(got["y"][rows], r, abs_sum(x64[rows], w64, b64), dtype)
+    assert ok, st
+    r = oracle.backward_dx(dyn, wn, m, k, n, dtype, rows=rows, out_f32=True)
+    ok, st = check_tc(got["dx"][rows], r, abs_sum(dy64[rows], w64.T), dtype)
+    assert ok, st
+    r = oracle.backward_dw(xn, dyn, m, k, n, dtype, dw_f32=True, cols=cols)
+    ok, st = check_tc(got["dw"][:, cols], r, abs_sum(x64.T, dy64[:, cols]), "f32")
+    assert ok, st
+
+
+@pytest.mark.parametrize("proj", synth.SEVEN_B, ids=lambda p: p[0])
+def test_tc_7b_layer_sampled(eng, proj):
+    name, k, n = proj
+    m, dtype = synth.SEVEN_B_M, "bf16"
+    x, w, dy, _ = synth.dense_inputs(m, k, n, dtype, x=("normal", 1.0), w=("normal", 0.02),
+                                     dy=("normal", 1.0), b=None)
+    got = run_dense(eng, x, w, dy, None, m, k, n, dtype, tc=1)
+    xn, wn, dyn = np_in(x, w, dy)
+    x64, w64, dy64 = (f64(a, dtype) for a in (xn, wn, dyn))
+    rows = sample_rows(m, 6, seed=2)
+    cols = sample_rows(n, 3, seed=3)
+    r = oracle.forward(xn, wn, None, m, k, n, dtype, rows=rows, out_f32=True)
+    ok, st = check_tc(got["y"][rows], r, abs_sum(x64[rows], w64), dtype)
+    assert ok, st
+    r = oracle.backward_dx(dyn, wn, m, k, n, dtype, rows=rows, out_f32=True)
+    ok, st = check_tc(got["dx"][rows], r, abs_sum(dy64[rows], w64.T), dtype)
+    assert ok, st
+    r = oracle.backward_dw(xn, dyn, m, k, n, dtype, dw_f32=True, cols=cols)
+    ok, st = check_tc(got["dw"][:, cols], r, abs_sum(x64.T, dy64[:, cols]), "f32")
+    assert ok, st
+
+
+@pytest.mark.parametrize("tc", [0, 1])
+def test_ten_runs_bit_identical(eng, tc):
+    m, k, n, dtype = 1024, 768, 1536, "bf16"
+    x, w, dy, b = synth.dense_inputs(m, k, n, dtype)
+    first = run_dense(eng, x, w, dy, b, m, k, n, dtype, tc=tc)
+    for _ in range(9):
+        again = run_dense(eng, x, w, dy, b, m, k, n, dtype, tc=tc)
+        for key in first:
+            assert np.array_equal(first[key], again[key]), key
+
+
+def test_batch_invariance_tc_7b_qkv(eng):
+    """Rows of Y and dX on the tensor-core tier do not depend on M."""
+    k, n, dtype = 4096, 12288, "bf16"
+    M = synth.SEVEN_B_M
+    x, w, dy, _ = synth.dense_inputs(M, k, n, dtype, b=None)
+    full = run_dense(eng, x, w, dy, None, M, k, n, dtype, tc=1, passes=("y", "dx"))
+    for mp in (1, 7, 64, 513):
+        part = run_dense(eng, x[:mp].contiguous(), w, dy[:mp].contiguous(), None, mp, k, n, dtype, tc=1,
+                         passes=("y", "dx"))
+        assert np.array_equal(part["y"], full["y"][:mp]), mp
+        assert np.array_equal(part["dx"], full["dx"][:mp]), mp
+
+
+@pytest.mark.parametrize("dtype,tc", [("f32", 0), ("bf16", 0), ("f16", 1), ("bf16", 1)])
+def test_batch_invariance_prefixes(eng, dtype, tc):
+    m, k, n = 64, 256, 512
+    x, w, dy, b = synth.dense_inputs(m, k, n, dtype, w=("normal", 1.0))
+    full = run_dense(eng, x, w, dy, b, m, k, n, dtype, tc=tc, passes=("y", "dx"))
+    for mp in (1, 17, 64):
+        part = run_dense(eng, x[:mp].contiguous(), w, dy[:mp].contiguous(), b, mp, k, n, dtype, tc=tc,
+                         passes=("y", "dx"))
+        assert np.array_equal(part["y"], full["y"][:mp])
+        assert np.array_equal(part["dx"], full["dx"][:mp])
+
+
+# ------------------------------------------------------------------- edge cases and errors
+
+def test_m_zero(eng):
+    k, n = 128, 256
+    y = torch.full((1, n), 7.0, dtype=torch.bfloat16, device="cuda")
+    w = torch.zeros(k, n, dtype=torch.bfloat16, device="cuda")
+    x = torch.zeros(1, k, dtype=torch.bfloat16, device="cuda")
+    for tc in (0, 1):
+        eng.forward(y, x, w, None, 0, k, n, "bf16", None, tc)
+        dw = torch.full((k, n), 5.0, dtype=torch.float32, device="cuda")
+        eng.backward_dw(dw, 1, x, x, 0, k, n, "bf16", None, tc)
+        eng.check()
+        assert torch.all(y == 7.0)
+        assert torch.all(dw == 0) and not torch.any(torch.signbit(dw))
+
+
+def test_errors_are_reported(eng):
+    h = eng.handle
+    x = torch.zeros(16, 128, dtype=torch.bfloat16, device="cuda")
+    w = torch.zeros(128, 128, dtype=torch.bfloat16, device="cuda")
+    y = torch.zeros(17, 128, dtype=torch.bfloat16, device="cuda")
+    assert bi.bi_forward(h, y, x, w, None, 16, 0, 128, "bf16", None, 1) == bi.BI_ERR_INVALID_ARG
+    assert bi.bi_forward(h, y, x, w, None, 16, 128, 128, 7, None, 1) == bi.BI_ERR_INVALID_ARG
+    assert bi.bi_forward(h, None, x, w, None, 16, 128, 128, "bf16", None, 1) == bi.BI_ERR_INVALID_ARG
+    assert bi.bi_forward(h, y, x, w, None, -1, 128, 128, "bf16", None, 1) == bi.BI_ERR_INVALID_ARG
+    # misaligned output with the tensor-core tier selected
+    st = bi.bi_forward(h, y.view(-1)[1:].data_ptr(), x, w, None, 16, 128, 128, "bf16", None, 1)
+    assert st == bi.BI_ERR_MISALIGNED, bi.bi_last_error(h)
+    assert "aligned" in bi.bi_last_error(h)
+    # the scalar tier accepts the same misaligned pointer
+    assert bi.bi_forward(h, y.view(-1)[1:].data_ptr(), x, w, None, 16, 128, 128, "bf16", None, 0) == bi.BI_OK
+    eng.check()
+
+
+def test_timeout_path_reports_and_recovers(eng):
+    h = eng.handle
+    assert bi.bi_engine_set_wait_limit(h, 20_000_000) == bi.BI_OK  # 20 ms
+    assert bi.bi_selftest_wait_timeout(h, None) == bi.BI_OK
+    assert bi.bi_engine_check(h, None) == bi.BI_ERR_TIMEOUT
+    assert "self-test" in bi.bi_last_error(h)
+    assert bi.bi_engine_set_wait_limit(h, 0) == bi.BI_OK
+    # the context is still usable and the status word was cleared
+    assert bi.bi_engine_check(h, None) == bi.BI_OK
+    m, k, n = 128, 128, 256
+    x, w, dy, b = synth.dense_inputs(m, k, n, "bf16")
+    got = run_dense(eng, x, w, dy, b, m, k, n, "bf16", tc=1, passes=("y",))
+    assert got["y"].shape == (m, n)
+
+
+def test_launch_count_counts_kernels(eng):
+    m, k, n = 128, 128, 256
+    x, w, dy, b = synth.dense_inputs(m, k, n, "bf16")
+    before = eng.launches()
+    run_dense(eng, x, w, dy, b, m, k, n, "bf16", tc=1)
+    assert eng.launches() - before == 3  # one tcgen05 kernel per pass
+    before = eng.launches()
+    run_dense(eng, x, w, dy, b, m, k, n, "bf16", tc=0, passes=("y", "dx"))
+    assert eng.launches() - before == 2

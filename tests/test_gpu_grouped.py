@@ -1,0 +1,179 @@
+"""GPU parity of the grouped per-row-expert passes through the C ABI."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import deterministic_invariant_gemm_fixed_gb300 as bi
+from deterministic_invariant_gemm_fixed_gb300 import synth
+from helpers import check_tc, dev, f64, out_np, sample_rows
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def eng():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    e = bi.Engine(0)
+    yield e
+    e.close()
+
+
+def ids_dev(ids):
+    return torch.from_numpy(synth.to_np(ids).astype(np.int32)).cuda()  # u32 bit patterns
+
+
+def run_grouped(eng, x, w, dy, ids, m, k, n, e, dtype, tc, with_dx=True):
+    tdt = synth.TORCH_DTYPES[dtype]
+    X, W, DY, I = dev(x), dev(w), dev(dy), ids_dev(ids)
+    y = torch.empty(m, n, dtype=tdt, device="cuda")
+    dx = torch.empty(m, k, dtype=tdt, device="cuda") if with_dx else None
+    dw = torch.empty(e, n, k, dtype=torch.float32, device="cuda")
+    eng.grouped_forward(y, X, W, I, m, k, n, e, dtype, None, tc)
+    eng.grouped_backward(dx, dw, X, W, DY, I, m, k, n, e, dtype, None, tc)
+    eng.check()
+    return out_np(y), (out_np(dx) if with_dx else None), out_np(dw)
+
+
+def small_case(dtype, m=700, k=96, n=136, e=5, seed=0):
+    x, w, dy, ids = synth.grouped_inputs(m, k, n, e, dtype, pad_frac=0.06, seed_offset=seed,
+                                         x=("normal", 1.0), w=("normal", 1.0), dy=("normal", 1.0))
+    ids = ids.clone()
+    ids[ids == 2] = 0          # expert 2 gets no rows
+    ids[5] = e + 1000          # an id far beyond E is padding
+    return x, w, dy, ids
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16", "f16"])
+def test_grouped_scalar_bit_exact(eng, dtype):
+    m, k, n, e = 700, 96, 136, 5
+    x, w, dy, ids = small_case(dtype)
+    y, dx, dw = run_grouped(eng, x, w, dy, ids, m, k, n, e, dtype, tc=0)
+    xn, wn, dyn, idn = (synth.to_np(t) for t in (x, w, dy, ids))
+    assert np.array_equal(y, oracle.grouped_forward(xn, wn, idn, m, k, n, e, dtype))
+    assert np.array_equal(dx, oracle.grouped_dinput(wn, dyn, idn, m, k, n, e, dtype))
+    assert np.array_equal(dw, oracle.grouped_dweights(xn, dyn, idn, m, k, n, e, dtype))
+    assert np.all(dw[2] == 0)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+def test_grouped_tc_within_tolerance(eng, dtype):
+    m, k, n, e = 700, 96, 136, 5
+    x, w, dy, ids = small_case(dtype)
+    y, dx, dw = run_grouped(eng, x, w, dy, ids, m, k, n, e, dtype, tc=1)
+    xn, wn, dyn, idn = (synth.to_np(t) for t in (x, w, dy, ids))
+    x64, w64, dy64 = f64(xn, dtype), f64(wn, dtype).reshape(e, n, k), f64(dyn, dtype)
+    valid = idn < e
+    S_y = np.zeros((m, n)); S_dx = np.zeros((m, k)); S_dw = np.zeros((e, n, k))
+    for g in range(e):
+        rows = np.nonzero(idn == g)[0]
+        S_y[rows] = np.abs(x64[rows]) @ np.abs(w64[g]).T
+        S_dx[rows] = np.abs(dy64[rows]) @ np.abs(w64[g])
+        S_dw[g] = np.abs(dy64[rows]).T @ np.abs(x64[rows])
+    r = oracle.grouped_forward(xn, wn, idn, m, k, n, e, dtype, out_f32=True)
+    ok, st = check_tc(y, r, S_y, dtype)
+    assert ok, st
+    r = oracle.grouped_dinput(wn, dyn, idn, m, k, n, e, dtype, out_f32=True)
+    ok, st = check_tc(dx, r, S_dx, dtype)
+    assert ok, st
+    r = oracle.grouped_dweights(xn, dyn, idn, m, k, n, e, dtype)
+    ok, st = check_tc(dw, r, S_dw, "f32")
+    assert ok, st
+    assert np.all(y[~valid] == 0) and np.all(dx[~valid] == 0)
+    assert np.all(dw[2] == 0)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+def test_grouped_tc_exact_on_small_integers(eng, dtype):
+    m, k, n, e = 640, 128, 200, 4
+    x = synth.small_ints((m, k), -8, 8, dtype, 31)
+    w = synth.small_ints((e, n, k), -8, 8, dtype, 32)
+    dy = synth.small_ints((m, n), -8, 8, dtype, 33)
+    ids = synth.expert_ids(m, e, 0.05, 34)
+    y, dx, dw = run_grouped(eng, x, w, dy, ids, m, k, n, e, dtype, tc=1)
+    xn, wn, dyn, idn = (synth.to_np(t) for t in (x, w, dy, ids))
+    assert np.array_equal(y, oracle.grouped_forward(xn, wn, idn, m, k, n, e, dtype))
+    assert np.array_equal(dx, oracle.grouped_dinput(wn, dyn, idn, m, k, n, e, dtype))
+    assert np.array_equal(dw, oracle.grouped_dweights(xn, dyn, idn, m, k, n, e, dtype))
+
+
+@pytest.mark.parametrize("tc", [0, 1])
+def test_grouped_full_config_sampled(eng, tc):
+    c = synth.GROUPED
+    m, k, n, e, dtype = c["m"], c["k"], c["n"], c["e"], c["dtype"]
+    x, w, dy, ids = synth.grouped_inputs(m, k, n, e, dtype, pad_frac=c["pad_frac"])
+    y, dx, dw = run_grouped(eng, x, w, dy, ids, m, k, n, e, dtype, tc=tc)
+    xn, wn, dyn, idn = (synth.to_np(t) for t in (x, w, dy, ids))
+    assert int((idn >= e).sum()) == round(0.05 * m)
+    rows = sample_rows(m, 24, seed=5)
+    rows = np.unique(np.concatenate([rows, np.nonzero(idn >= e)[0][:3]]))
+    rng = np.random.default_rng(6)
+    sel = (rng.integers(0, e, size=6), rng.integers(0, n, size=6))
+    if tc == 0:
+        assert np.array_equal(y[rows], oracle.grouped_forward(xn, wn, idn, m, k, n, e, dtype, rows=rows))
+        assert np.array_equal(dx[rows], oracle.grouped_dinput(wn, dyn, idn, m, k, n, e, dtype, rows=rows))
+        assert np.array_equal(dw[sel[0], sel[1]], oracle.grouped_dweights(xn, dyn, idn, m, k, n, e, dtype, sel=sel))
+        return
+    x64, dy64 = f64(xn, dtype), f64(dyn, dtype)
+    w64 = f64(wn, dtype).reshape(e, n, k)
+    S_y = np.zeros((rows.size, n)); S_dx = np.zeros((rows.size, k))
+    for i, r_ in enumerate(rows):
+        if idn[r_] < e:
+            S_y[i] = np.abs(w64[idn[r_]]) @ np.abs(x64[r_])
+            S_dx[i] = np.abs(dy64[r_]) @ np.abs(w64[idn[r_]])
+    r = oracle.grouped_forward(xn, wn, idn, m, k, n, e, dtype, rows=rows, out_f32=True)
+    ok, st = check_tc(y[rows], r, S_y, dtype)
+    assert ok, st
+    r = oracle.grouped_dinput(wn, dyn, idn, m, k, n, e, dtype, rows=rows, out_f32=True)
+    ok, st = check_tc(dx[rows], r, S_dx, dtype)
+    assert ok, st
+    S_dw = np.stack([np.abs(dy64[idn == g_, j]) @ np.abs(x64[idn == g_]) for g_, j in zip(*sel)])
+    r = oracle.grouped_dweights(xn, dyn, idn, m, k, n, e, dtype, sel=sel)
+    ok, st = check_tc(dw[sel[0], sel[1]], r, S_dw, "f32")
+    assert ok, st
+
+
+@pytest.mark.parametrize("tc", [0, 1])
+def test_grouped_ten_runs_and_prefix_invariance(eng, tc):
+    m, k, n, e, dtype = 1100, 128, 256, 6, "bf16"
+    x, w, dy, ids = synth.grouped_inputs(m, k, n, e, dtype)
+    first = run_grouped(eng, x, w, dy, ids, m, k, n, e, dtype, tc=tc)
+    for _ in range(9):
+        again = run_grouped(eng, x, w, dy, ids, m, k, n, e, dtype, tc=tc)
+        for a, b in zip(first, again):
+            assert np.array_equal(a, b)
+    for mp in (1, 129, 513):
+        part = run_grouped(eng, x[:mp].contiguous(), w, dy[:mp].contiguous(), ids[:mp].contiguous(),
+                           mp, k, n, e, dtype, tc=tc)
+        assert np.array_equal(part[0], first[0][:mp])
+        assert np.array_equal(part[1], first[1][:mp])
+
+
+def test_grouped_single_expert_matches_dense_scalar(eng):
+    m, k, n, dtype = 300, 96, 80, "bf16"
+    x, w, dy, _ = synth.grouped_inputs(m, k, n, 1, dtype, pad_frac=0.0)
+    ids = torch.zeros(m, dtype=torch.int64)
+    y, dx, dw = run_grouped(eng, x, w, dy, ids, m, k, n, 1, dtype, tc=0)
+    wd = w.reshape(n, k).t().contiguous()
+    Y = torch.empty(m, n, dtype=torch.bfloat16, device="cuda")
+    DX = torch.empty(m, k, dtype=torch.bfloat16, device="cuda")
+    DW = torch.empty(k, n, dtype=torch.float32, device="cuda")
+    eng.forward(Y, dev(x), dev(wd), None, m, k, n, dtype, None, 0)
+    eng.backward_dx(DX, dev(dy), dev(wd), m, k, n, dtype, None, 0)
+    eng.backward_dw(DW, 1, dev(x), dev(dy), m, k, n, dtype, None, 0)
+    assert np.array_equal(y, out_np(Y))
+    assert np.array_equal(dx, out_np(DX))
+    assert np.array_equal(dw[0], out_np(DW).T)
+
+
+def test_grouped_m_zero_zeroes_dw(eng):
+    k, n, e = 64, 64, 3
+    dw = torch.full((e, n, k), 3.0, dtype=torch.float32, device="cuda")
+    z = torch.zeros(1, 64, dtype=torch.bfloat16, device="cuda")
+    ids = torch.zeros(1, dtype=torch.int32, device="cuda")
+    eng.grouped_backward(None, dw, z, z, z, ids, 0, k, n, e, "bf16", None, 1)
+    eng.check()
+    assert torch.all(dw == 0)
+    h = eng.handle
+    assert bi.bi_grouped_forward(h, z, z, z, ids, 1, k, n, 0, "bf16", None, 1) == bi.BI_ERR_INVALID_ARG
