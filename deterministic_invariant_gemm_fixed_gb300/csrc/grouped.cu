@@ -22,7 +22,7 @@ namespace bi {
 namespace {
 
 constexpr int SEG_THREADS = 256;
-constexpr int SEG_ROWS_PER_BLOCK = 4096;
+constexpr int SEG_ROWS_PER_BLOCK = 256;  // one step per block: many blocks in flight
 constexpr uint32_t NONE = 0xffffffffu;
 
 __device__ __forceinline__ uint32_t bucket_of(uint32_t id, uint32_t E) { return id < E ? id : E; }
@@ -31,11 +31,15 @@ __device__ __forceinline__ uint32_t bucket_of(uint32_t id, uint32_t E) { return 
 // earlier rows with the same bucket, and whether no later row shares it.
 __device__ __forceinline__ void rank_in_step(const uint32_t* sb, int tid, uint32_t g, uint32_t& rank,
                                              bool& last) {
-    rank = 0;
-    for (int j = 0; j < tid; ++j) rank += sb[j] == g;
-    last = true;
-    for (int j = tid + 1; j < SEG_THREADS; ++j)
-        if (sb[j] == g) { last = false; break; }
+    uint32_t before = 0, after = 0;
+#pragma unroll 8
+    for (int j = 0; j < SEG_THREADS; ++j) {
+        const uint32_t same = sb[j] == g;
+        before += (j < tid) & same;
+        after += (j > tid) & same;
+    }
+    rank = before;
+    last = after == 0;
 }
 
 __global__ void __launch_bounds__(SEG_THREADS)
