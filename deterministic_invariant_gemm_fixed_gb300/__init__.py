@@ -46,6 +46,7 @@ SIGNATURES = {
     "bi_engine_set_wait_limit": (_i32, [_p, _u64]),
     "bi_selftest_wait_timeout": (_i32, [_p, _p]),
     "bi_version": (ctypes.c_char_p, []),
+    "bi_grouped_forward_noalloc": (_i32, [_p, _p, _p, _p, _i64, _i64, _i64, _i64, _i32, _p]),
 }
 
 
@@ -163,6 +164,13 @@ def bi_grouped_backward(engine, dx, dw, x, w, dy, row_experts, m, k, n, e, dtype
     return _lib.bi_grouped_backward(engine, _ptr(dx), _ptr(dw), _ptr(x), _ptr(w), _ptr(dy),
                                     _ptr(row_experts), m, k, n, e, dtype_code(dtype), _stream(stream),
                                     int(tensor_cores))
+
+
+def bi_grouped_forward_noalloc(y, x, w, row_experts, m, k, n, e, dtype, stream=None) -> int:
+    """Scalar-tier grouped forward with no allocation (see include/bi.h); errors
+    are read with bi_last_error(None)."""
+    return _lib.bi_grouped_forward_noalloc(_ptr(y), _ptr(x), _ptr(w), _ptr(row_experts), m, k, n, e,
+                                           dtype_code(dtype), _stream(stream))
 
 
 def bi_dispatch_tier(pass_, dtype, tensor_cores, k, n) -> int:

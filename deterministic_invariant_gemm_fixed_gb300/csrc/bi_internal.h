@@ -92,6 +92,8 @@ inline int64_t padded_rows_max(int64_t M, int64_t E) { return ((M + 127) / 128) 
 }  // namespace bi
 
 namespace bi {
+// Records `msg` as this thread's last error (bi_last_error(NULL)) and returns st.
+bi_status set_thread_error(bi_status st, const std::string& msg);
 __host__ __device__ __forceinline__ int64_t lmin(int64_t a, int64_t b) { return a < b ? a : b; }
 __host__ __device__ __forceinline__ int64_t lmax(int64_t a, int64_t b) { return a > b ? a : b; }
 }  // namespace bi

@@ -81,6 +81,10 @@ bi::LaunchCtx ctx(bi_engine eng, void* stream) {
 
 }  // namespace
 
+namespace bi {
+bi_status set_thread_error(bi_status st, const std::string& msg) { return fail(nullptr, st, msg); }
+}  // namespace bi
+
 extern "C" {
 
 const char* bi_version(void) { return "bi 0.1.0 (sm_103a)"; }

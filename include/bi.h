@@ -159,6 +159,25 @@ bi_status bi_grouped_backward(bi_engine engine, void* dx, float* dw, const void*
                               int64_t m, int64_t k, int64_t n, int64_t e,
                               bi_dtype dtype, void* stream, int tensor_cores);
 
+/* Grouped forward that allocates nothing.  No counterpart on the pages: this
+ * entry point exists for callers that cannot allocate GPU memory when they run
+ * it (a memory-budgeted runtime whose allocator must not be bypassed, a plug-in
+ * handed buffers but no allocation rights, a path that must never block on the
+ * device heap).  It computes exactly what bi_grouped_forward computes with
+ * tensor_cores = 0 (the scalar tier, bit for bit), on the current CUDA device,
+ * without an engine, and calls no cudaMalloc, cudaFree or other allocating
+ * routine.  Its grouping scratch lives in one fixed 4 MiB device array inside
+ * the library, reserved on every GPU that loads the library until the process
+ * exits; calls needing more than that (4*(2E+4) + 4*M + 4*(E+1)*ceil(M/256)
+ * bytes, each part rounded up to 256) return BI_ERR_UNSUPPORTED.  All calls on a
+ * device share the array: calls whose GPU work overlaps (unordered streams or
+ * threads) race and give wrong results.  The first call on a device resolves
+ * the array's address on that device; make it before any stream capture.
+ * Errors are reported through bi_last_error(NULL). */
+bi_status bi_grouped_forward_noalloc(void* y, const void* x, const void* w,
+                                     const uint32_t* row_experts, int64_t m, int64_t k, int64_t n,
+                                     int64_t e, bi_dtype dtype, void* stream);
+
 /* ---- introspection ---------------------------------------------------- */
 
 /* The dispatcher's choice for a call: 0 = scalar tier, 1 = tensor-core tier.
