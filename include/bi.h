@@ -134,15 +134,15 @@ bi_status bi_backward_dx(bi_engine engine, void* dx, const void* dy, const void*
 /* Weight gradient: dw[K,N] = X[M,K]^T * dY[M,N], reduced over M by the fixed
  * chunk tree.  dw_f32 = 1 writes f32 (no rounding), 0 writes the operand type.
  * Source: ViperLLM ffma.py, _FFMAAddmm.backward (gW = x^T gy, cast back);
- * sgemm-bi 0.1.1.post2 "Use" ("deterministic dW (f32-accumulated)"). */
+ * sgemm-bi 0.1.1.post2 "Use" (the weight gradient is accumulated in f32). */
 bi_status bi_backward_dw(bi_engine engine, void* dw, int dw_f32, const void* x, const void* dy,
                          int64_t m, int64_t k, int64_t n, bi_dtype dtype, void* stream, int tensor_cores);
 
 /* Grouped forward: y[m,:] = round( X[m,:] * W[e(m)]^T ) with W [E,N,K] and
  * e(m) = row_experts[m]; rows with e(m) >= E are +0.  Rows need not be sorted.
  * Source: rublas 0.1.45 src/tensor_grouped/mod.rs, fn grouped_matmul_nt
- * ("Group IDs outside [0,E) denote padding and produce zero rows"; FP32
- * accumulation, one output rounding). */
+ * (an id outside [0,E) marks a padding row whose output is all zeros;
+ * f32 accumulation with a single rounding of the output). */
 bi_status bi_grouped_forward(bi_engine engine, void* y, const void* x, const void* w,
                              const uint32_t* row_experts, int64_t m, int64_t k, int64_t n, int64_t e,
                              bi_dtype dtype, void* stream, int tensor_cores);
@@ -151,7 +151,7 @@ bi_status bi_grouped_forward(bi_engine engine, void* y, const void* x, const voi
  * and dw[e] (f32, [E,N,K]) = sum over the rows of expert e, in ascending row
  * index, of dY[m,:]^T X[m,:]; an expert with no rows gets +0.  dx may be NULL
  * to compute dw only.  Source: rublas 0.1.45 src/tensor_grouped/mod.rs,
- * struct GroupedBackward ("dweights is always FP32") and fn
+ * struct GroupedBackward (the weight gradient is kept in f32) and fn
  * grouped_matmul_nt_backward_segmented_with_strategy (the segment offsets are
  * built inside the library here, from row_experts). */
 bi_status bi_grouped_backward(bi_engine engine, void* dx, float* dw, const void* x, const void* w,
@@ -182,8 +182,8 @@ bi_status bi_grouped_forward_noalloc(void* y, const void* x, const void* w,
 
 /* The dispatcher's choice for a call: 0 = scalar tier, 1 = tensor-core tier.
  * A pure function of its arguments (M is not one of them).  Source:
- * sgemm-bi 0.1.1.post2, "Determinism contracts" ("falls back to the scalar
- * tier when an output dim is < 64 (shape-only dispatch)"). */
+ * sgemm-bi 0.1.1.post2, "Determinism contracts" (shapes with an output
+ * dimension below 64 go to the scalar tier, decided from the shape alone). */
 int bi_dispatch_tier(int pass, bi_dtype dtype, int tensor_cores, int64_t k, int64_t n);
 
 /* Number of kernels this engine has launched since it was created. */
