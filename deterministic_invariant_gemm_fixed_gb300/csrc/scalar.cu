@@ -69,19 +69,22 @@ __device__ __forceinline__ void load8(const T* p, int avail, float (&v)[8]) {
 }
 
 // Shared tile: s[l][i] with l the contraction step, i the row or column.
-struct Smem {
-    float a[2][TK][TM + PAD];
+template <int TMV>
+struct SmemT {
+    float a[2][TK][TMV + PAD];
     float b[2][TK][TN + PAD];
 };
+using Smem = SmemT<TM>;
 
 // 8x8 micro-tile product over one staged block: acc[i][j] chains over l ascending.
-__device__ __forceinline__ void mma_block(const float (*as)[TM + PAD], const float (*bs)[TN + PAD],
+template <int TMV = TM>
+__device__ __forceinline__ void mma_block(const float (*as)[TMV + PAD], const float (*bs)[TN + PAD],
                                           int ty, int tx, float (&acc)[8][8]) {
 #pragma unroll
     for (int l = 0; l < TK; ++l) {
         float a[8], b[8];
         const float4 a0 = *reinterpret_cast<const float4*>(&as[l][ty * 4]);
-        const float4 a1 = *reinterpret_cast<const float4*>(&as[l][64 + ty * 4]);
+        const float4 a1 = *reinterpret_cast<const float4*>(&as[l][TMV / 2 + ty * 4]);
         const float4 b0 = *reinterpret_cast<const float4*>(&bs[l][tx * 4]);
         const float4 b1 = *reinterpret_cast<const float4*>(&bs[l][64 + tx * 4]);
         a[0] = a0.x; a[1] = a0.y; a[2] = a0.z; a[3] = a0.w;
@@ -95,7 +98,9 @@ __device__ __forceinline__ void mma_block(const float (*as)[TM + PAD], const flo
     }
 }
 
-__device__ __forceinline__ int mrow(int ty, int i) { return i < 4 ? ty * 4 + i : 64 + ty * 4 + (i - 4); }
+// Thread (ty, tx) owns rows {4ty..4ty+3, TMV/2+4ty..} and columns {4tx..4tx+3, 64+4tx..}.
+template <int TMV = TM>
+__device__ __forceinline__ int mrow(int ty, int i) { return i < 4 ? ty * 4 + i : TMV / 2 + ty * 4 + (i - 4); }
 
 // ------------------------------------------------------------------ rows kernels
 
@@ -111,9 +116,12 @@ struct RowsArgs {
 };
 
 // out[r, c] = down( chain_l a[r, l] * b(l, c) (+ bias[c]) )
-template <typename T, bool BT, bool GROUPED, bool VEC>
-__global__ void __launch_bounds__(NT) scalar_rows_kernel(const RowsArgs p) {
-    __shared__ __align__(16) Smem sm;
+// TMV = tile height (128 or 64); 2*TMV threads, each owning 8 x 8 outputs.
+template <typename T, bool BT, bool GROUPED, bool VEC, int TMV>
+__global__ void __launch_bounds__(2 * TMV, TMV == 128 ? 2 : 4) scalar_rows_kernel(const RowsArgs p) {
+    constexpr int NTV = 2 * TMV;
+    constexpr int SL = (TK * TN) / (NTV * 8);  // 8-element B slots per thread
+    __shared__ __align__(16) SmemT<TMV> sm;
     const int tid = threadIdx.x, ty = tid / 16, tx = tid % 16;
     const T* A = static_cast<const T*>(p.a);
     const T* B = static_cast<const T*>(p.b);
@@ -121,7 +129,7 @@ __global__ void __launch_bounds__(NT) scalar_rows_kernel(const RowsArgs p) {
     const int64_t c0 = static_cast<int64_t>(blockIdx.y) * TN;
 
     // rows of this tile: r0 + i (dense) or sorted positions of one expert
-    int64_t r0 = static_cast<int64_t>(blockIdx.x) * TM;
+    int64_t r0 = static_cast<int64_t>(blockIdx.x) * TMV;
     int64_t rvalid = p.R - r0;
     uint32_t sbase = 0;
     if (GROUPED) {
@@ -130,52 +138,60 @@ __global__ void __launch_bounds__(NT) scalar_rows_kernel(const RowsArgs p) {
         bool found = false;
         for (; g < p.E; ++g) {
             const int64_t cnt = p.seg[g + 1] - p.seg[g];
-            const int64_t tiles = (cnt + TM - 1) / TM;
+            const int64_t tiles = (cnt + TMV - 1) / TMV;
             if (t < tiles) { found = true; break; }
             t -= tiles;
         }
         if (!found) return;
         const int64_t cnt = p.seg[g + 1] - p.seg[g];
-        sbase = p.seg[g] + static_cast<uint32_t>(t * TM);
-        rvalid = cnt - t * TM;
+        sbase = p.seg[g] + static_cast<uint32_t>(t * TMV);
+        rvalid = cnt - t * TMV;
         B += static_cast<int64_t>(g) * C * L;
     }
-    if (rvalid > TM) rvalid = TM;
+    if (rvalid > TMV) rvalid = TMV;
 
     // global -> register staging of one TK block
-    const int a_row = tid / 2, a_seg = (tid % 2) * 8;          // A: 128 rows x 16 steps
+    const int a_row = tid / 2, a_seg = (tid % 2) * 8;          // A: TMV rows x 16 steps
     int64_t a_src_row = -1;
     if (a_row < rvalid) a_src_row = GROUPED ? static_cast<int64_t>(p.perm[sbase + a_row]) : r0 + a_row;
-    float ra[8], rb[8];
+    float ra[8], rb[SL][8];
     auto load_a = [&](int64_t l0) {
         const int64_t l = l0 + a_seg;
         const int avail = a_src_row < 0 ? 0 : static_cast<int>(lmin(8, lmax(0, L - l)));
         load8<T, VEC>(A + (a_src_row < 0 ? 0 : a_src_row * L + l), avail, ra);
     };
     auto load_b = [&](int64_t l0) {
-        if (BT) {  // b(l, c) = B[c * L + l]: 128 cols x 16 steps
-            const int c = tid / 2, s = (tid % 2) * 8;
-            const int64_t gc = c0 + c, l = l0 + s;
-            const int avail = gc < C ? static_cast<int>(lmin(8, lmax(0, L - l))) : 0;
-            load8<T, VEC>(B + (avail ? gc * L + l : 0), avail, rb);
-        } else {   // b(l, c) = B[l * C + c]: 16 steps x 128 cols
-            const int l = tid / 16, s = (tid % 16) * 8;
-            const int64_t gl = l0 + l, gc = c0 + s;
-            const int avail = gl < L ? static_cast<int>(lmin(8, lmax(0, C - gc))) : 0;
-            load8<T, VEC>(B + (avail ? gl * C + gc : 0), avail, rb);
+#pragma unroll
+        for (int q = 0; q < SL; ++q) {
+            const int e = tid + q * NTV;  // 0..255
+            if (BT) {  // b(l, c) = B[c * L + l]: 128 cols x 16 steps
+                const int c = e / 2, s = (e % 2) * 8;
+                const int64_t gc = c0 + c, l = l0 + s;
+                const int avail = gc < C ? static_cast<int>(lmin(8, lmax(0, L - l))) : 0;
+                load8<T, VEC>(B + (avail ? gc * L + l : 0), avail, rb[q]);
+            } else {   // b(l, c) = B[l * C + c]: 16 steps x 128 cols
+                const int l = e / 16, s = (e % 16) * 8;
+                const int64_t gl = l0 + l, gc = c0 + s;
+                const int avail = gl < L ? static_cast<int>(lmin(8, lmax(0, C - gc))) : 0;
+                load8<T, VEC>(B + (avail ? gl * C + gc : 0), avail, rb[q]);
+            }
         }
     };
     auto store = [&](int buf) {
 #pragma unroll
         for (int i = 0; i < 8; ++i) sm.a[buf][a_seg + i][a_row] = ra[i];
-        if (BT) {
-            const int c = tid / 2, s = (tid % 2) * 8;
 #pragma unroll
-            for (int i = 0; i < 8; ++i) sm.b[buf][s + i][c] = rb[i];
-        } else {
-            const int l = tid / 16, s = (tid % 16) * 8;
-            *reinterpret_cast<float4*>(&sm.b[buf][l][s]) = make_float4(rb[0], rb[1], rb[2], rb[3]);
-            *reinterpret_cast<float4*>(&sm.b[buf][l][s + 4]) = make_float4(rb[4], rb[5], rb[6], rb[7]);
+        for (int q = 0; q < SL; ++q) {
+            const int e = tid + q * NTV;
+            if (BT) {
+                const int c = e / 2, s = (e % 2) * 8;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) sm.b[buf][s + i][c] = rb[q][i];
+            } else {
+                const int l = e / 16, s = (e % 16) * 8;
+                *reinterpret_cast<float4*>(&sm.b[buf][l][s]) = make_float4(rb[q][0], rb[q][1], rb[q][2], rb[q][3]);
+                *reinterpret_cast<float4*>(&sm.b[buf][l][s + 4]) = make_float4(rb[q][4], rb[q][5], rb[q][6], rb[q][7]);
+            }
         }
     };
 
@@ -192,7 +208,7 @@ __global__ void __launch_bounds__(NT) scalar_rows_kernel(const RowsArgs p) {
     for (int64_t kb = 0; kb < nkb; ++kb) {
         const bool more = kb + 1 < nkb;
         if (more) { load_a((kb + 1) * TK); load_b((kb + 1) * TK); }
-        mma_block(sm.a[buf], sm.b[buf], ty, tx, acc);
+        mma_block<TMV>(sm.a[buf], sm.b[buf], ty, tx, acc);
         if (more) store(buf ^ 1);
         __syncthreads();
         buf ^= 1;
@@ -203,7 +219,7 @@ __global__ void __launch_bounds__(NT) scalar_rows_kernel(const RowsArgs p) {
     const T* bias = static_cast<const T*>(p.bias);
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-        const int lr = mrow(ty, i);
+        const int lr = mrow<TMV>(ty, i);
         if (lr >= rvalid) continue;
         const int64_t orow = GROUPED ? static_cast<int64_t>(p.perm[sbase + lr]) : r0 + lr;
 #pragma unroll
@@ -233,7 +249,7 @@ struct DwArgs {
 
 // partial[z][r][c] = chain over the rows of chunk z of a[m, r] * b[m, c]
 template <typename T, bool GROUPED, bool VEC>
-__global__ void __launch_bounds__(NT) scalar_dw_chunk_kernel(const DwArgs p) {
+__global__ void __launch_bounds__(NT, 2) scalar_dw_chunk_kernel(const DwArgs p) {
     __shared__ __align__(16) Smem sm;
     const int tid = threadIdx.x, ty = tid / 16, tx = tid % 16;
     const T* A = static_cast<const T*>(p.a);
@@ -369,23 +385,38 @@ __global__ void dw_tree_grouped_kernel(const float* partials, int64_t RC, const 
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// Row tiles for R rows at tile height tm (grouped: an upper bound over experts).
+int64_t row_tiles_for(int64_t R, int64_t E, bool grouped, int tm) {
+    return (R + tm - 1) / tm + (grouped ? E : 0);
+}
+
 template <typename T, bool BT, bool G>
-cudaError_t rows_t(const LaunchCtx& c, const RowsArgs& a, int64_t row_tiles) {
+cudaError_t rows_t(const LaunchCtx& c, const RowsArgs& a) {
     // 8-element loads need rows of whole 16-byte units and aligned bases
     const int64_t unit = 16 / sizeof(T);
     bool vec = aligned16(a.a) && aligned16(a.b) && a.L % unit == 0 && (BT || a.C % unit == 0);
     if (sizeof(T) == 4) vec = vec && a.L % 4 == 0 && (BT || a.C % 4 == 0);
-    dim3 grid(static_cast<unsigned>(row_tiles), static_cast<unsigned>((a.C + TN - 1) / TN));
-    if (vec) scalar_rows_kernel<T, BT, G, true><<<grid, NT, 0, c.stream>>>(a);
-    else scalar_rows_kernel<T, BT, G, false><<<grid, NT, 0, c.stream>>>(a);
+    // The tile shape does not touch any output's chain, so it may follow the
+    // shape: 64-row tiles when 128-row tiles would leave the SMs under-filled.
+    const int64_t col_tiles = (a.C + TN - 1) / TN;
+    const bool small = row_tiles_for(a.R, a.E, G, 128) * col_tiles < int64_t(c.sm_count) * 6;
+    if (small) {
+        dim3 grid(static_cast<unsigned>(row_tiles_for(a.R, a.E, G, 64)), static_cast<unsigned>(col_tiles));
+        if (vec) scalar_rows_kernel<T, BT, G, true, 64><<<grid, 128, 0, c.stream>>>(a);
+        else scalar_rows_kernel<T, BT, G, false, 64><<<grid, 128, 0, c.stream>>>(a);
+    } else {
+        dim3 grid(static_cast<unsigned>(row_tiles_for(a.R, a.E, G, 128)), static_cast<unsigned>(col_tiles));
+        if (vec) scalar_rows_kernel<T, BT, G, true, 128><<<grid, 256, 0, c.stream>>>(a);
+        else scalar_rows_kernel<T, BT, G, false, 128><<<grid, 256, 0, c.stream>>>(a);
+    }
     c.count();
     return cudaGetLastError();
 }
 
 template <typename T>
-cudaError_t rows_dispatch(const LaunchCtx& c, const RowsArgs& a, int bt, bool grouped, int64_t tiles) {
-    if (grouped) return bt ? rows_t<T, true, true>(c, a, tiles) : rows_t<T, false, true>(c, a, tiles);
-    return bt ? rows_t<T, true, false>(c, a, tiles) : rows_t<T, false, false>(c, a, tiles);
+cudaError_t rows_dispatch(const LaunchCtx& c, const RowsArgs& a, int bt, bool grouped) {
+    if (grouped) return bt ? rows_t<T, true, true>(c, a) : rows_t<T, false, true>(c, a);
+    return bt ? rows_t<T, true, false>(c, a) : rows_t<T, false, false>(c, a);
 }
 
 template <typename T, bool G>
@@ -411,11 +442,10 @@ unsigned tree_grid(int64_t n, int sm) {
 cudaError_t scalar_rows(const LaunchCtx& c, bi_dtype dt, void* out, const void* a, const void* b,
                         const void* bias, int64_t R, int64_t L, int64_t C, int b_contr_contig) {
     RowsArgs args{out, a, b, bias, R, L, C, 0, nullptr, nullptr};
-    const int64_t tiles = (R + TM - 1) / TM;
     switch (dt) {
-        case BI_F32: return rows_dispatch<float>(c, args, b_contr_contig, false, tiles);
-        case BI_BF16: return rows_dispatch<__nv_bfloat16>(c, args, b_contr_contig, false, tiles);
-        default: return rows_dispatch<__half>(c, args, b_contr_contig, false, tiles);
+        case BI_F32: return rows_dispatch<float>(c, args, b_contr_contig, false);
+        case BI_BF16: return rows_dispatch<__nv_bfloat16>(c, args, b_contr_contig, false);
+        default: return rows_dispatch<__half>(c, args, b_contr_contig, false);
     }
 }
 
@@ -423,11 +453,10 @@ cudaError_t scalar_rows_grouped(const LaunchCtx& c, bi_dtype dt, void* out, cons
                                 const void* b, int64_t M, int64_t L, int64_t C, int64_t E,
                                 int b_contr_contig, const uint32_t* seg, const uint32_t* perm) {
     RowsArgs args{out, a, b, nullptr, M, L, C, E, seg, perm};
-    const int64_t tiles = (M + TM - 1) / TM + E;  // upper bound over per-expert tiles
     switch (dt) {
-        case BI_F32: return rows_dispatch<float>(c, args, b_contr_contig, true, tiles);
-        case BI_BF16: return rows_dispatch<__nv_bfloat16>(c, args, b_contr_contig, true, tiles);
-        default: return rows_dispatch<__half>(c, args, b_contr_contig, true, tiles);
+        case BI_F32: return rows_dispatch<float>(c, args, b_contr_contig, true);
+        case BI_BF16: return rows_dispatch<__nv_bfloat16>(c, args, b_contr_contig, true);
+        default: return rows_dispatch<__half>(c, args, b_contr_contig, true);
     }
 }
 
