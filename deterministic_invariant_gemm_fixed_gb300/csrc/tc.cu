@@ -579,6 +579,295 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
 }
 
+// ---------------------------------------------------------------- CTA-pair kernel
+//
+// Dense passes on a pair of CTAs (a 2-CTA cluster) that run one
+// tcgen05.mma.cta_group::2 of shape M256 x N256 x K16: CTA r of the pair holds
+// rows [128r, 128r+128) of the A tile and columns [128r, 128r+128) of the B
+// tile in its own shared memory, and receives rows [128r, 128r+128) of the
+// 256 x 256 accumulator in its own tensor memory.  Only CTA 0 issues MMAs.
+// Per CTA a 64-wide contraction block is 32 KB (A 16 KB + B 16 KB), so a
+// 6-stage ring fits.  The arithmetic of each output element is the same
+// ascending chain of K16 blocks as in tc_gemm_kernel; only the instruction
+// shape and the CTA mapping differ, both fixed by the pass, never by M.
+//
+// Barriers: full[s] (CTA 0, count 1, 64 KB expected from both CTAs' copies),
+// empty[s] (each CTA, released by CTA 0's commit multicast to both), tfull[b]
+// (each CTA, commit multicast), tempty[b] (CTA 0, 8 arrivals: the 4 epilogue
+// warps of each CTA).
+constexpr int P_STAGES = 6;
+constexpr int P_A_BYTES = 128 * BK * 2;
+constexpr int P_B_BYTES = 128 * BK * 2;
+constexpr int P_STAGE_BYTES = P_A_BYTES + P_B_BYTES;
+constexpr int P_SMEM_BYTES = 1024 + P_STAGES * P_STAGE_BYTES + BAR_BYTES;
+
+__device__ __forceinline__ uint32_t mapa_rank(uint32_t saddr, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+    return r;
+}
+
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap* map, int x, int y,
+                                                 uint32_t bar_cluster) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar_cluster)
+        : "memory");
+}
+
+__device__ __forceinline__ void mma_f16_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                             uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+__device__ __forceinline__ void mma_commit_pair_mc(uint32_t bar, uint16_t mask) {
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+        " [%0], %1;" ::"r"(bar), "h"(mask)
+        : "memory");
+}
+
+__device__ __forceinline__ void mma_commit_pair(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar_cluster) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster)
+                 : "memory");
+}
+
+template <int FMT, bool A_MN, bool B_MN>
+__device__ __forceinline__ constexpr uint32_t instr_desc_pair() {
+    return (1u << 4) | (static_cast<uint32_t>(FMT) << 7) | (static_cast<uint32_t>(FMT) << 10) |
+           (static_cast<uint32_t>(A_MN) << 15) | (static_cast<uint32_t>(B_MN) << 16) |
+           (static_cast<uint32_t>(256 >> 3) << 17) | (static_cast<uint32_t>(256 >> 4) << 24);
+}
+
+template <int FMT, bool A_MN, bool B_MN, bool OUT_F32>
+__global__ void __launch_bounds__(THREADS, 1)
+    tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                        const Params p) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    uint8_t* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
+    const uint32_t sbase = smem_u32(smem);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + P_STAGES * P_STAGE_BYTES);
+    const uint32_t bar0 = smem_u32(bars);
+    auto full_bar = [&](int s) { return bar0 + 8u * s; };
+    auto empty_bar = [&](int s) { return bar0 + 8u * (P_STAGES + s); };
+    auto tfull_bar = [&](int b) { return bar0 + 8u * (2 * P_STAGES + b); };
+    auto tempty_bar = [&](int b) { return bar0 + 8u * (2 * P_STAGES + 2 + b); };
+    const uint32_t drain_bar = bar0 + 8u * (2 * P_STAGES + 4);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * P_STAGES + 5);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const uint32_t crank = blockIdx.x & 1u;
+    const int cidx = static_cast<int>(blockIdx.x >> 1);
+    const int ncl = static_cast<int>(gridDim.x >> 1);
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < P_STAGES; ++s) {
+            mbar_init(full_bar(s), 1);
+            mbar_init(empty_bar(s), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(tfull_bar(b), 1);
+            mbar_init(tempty_bar(b), 8);
+        }
+        mbar_init(drain_bar, 1);
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 1) {  // one warp of each CTA of the pair allocates together
+        asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         smem_u32(tmem_slot)),
+                     "r"(TMEM_COLS)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync();
+    tc_fence_after();
+    const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
+
+    const int units_m = (p.num_m + 1) / 2;  // 256-row pair tiles
+    const int total = units_m * p.num_n;
+    auto unit_tile = [&](int t, int& mpair, int& nb) {
+        const int span = GROUP_M * p.num_n;
+        const int grp = t / span;
+        const int first = grp * GROUP_M;
+        const int gsize = min(units_m - first, GROUP_M);
+        const int r = t - grp * span;
+        mpair = first + r % gsize;
+        nb = r / gsize;
+    };
+
+    if (warp == 0 && lane == 0) {
+        // ------------------------------------------------------------ producer (both CTAs)
+        int s = 0;
+        uint32_t ph = 0;
+        for (int t = cidx; t < total; t += ncl) {
+            int mpair, nb;
+            unit_tile(t, mpair, nb);
+            const int arow = mpair * 256 + static_cast<int>(crank) * 128;  // A rows of this CTA
+            const int bcol = nb * BN + static_cast<int>(crank) * 128;      // B cols of this CTA
+            for (int kb = 0; kb < p.num_kb; ++kb) {
+                if (!mbar_wait(empty_bar(s), ph ^ 1u, abort_flag, p, DEV_TIMEOUT_PRODUCER)) goto done_p;
+                const uint32_t fb_leader = mapa_rank(full_bar(s), 0);
+                if (crank == 0) mbar_expect_tx(full_bar(s), 2 * P_STAGE_BYTES);
+                const uint32_t a_dst = sbase + s * P_STAGE_BYTES;
+                const uint32_t b_dst = a_dst + P_A_BYTES;
+                const int kofs = kb * BK;
+                if (A_MN) {
+                    for (int a = 0; a < 2; ++a)
+                        tma_load_2d_pair(a_dst + a * (BK * 128), &tmA, arow + a * 64, kofs, fb_leader);
+                } else {
+                    tma_load_2d_pair(a_dst, &tmA, kofs, arow, fb_leader);
+                }
+                if (B_MN) {
+                    for (int b = 0; b < 2; ++b)
+                        tma_load_2d_pair(b_dst + b * (BK * 128), &tmB, bcol + b * 64, kofs, fb_leader);
+                } else {
+                    tma_load_2d_pair(b_dst, &tmB, kofs, bcol, fb_leader);
+                }
+                if (++s == P_STAGES) { s = 0; ph ^= 1u; }
+            }
+        }
+    done_p:;
+        // Copies of this CTA complete on CTA 0's barriers; CTA 0's MMA thread
+        // consumes them before it finishes, and the pair meets at the cluster
+        // barrier below before either CTA releases its shared memory.
+    } else if (warp == 1 && lane == 0 && crank == 0) {
+        // ------------------------------------------------------------ MMA issuer (CTA 0)
+        constexpr uint32_t idesc = instr_desc_pair<FMT, A_MN, B_MN>();
+        int s = 0;
+        uint32_t ph = 0;
+        int ab = 0;
+        uint32_t aph = 0;
+        for (int t = cidx; t < total; t += ncl) {
+            if (!mbar_wait(tempty_bar(ab), aph ^ 1u, abort_flag, p, DEV_TIMEOUT_MMA)) break;
+            tc_fence_after();
+            const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(ab * BN);
+            bool ok = true;
+            for (int kb = 0; kb < p.num_kb; ++kb) {
+                if (!mbar_wait(full_bar(s), ph, abort_flag, p, DEV_TIMEOUT_MMA)) { ok = false; break; }
+                tc_fence_after();
+                const uint32_t a_s = sbase + s * P_STAGE_BYTES;
+                const uint32_t b_s = a_s + P_A_BYTES;
+#pragma unroll
+                for (int kk = 0; kk < BK / UK; ++kk) {
+                    const uint64_t ad = A_MN ? smem_desc(a_s + kk * 2048, BK * 128, 1024)
+                                             : smem_desc(a_s + kk * 32, 16, 1024);
+                    const uint64_t bd = B_MN ? smem_desc(b_s + kk * 2048, BK * 128, 1024)
+                                             : smem_desc(b_s + kk * 32, 16, 1024);
+                    mma_f16_pair(d_tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+                }
+                mma_commit_pair_mc(empty_bar(s), 0x3);
+                if (++s == P_STAGES) { s = 0; ph ^= 1u; }
+            }
+            if (!ok) break;
+            mma_commit_pair_mc(tfull_bar(ab), 0x3);
+            if (++ab == 2) { ab = 0; aph ^= 1u; }
+        }
+        mma_commit_pair(drain_bar);
+        mbar_wait(drain_bar, 0, abort_flag, p, DEV_TIMEOUT_MMA);
+    } else if (warp >= 2) {
+        // ------------------------------------------------------------ epilogue (both CTAs)
+        const int q = warp & 3;
+        const int r = q * 32 + lane;
+        const uint32_t tempty_leader0 = mapa_rank(tempty_bar(0), 0);
+        const uint32_t tempty_leader1 = mapa_rank(tempty_bar(1), 0);
+        int ab = 0;
+        uint32_t aph = 0;
+        for (int t = cidx; t < total; t += ncl) {
+            int mpair, nb;
+            unit_tile(t, mpair, nb);
+            const int64_t gr = static_cast<int64_t>(mpair) * 256 + crank * 128 + r;
+            const int64_t orow = gr < p.rows ? gr : -1;
+            const int64_t col0 = static_cast<int64_t>(nb) * BN;
+            bool ok = mbar_wait(tfull_bar(ab), aph, abort_flag, p, DEV_TIMEOUT_EPILOGUE);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) break;
+            tc_fence_after();
+            const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
+                                   static_cast<uint32_t>(ab * BN);
+            for (int c0 = 0; c0 < BN; c0 += 16) {
+                if (col0 + c0 >= p.cols) break;
+                uint32_t v[16];
+                tmem_ld16(tbase + c0, v);
+                if (orow < 0) continue;
+                float f[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) f[i] = __uint_as_float(v[i]);
+                const int64_t cb = col0 + c0;
+                if (p.bias != nullptr) {
+#pragma unroll
+                    for (int i = 0; i < 16; ++i)
+                        if (cb + i < p.cols) f[i] = f[i] + OutT<FMT>::load(p.bias, cb + i);
+                }
+                const bool full = cb + 16 <= p.cols;
+                if (OUT_F32) {
+                    float* dst = static_cast<float*>(p.out) + orow * p.ldo + cb;
+                    if (full) {
+#pragma unroll
+                        for (int i = 0; i < 16; i += 4)
+                            *reinterpret_cast<float4*>(dst + i) = make_float4(f[i], f[i + 1], f[i + 2], f[i + 3]);
+                    } else {
+                        for (int i = 0; i < 16; ++i)
+                            if (cb + i < p.cols) dst[i] = f[i];
+                    }
+                } else {
+                    using T = typename OutT<FMT>::T;
+                    T* dst = static_cast<T*>(p.out) + orow * p.ldo + cb;
+                    if (full) {
+                        uint4 w0, w1;
+                        w0.x = OutT<FMT>::pack(f[0], f[1]);
+                        w0.y = OutT<FMT>::pack(f[2], f[3]);
+                        w0.z = OutT<FMT>::pack(f[4], f[5]);
+                        w0.w = OutT<FMT>::pack(f[6], f[7]);
+                        w1.x = OutT<FMT>::pack(f[8], f[9]);
+                        w1.y = OutT<FMT>::pack(f[10], f[11]);
+                        w1.z = OutT<FMT>::pack(f[12], f[13]);
+                        w1.w = OutT<FMT>::pack(f[14], f[15]);
+                        reinterpret_cast<uint4*>(dst)[0] = w0;
+                        reinterpret_cast<uint4*>(dst)[1] = w1;
+                    } else {
+                        for (int i = 0; i < 16; ++i)
+                            if (cb + i < p.cols) OutT<FMT>::store1(dst, i, f[i]);
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster(ab ? tempty_leader1 : tempty_leader0);
+            if (++ab == 2) { ab = 0; aph ^= 1u; }
+        }
+    }
+
+    // ---------------------------------------------------------------- teardown
+    tc_fence_before();
+    __syncthreads();
+    __syncwarp();
+    cluster_sync();  // CTA 0's MMAs have finished reading both CTAs' shared memory
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
+                     "r"(TMEM_COLS)
+                     : "memory");
+    }
+}
+
 // ---------------------------------------------------------------- host side
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -668,6 +957,50 @@ cudaError_t launch(const LaunchCtx& c, const CUtensorMap& a, const CUtensorMap& 
     return cudaGetLastError();
 }
 
+
+template <int FMT, bool A_MN, bool B_MN, bool OUT_F32>
+cudaError_t launch_pair(const LaunchCtx& c, const CUtensorMap& a, const CUtensorMap& b, Params p) {
+    auto kern = tc_gemm_pair_kernel<FMT, A_MN, B_MN, OUT_F32>;
+    static std::once_flag once;
+    static cudaError_t attr_err = cudaSuccess;
+    static int max_clusters = 0;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = 2;
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = 1;
+    std::call_once(once, [&] {
+        attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, P_SMEM_BYTES);
+        if (attr_err == cudaSuccess) {
+            cudaLaunchConfig_t q = {};
+            q.gridDim = dim3(128);
+            q.blockDim = dim3(THREADS);
+            q.dynamicSmemBytes = P_SMEM_BYTES;
+            q.attrs = at;
+            q.numAttrs = 1;
+            attr_err = cudaOccupancyMaxActiveClusters(&max_clusters, kern, &q);
+            if (attr_err == cudaSuccess && max_clusters < 1) attr_err = cudaErrorInvalidConfiguration;
+        }
+    });
+    if (attr_err != cudaSuccess) return attr_err;
+    const int64_t units = int64_t((p.num_m + 1) / 2) * p.num_n;
+    if (units <= 0) return cudaSuccess;
+    p.status = c.status;
+    p.wait_limit = c.wait_limit_ns;
+    const int64_t clusters = units < max_clusters ? units : max_clusters;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(clusters * 2));
+    cfg.blockDim = dim3(THREADS);
+    cfg.dynamicSmemBytes = P_SMEM_BYTES;
+    cfg.stream = c.stream;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, a, b, p);
+    if (e != cudaSuccess) return e;
+    c.count();
+    return cudaGetLastError();
+}
+
 template <int FMT>
 cudaError_t forward_t(const LaunchCtx& c, bi_dtype dt, void* y, const void* x, const void* w,
                       const void* bias, int64_t M, int64_t K, int64_t N) {
@@ -680,7 +1013,7 @@ cudaError_t forward_t(const LaunchCtx& c, bi_dtype dt, void* y, const void* x, c
     p.num_m = static_cast<int>((M + BM - 1) / BM);
     p.num_n = static_cast<int>((N + BN - 1) / BN);
     p.num_kb = static_cast<int>((K + BK - 1) / BK);
-    return launch<FMT, false, true, false, DENSE, false, 2>(c, a, b, p, int64_t((p.num_m + 1) / 2) * p.num_n);
+    return launch_pair<FMT, false, true, false>(c, a, b, p);
 }
 
 template <int FMT>
@@ -695,7 +1028,7 @@ cudaError_t dx_t(const LaunchCtx& c, bi_dtype dt, void* dx, const void* dy, cons
     p.num_m = static_cast<int>((M + BM - 1) / BM);
     p.num_n = static_cast<int>((K + BN - 1) / BN);
     p.num_kb = static_cast<int>((N + BK - 1) / BK);
-    return launch<FMT, false, false, false, DENSE, false, 2>(c, a, b, p, int64_t((p.num_m + 1) / 2) * p.num_n);
+    return launch_pair<FMT, false, false, false>(c, a, b, p);
 }
 
 template <int FMT, bool F32>
@@ -710,7 +1043,7 @@ cudaError_t dw_t(const LaunchCtx& c, bi_dtype dt, void* dw, const void* x, const
     p.num_m = static_cast<int>((K + BM - 1) / BM);
     p.num_n = static_cast<int>((N + BN - 1) / BN);
     p.num_kb = static_cast<int>((M + BK - 1) / BK);
-    return launch<FMT, true, true, false, DENSE, F32, 2>(c, a, b, p, int64_t((p.num_m + 1) / 2) * p.num_n);
+    return launch_pair<FMT, true, true, F32>(c, a, b, p);
 }
 
 template <int FMT>
