@@ -587,7 +587,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 // tile in its own shared memory, and receives rows [128r, 128r+128) of the
 // 256 x 256 accumulator in its own tensor memory.  Only CTA 0 issues MMAs.
 // Per CTA a 64-wide contraction block is 32 KB (A 16 KB + B 16 KB), so a
-// 6-stage ring fits.  The arithmetic of each output element is the same
+// 7-stage ring fits.  The arithmetic of each output element is the same
 // ascending chain of K16 blocks as in tc_gemm_kernel; only the instruction
 // shape and the CTA mapping differ, both fixed by the pass, never by M.
 //
@@ -595,7 +595,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 // empty[s] (each CTA, released by CTA 0's commit multicast to both), tfull[b]
 // (each CTA, commit multicast), tempty[b] (CTA 0, 8 arrivals: the 4 epilogue
 // warps of each CTA).
-constexpr int P_STAGES = 6;
+constexpr int P_STAGES = 7;
 constexpr int P_A_BYTES = 128 * BK * 2;
 constexpr int P_B_BYTES = 128 * BK * 2;
 constexpr int P_STAGE_BYTES = P_A_BYTES + P_B_BYTES;
