@@ -208,11 +208,21 @@ def oracle_sample(rows=512, cols=128, seed=0):
     return total_t, total_fl, oracle.num_threads(), desc
 
 
+PAIR_BEGIN = "// ---------------------------------------------------------------- CTA-pair kernel"
+PAIR_END = "// ---------------------------------------------------------------- host side"
+
+
+def pair_kernel_sha():
+    """sha256 prefix of the CTA-pair kernel's source text (the dense passes)."""
+    src = open(os.path.join(ROOT, "deterministic_invariant_gemm_fixed_gb300", "csrc", "tc.cu")).read()
+    i, j = src.find(PAIR_BEGIN), src.find(PAIR_END)
+    return hashlib.sha256(src[i:j].encode()).hexdigest()[:16]
+
+
 def traffic_from_profiles(kernel_tag):
     """DRAM bytes per launch recorded by an ncu capture summary under profiles/,
-    valid only while the kernel source is unchanged (sha256 of csrc/tc.cu)."""
-    src = os.path.join(ROOT, "deterministic_invariant_gemm_fixed_gb300", "csrc", "tc.cu")
-    sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    valid only while the kernel's source is unchanged (see pair_kernel_sha)."""
+    sha = pair_kernel_sha()
     pdir = os.path.join(ROOT, "profiles")
     if not os.path.isdir(pdir):
         return None
@@ -224,7 +234,7 @@ def traffic_from_profiles(kernel_tag):
             if not mo:
                 continue
             d = json.loads(mo.group(1))
-            if d.get("kernel") == kernel_tag and d.get("tc_cu_sha256_16") == sha:
+            if d.get("kernel") == kernel_tag and d.get("pair_kernel_sha256_16") == sha:
                 return float(d["bytes_per_launch"])
     return None
 
@@ -388,8 +398,9 @@ def our_arm(args, rank, world):
     peak = float(pk.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
     d = per[dom]
     achieved = d["fl"] / d["n"] / (d["t"] / d["n"]) / 1e12
-    kernel_tag = {"fwd": "tc_gemm fwd (A K-major, B MN-major)", "dx": "tc_gemm dX (A K-major, B K-major)",
-                  "dw": "tc_gemm dW (A MN-major, B MN-major, f32 out)"}[dom]
+    kernel_tag = {"fwd": "tc_gemm_pair_kernel fwd (A K-major, B MN-major)",
+                  "dx": "tc_gemm_pair_kernel dX (A K-major, B K-major)",
+                  "dw": "tc_gemm_pair_kernel dW (A MN-major, B MN-major, f32 out)"}[dom]
     traffic = traffic_from_profiles(dom)
     passes = {p: {"tflops": v["fl"] / v["t"] / 1e12, "share": v["t"] / total_t,
                   "by_projection_tflops": {nm: f / t / 1e12 for nm, (f, t) in v["by_proj"].items()}}

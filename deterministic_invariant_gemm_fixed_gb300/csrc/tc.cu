@@ -1,18 +1,21 @@
-// Tensor-core tier: one persistent, warp-specialised tcgen05 GEMM kernel for sm_103a.
+// Tensor-core tier: persistent, warp-specialised tcgen05 GEMM kernels for sm_103a.
 //
 // Contract (sgemm-bi 0.1.1.post2, "Determinism contracts", row "tensor cores"):
 // f32 accumulation, bit-identical across runs, each output row independent of M.
-// The kernel keeps every arithmetic choice fixed by (pass, dtype, K, N):
-//   - one MMA shape, M128 x N256 x K16 (tcgen05.mma.cta_group::1.kind::f16),
-//     f32 accumulator in tensor memory;
+// Every arithmetic choice is fixed by (pass, dtype, K, N):
+//   - one MMA shape per pass family: the dense passes run
+//     tcgen05.mma.cta_group::2 M256 x N256 x K16 on a CTA pair
+//     (tc_gemm_pair_kernel), the grouped passes run tcgen05.mma.cta_group::1
+//     M128 x N256 x K16 on single CTAs (tc_gemm_kernel); f32 accumulators live
+//     in tensor memory;
 //   - the contracted index is walked in 64-wide blocks in ascending order, four
 //     K16 instructions per block, accumulating into the same TMEM tile;
 //   - no split of the contraction, no atomics, no stream-K;
 //   - M only decides how many tiles exist and which CTA runs which tile, which
 //     cannot change the arithmetic of any output element.
 //
-// Roles (192 threads):
-//   warp 0 lane 0  TMA producer: cp.async.bulk.tensor loads into a 4-stage ring
+// Roles (192 threads per CTA):
+//   warp 0 lane 0  TMA producer: cp.async.bulk.tensor loads into a ring of stages
 //   warp 1 lane 0  MMA issuer (warp 1 also owns the TMEM allocation)
 //   warps 2..5     epilogue: tcgen05.ld -> (+bias) -> one rounding -> st.global
 // The accumulator is double-buffered (2 x 256 TMEM columns) so the epilogue of
@@ -134,19 +137,6 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
         : "memory");
 }
 
-// Same as tma_load_2d, but the box is written at the same shared-memory offset
-// in every CTA of the cluster named by `mask`, and each of those CTAs' mbarrier
-// at offset `bar` receives the transaction bytes.  The source is this GPU's
-// own global memory.
-__device__ __forceinline__ void tma_load_2d_mc(uint32_t dst, const CUtensorMap* map, int x, int y,
-                                               uint32_t bar, uint16_t mask) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
-        " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar), "h"(mask)
-        : "memory");
-}
-
 __device__ __forceinline__ void cluster_sync() {
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
@@ -192,14 +182,6 @@ __device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t adesc, uint64_
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
     asm volatile(
         "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-        : "memory");
-}
-
-// Commit that arrives on the mbarrier at offset `bar` of every CTA in `mask`.
-__device__ __forceinline__ void mma_commit_mc(uint32_t bar, uint16_t mask) {
-    asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-        " [%0], %1;" ::"r"(bar), "h"(mask)
         : "memory");
 }
 
@@ -253,20 +235,17 @@ struct Tile {
     uint32_t sbase; // grouped rows: sorted position of the tile's first row
 };
 
-// t indexes work units: single tiles (CL = 1) or pairs of vertically adjacent
-// tiles that share their B tile (CL = 2; `rank` picks the row tile of the pair).
-template <int MODE, int CL>
-__device__ __forceinline__ bool get_tile(const Params& p, int t, int rank, Tile& ti) {
+template <int MODE>
+__device__ __forceinline__ bool get_tile(const Params& p, int t, Tile& ti) {
     if (MODE == DENSE) {
-        const int units_m = (p.num_m + CL - 1) / CL;
-        const int total = units_m * p.num_n;
+        const int total = p.num_m * p.num_n;
         if (t >= total) return false;
         const int span = GROUP_M * p.num_n;
         const int grp = t / span;
         const int first_m = grp * GROUP_M;
-        const int gsize = min(units_m - first_m, GROUP_M);
+        const int gsize = min(p.num_m - first_m, GROUP_M);
         const int r = t - grp * span;
-        ti.m_blk = (first_m + r % gsize) * CL + rank;  // may be num_m for an odd last pair
+        ti.m_blk = first_m + r % gsize;
         ti.n_blk = r / gsize;
         ti.g = 0;
         ti.nkb = p.num_kb;
@@ -315,7 +294,7 @@ __device__ __forceinline__ bool get_tile(const Params& p, int t, int rank, Tile&
 
 // ---------------------------------------------------------------- the kernel
 
-template <int FMT, bool A_MN, bool B_MN, bool B3D, int MODE, bool OUT_F32, int CL>
+template <int FMT, bool A_MN, bool B_MN, bool B3D, int MODE, bool OUT_F32>
 __global__ void __launch_bounds__(THREADS, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const Params p) {
@@ -335,16 +314,11 @@ __global__ void __launch_bounds__(THREADS, 1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    // cluster of CL CTAs (1-D grid, cluster dims (CL,1,1)): rank inside the
-    // cluster, cluster index, number of clusters
-    const int crank = CL == 2 ? static_cast<int>(blockIdx.x & 1u) : 0;
-    const int cidx = static_cast<int>(blockIdx.x) / CL;
-    const int ncl = static_cast<int>(gridDim.x) / CL;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(full_bar(s), 1);
-            mbar_init(empty_bar(s), CL);  // released by the MMAs of every CTA that reads the stage
+            mbar_init(empty_bar(s), 1);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(tfull_bar(b), 1);
@@ -363,7 +337,6 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
     tc_fence_before();
     __syncthreads();
-    if (CL == 2) cluster_sync();  // the peer's barriers exist before any multicast reaches them
     tc_fence_after();
     const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
 
@@ -373,7 +346,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         uint32_t ph = 0;
         uint32_t used = 0, last_par = 0;  // per stage: ever issued / parity of the last issue
         Tile ti;
-        for (int t = cidx; get_tile<MODE, CL>(p, t, crank, ti); t += ncl) {
+        for (int t = blockIdx.x; get_tile<MODE>(p, t, ti); t += gridDim.x) {
             if (ti.nkb == 0) continue;
             for (int kb = 0; kb < ti.nkb; ++kb) {
                 if (!mbar_wait(empty_bar(s), ph ^ 1u, abort_flag, p, DEV_TIMEOUT_PRODUCER)) goto drain;
@@ -407,16 +380,6 @@ __global__ void __launch_bounds__(THREADS, 1)
                     } else {
                         tma_load_3d(b_dst, &tmB, kofs, ti.n_blk * BN, ti.g, fb);
                     }
-                } else if (CL == 2) {
-                    // this CTA fetches its half of the shared B tile for both CTAs
-                    if (B_MN) {
-                        for (int b = crank * 2; b < crank * 2 + 2; ++b)
-                            tma_load_2d_mc(b_dst + b * (BK * 128), &tmB, ti.n_blk * BN + b * 64, kofs,
-                                           fb, 0x3);
-                    } else {
-                        tma_load_2d_mc(b_dst + crank * (BN / 2) * 128, &tmB, kofs,
-                                       ti.n_blk * BN + crank * (BN / 2), fb, 0x3);
-                    }
                 } else if (B_MN) {
                     for (int b = 0; b < BN / 64; ++b)
                         tma_load_2d(b_dst + b * (BK * 128), &tmB, ti.n_blk * BN + b * 64, kofs, fb);
@@ -444,7 +407,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         int ab = 0;
         uint32_t aph = 0;
         Tile ti;
-        for (int t = cidx; get_tile<MODE, CL>(p, t, crank, ti); t += ncl) {
+        for (int t = blockIdx.x; get_tile<MODE>(p, t, ti); t += gridDim.x) {
             if (ti.nkb == 0) continue;
             if (!mbar_wait(tempty_bar(ab), aph ^ 1u, abort_flag, p, DEV_TIMEOUT_MMA)) break;
             tc_fence_after();
@@ -465,10 +428,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                                             : smem_desc(b_s + kk * 32, 16, 1024);
                     mma_f16(d_tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
                 }
-                // frees the stage once these MMAs have read it (in both CTAs of a
-                // pair: the peer's next multicast writes into this CTA's stage too)
-                if (CL == 2) mma_commit_mc(empty_bar(s), 0x3);
-                else mma_commit(empty_bar(s));
+                mma_commit(empty_bar(s));  // frees the stage once these MMAs have read it
                 if (++s == STAGES) { s = 0; ph ^= 1u; }
             }
             if (!ok) break;
@@ -485,7 +445,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         int ab = 0;
         uint32_t aph = 0;
         Tile ti;
-        for (int t = cidx; get_tile<MODE, CL>(p, t, crank, ti); t += ncl) {
+        for (int t = blockIdx.x; get_tile<MODE>(p, t, ti); t += gridDim.x) {
             // output row of this thread (or -1)
             int64_t orow = -1;
             void* out = p.out;
@@ -568,8 +528,6 @@ __global__ void __launch_bounds__(THREADS, 1)
     // ---------------------------------------------------------------- teardown
     tc_fence_before();
     __syncthreads();
-    __syncwarp();
-    if (CL == 2) cluster_sync();  // no CTA leaves while its peer may still signal it
     if (warp == 1) {
         __syncwarp();
         tc_fence_after();
@@ -903,56 +861,21 @@ cudaError_t make_map(CUtensorMap* m, bi_dtype dt, const void* ptr, uint64_t inne
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-// units_upper: work units (tiles, or tile pairs when CL = 2) an upper bound of.
-template <int FMT, bool A_MN, bool B_MN, bool B3D, int MODE, bool OUT_F32, int CL = 1>
+template <int FMT, bool A_MN, bool B_MN, bool B3D, int MODE, bool OUT_F32>
 cudaError_t launch(const LaunchCtx& c, const CUtensorMap& a, const CUtensorMap& b, Params p,
-                   int64_t units_upper) {
-    auto kern = tc_gemm_kernel<FMT, A_MN, B_MN, B3D, MODE, OUT_F32, CL>;
+                   int64_t tiles_upper) {
+    auto kern = tc_gemm_kernel<FMT, A_MN, B_MN, B3D, MODE, OUT_F32>;
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
-    static int max_clusters = 0;
     std::call_once(once, [&] {
         attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
-        if (attr_err == cudaSuccess && CL > 1) {
-            cudaLaunchConfig_t q = {};
-            q.gridDim = dim3(CL * 64);
-            q.blockDim = dim3(THREADS);
-            q.dynamicSmemBytes = SMEM_BYTES;
-            cudaLaunchAttribute at[1];
-            at[0].id = cudaLaunchAttributeClusterDimension;
-            at[0].val.clusterDim.x = CL;
-            at[0].val.clusterDim.y = 1;
-            at[0].val.clusterDim.z = 1;
-            q.attrs = at;
-            q.numAttrs = 1;
-            attr_err = cudaOccupancyMaxActiveClusters(&max_clusters, kern, &q);
-            if (attr_err == cudaSuccess && max_clusters < 1) attr_err = cudaErrorInvalidConfiguration;
-        }
     });
     if (attr_err != cudaSuccess) return attr_err;
-    if (units_upper <= 0) return cudaSuccess;
+    if (tiles_upper <= 0) return cudaSuccess;
+    const int grid = static_cast<int>(tiles_upper < c.sm_count ? tiles_upper : c.sm_count);
     p.status = c.status;
     p.wait_limit = c.wait_limit_ns;
-    if (CL == 1) {
-        const int grid = static_cast<int>(units_upper < c.sm_count ? units_upper : c.sm_count);
-        kern<<<grid, THREADS, SMEM_BYTES, c.stream>>>(a, b, p);
-    } else {
-        const int64_t clusters = units_upper < max_clusters ? units_upper : max_clusters;
-        cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3(static_cast<unsigned>(clusters * CL));
-        cfg.blockDim = dim3(THREADS);
-        cfg.dynamicSmemBytes = SMEM_BYTES;
-        cfg.stream = c.stream;
-        cudaLaunchAttribute at[1];
-        at[0].id = cudaLaunchAttributeClusterDimension;
-        at[0].val.clusterDim.x = CL;
-        at[0].val.clusterDim.y = 1;
-        at[0].val.clusterDim.z = 1;
-        cfg.attrs = at;
-        cfg.numAttrs = 1;
-        cudaError_t e = cudaLaunchKernelEx(&cfg, kern, a, b, p);
-        if (e != cudaSuccess) return e;
-    }
+    kern<<<grid, THREADS, SMEM_BYTES, c.stream>>>(a, b, p);
     c.count();
     return cudaGetLastError();
 }
