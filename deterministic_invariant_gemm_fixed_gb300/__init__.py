@@ -39,6 +39,7 @@ SIGNATURES = {
     "bi_forward": (_i32, [_p, _p, _p, _p, _p, _i64, _i64, _i64, _i32, _p, _i32]),
     "bi_backward_dx": (_i32, [_p, _p, _p, _p, _i64, _i64, _i64, _i32, _p, _i32]),
     "bi_backward_dw": (_i32, [_p, _p, _i32, _p, _p, _i64, _i64, _i64, _i32, _p, _i32]),
+    "bi_bias_grad": (_i32, [_p, _p, _i32, _p, _i64, _i64, _i32, _p]),
     "bi_grouped_forward": (_i32, [_p, _p, _p, _p, _p, _i64, _i64, _i64, _i64, _i32, _p, _i32]),
     "bi_grouped_backward": (_i32, [_p, _p, _p, _p, _p, _p, _p, _i64, _i64, _i64, _i64, _i32, _p, _i32]),
     "bi_dispatch_tier": (_i32, [_i32, _i32, _i32, _i64, _i64]),
@@ -154,6 +155,10 @@ def bi_backward_dw(engine, dw, dw_f32, x, dy, m, k, n, dtype, stream=None, tenso
                                dtype_code(dtype), _stream(stream), int(tensor_cores))
 
 
+def bi_bias_grad(engine, db, db_f32, dy, m, n, dtype, stream=None) -> int:
+    return _lib.bi_bias_grad(engine, _ptr(db), int(db_f32), _ptr(dy), m, n, dtype_code(dtype), _stream(stream))
+
+
 def bi_grouped_forward(engine, y, x, w, row_experts, m, k, n, e, dtype, stream=None, tensor_cores=1) -> int:
     return _lib.bi_grouped_forward(engine, _ptr(y), _ptr(x), _ptr(w), _ptr(row_experts), m, k, n, e,
                                    dtype_code(dtype), _stream(stream), int(tensor_cores))
@@ -217,6 +222,9 @@ class Engine:
 
     def backward_dw(self, dw, dw_f32, x, dy, m, k, n, dtype, stream=None, tensor_cores=1):
         self._ok(bi_backward_dw(self.handle, dw, dw_f32, x, dy, m, k, n, dtype, stream, tensor_cores))
+
+    def bias_grad(self, db, db_f32, dy, m, n, dtype, stream=None):
+        self._ok(bi_bias_grad(self.handle, db, db_f32, dy, m, n, dtype, stream))
 
     def grouped_forward(self, y, x, w, ids, m, k, n, e, dtype, stream=None, tensor_cores=1):
         self._ok(bi_grouped_forward(self.handle, y, x, w, ids, m, k, n, e, dtype, stream, tensor_cores))

@@ -55,6 +55,11 @@ cudaError_t scalar_dw_grouped(const LaunchCtx& c, bi_dtype dt, float* out, const
                               const uint32_t* seg, const uint32_t* perm, float* partials,
                               int64_t max_chunks);
 
+// Bias gradient: out[N] = column sums of dY [M, N] in the dW chunk/tree order.
+// partials: J*N floats (J = ceil(M/256)); may be null when J == 1.
+cudaError_t bias_grad(const LaunchCtx& c, bi_dtype dt, void* out, int out_f32, const void* dy,
+                      int64_t M, int64_t N, float* partials);
+
 // ---- grouping (grouped.cu) ------------------------------------------------
 // Segment table layout (u32): [0, E+2) offsets of groups 0..E (group E =
 // padding) plus M; [E+2, 2E+3) padded starts of experts 0..E (rows rounded up

@@ -252,6 +252,28 @@ bi_status bi_backward_dw(bi_engine eng, void* dw, int dw_f32, const void* x, con
     return e == cudaSuccess ? BI_OK : cuda_fail(eng, e, "bi_backward_dw");
 }
 
+bi_status bi_bias_grad(bi_engine eng, void* db, int db_f32, const void* dy, int64_t m, int64_t n,
+                       bi_dtype dtype, void* stream) {
+    bi_status st = check_common(eng, dtype, m, 1, n);
+    if (st != BI_OK) return st;
+    if (!db) return fail(eng, BI_ERR_INVALID_ARG, "db must not be NULL");
+    if (m > 0 && !dy) return fail(eng, BI_ERR_INVALID_ARG, "dy must not be NULL");
+    const int64_t J = (m + BI_DW_CHUNK - 1) / BI_DW_CHUNK;
+    if (J > 65535) return fail(eng, BI_ERR_UNSUPPORTED, "m is limited to 65535 * 256 rows");
+    const int out_f32 = db_f32 || dtype == BI_F32;
+    DeviceGuard g(eng->device);
+    if (!g.ok) return fail(eng, BI_ERR_CUDA, "cudaSetDevice failed");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (m == 0) {
+        cudaError_t e = cudaMemsetAsync(db, 0, static_cast<size_t>(n * (out_f32 ? 4 : dsize(dtype))), s);
+        return e == cudaSuccess ? BI_OK : cuda_fail(eng, e, "bi_bias_grad");
+    }
+    Scratch part(eng, s, J > 1 ? static_cast<size_t>(J * n * 4) : 0);
+    if (part.err != cudaSuccess) return cuda_fail(eng, part.err, "bias-gradient scratch");
+    cudaError_t e = bi::bias_grad(ctx(eng, stream), dtype, db, out_f32, dy, m, n, static_cast<float*>(part.ptr));
+    return e == cudaSuccess ? BI_OK : cuda_fail(eng, e, "bi_bias_grad");
+}
+
 namespace {
 
 bi_status check_grouped(bi_engine eng, bi_dtype dt, int64_t m, int64_t k, int64_t n, int64_t e) {

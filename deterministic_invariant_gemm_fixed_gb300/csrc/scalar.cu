@@ -381,6 +381,28 @@ __global__ void dw_tree_grouped_kernel(const float* partials, int64_t RC, const 
         out[g * RC + e] = tree_from(partials + cstart * RC + e, RC, J);
 }
 
+// ------------------------------------------------------------------ bias gradient
+
+// Column sums of dY in the fixed order of the dW reduction: chunk c (blockIdx.y)
+// of BI_DW_CHUNK rows, f32 additions from +0.0f in row order; one thread per
+// column, so a warp reads consecutive columns of one row.  With `partials` the
+// chunk sums go to the workspace for the tree; without it (one chunk) the
+// result is rounded and stored directly.
+template <typename T>
+__global__ void bias_chunk_kernel(const T* dy, int64_t M, int64_t N, float* partials, void* out,
+                                  int out_f32) {
+    const int64_t j = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x;
+    const int64_t c = blockIdx.y;
+    if (j >= N) return;
+    const int64_t r0 = c * BI_DW_CHUNK;
+    const int64_t r1 = lmin(M, r0 + BI_DW_CHUNK);
+    float acc = 0.0f;
+    for (int64_t r = r0; r < r1; ++r) acc = __fadd_rn(acc, Elem<T>::up(dy[r * N + j]));
+    if (partials) partials[c * N + j] = acc;
+    else if (out_f32) static_cast<float*>(out)[j] = acc;
+    else static_cast<T*>(out)[j] = Elem<T>::down(acc);
+}
+
 // ------------------------------------------------------------------ host helpers
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -477,6 +499,29 @@ cudaError_t scalar_dw(const LaunchCtx& c, bi_dtype dt, void* out, int out_f32, c
         case BI_F32: dw_tree_kernel<float><<<grid, 256, 0, c.stream>>>(partials, RC, J, out, out_f32); break;
         case BI_BF16: dw_tree_kernel<__nv_bfloat16><<<grid, 256, 0, c.stream>>>(partials, RC, J, out, out_f32); break;
         default: dw_tree_kernel<__half><<<grid, 256, 0, c.stream>>>(partials, RC, J, out, out_f32); break;
+    }
+    c.count();
+    return cudaGetLastError();
+}
+
+cudaError_t bias_grad(const LaunchCtx& c, bi_dtype dt, void* out, int out_f32, const void* dy,
+                      int64_t M, int64_t N, float* partials) {
+    const int64_t J = (M + BI_DW_CHUNK - 1) / BI_DW_CHUNK;
+    float* part = J > 1 ? partials : nullptr;
+    dim3 grid(static_cast<unsigned>((N + 255) / 256), static_cast<unsigned>(J));
+    switch (dt) {
+        case BI_F32: bias_chunk_kernel<float><<<grid, 256, 0, c.stream>>>(static_cast<const float*>(dy), M, N, part, out, out_f32); break;
+        case BI_BF16: bias_chunk_kernel<__nv_bfloat16><<<grid, 256, 0, c.stream>>>(static_cast<const __nv_bfloat16*>(dy), M, N, part, out, out_f32); break;
+        default: bias_chunk_kernel<__half><<<grid, 256, 0, c.stream>>>(static_cast<const __half*>(dy), M, N, part, out, out_f32); break;
+    }
+    c.count();
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess || J <= 1) return e;
+    const unsigned tg = tree_grid(N, c.sm_count);
+    switch (dt) {
+        case BI_F32: dw_tree_kernel<float><<<tg, 256, 0, c.stream>>>(partials, N, J, out, out_f32); break;
+        case BI_BF16: dw_tree_kernel<__nv_bfloat16><<<tg, 256, 0, c.stream>>>(partials, N, J, out, out_f32); break;
+        default: dw_tree_kernel<__half><<<tg, 256, 0, c.stream>>>(partials, N, J, out, out_f32); break;
     }
     c.count();
     return cudaGetLastError();

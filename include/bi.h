@@ -138,6 +138,16 @@ bi_status bi_backward_dx(bi_engine engine, void* dx, const void* dy, const void*
 bi_status bi_backward_dw(bi_engine engine, void* dw, int dw_f32, const void* x, const void* dy,
                          int64_t m, int64_t k, int64_t n, bi_dtype dtype, void* stream, int tensor_cores);
 
+/* Bias gradient: db[N] = sum over rows of dY[M,N], in a fixed order: chunks of
+ * BI_DW_CHUNK rows from row 0, f32 additions from +0 in row order inside a
+ * chunk, the dW tree over chunk sums; db_f32 = 1 writes f32, 0 rounds once to
+ * the operand type.  Bit-identical across runs.  Source: sgemm-bi 0.1.1.post2,
+ * "Determinism contracts" (the page computes the bias gradient as an f32
+ * column sum in torch, outside its engine; this is that sum in fixed order);
+ * ViperLLM ffma.py, _FFMAAddmm.backward (gb = gy.sum(0)). */
+bi_status bi_bias_grad(bi_engine engine, void* db, int db_f32, const void* dy, int64_t m, int64_t n,
+                       bi_dtype dtype, void* stream);
+
 /* Grouped forward: y[m,:] = round( X[m,:] * W[e(m)]^T ) with W [E,N,K] and
  * e(m) = row_experts[m]; rows with e(m) >= E are +0.  Rows need not be sorted.
  * Source: rublas 0.1.45 src/tensor_grouped/mod.rs, fn grouped_matmul_nt

@@ -21,6 +21,8 @@ What each function computes (the sources are the pages' own titles):
 * ``backward_dw``  - ViperLLM ffma.py, _FFMAAddmm.backward: gW = x^T gy, with
                      the reduction over rows cut into chunks of ``chunk`` rows
                      and summed by the fixed pairwise tree.
+* ``bias_grad``    - sgemm-bi 0.1.1.post2 (the bias gradient is an f32 column
+                     sum, kept outside the engine there); here in fixed order.
 * ``grouped_*``    - rublas 0.1.45 src/tensor_grouped/mod.rs: fn
                      grouped_matmul_nt (ids outside [0,E) give zero rows),
                      struct GroupedBackward (dweights always f32).
@@ -77,6 +79,7 @@ def _load():
                 "or_backward_dx_rows": [p, p, p, p, i64, i64, i64, i64, i32, i32],
                 "or_backward_dw_cols": [p, p, p, p, i64, i64, i64, i64, i32, i64, i32],
                 "or_grouped_segment": [p, i64, i64, p, p],
+                "or_bias_grad": [p, p, i64, i64, i32, i64, i32],
                 "or_grouped_forward_rows": [p, p, p, p, p, i64, i64, i64, i64, i64, i32, i32],
                 "or_grouped_dinput_rows": [p, p, p, p, p, i64, i64, i64, i64, i64, i32, i32],
                 "or_grouped_dweights_sel": [p, p, p, p, p, p, i64, i64, i64, i64, i64, i32, i64],
@@ -200,6 +203,16 @@ def backward_dw(x, dy, m, k, n, dtype, dw_f32=False, chunk=DW_CHUNK, cols=None):
     if rc:
         raise MemoryError("oracle dW failed")
     return dw
+
+
+def bias_grad(dy, m, n, dtype, out_f32=False, chunk=DW_CHUNK):
+    """db[N]: the fixed-order column sum of dY (chunks of `chunk` rows, f32
+    additions from +0 in row order, then the dW tree over chunk partials)."""
+    _check(dy, dtype, m * n, "dy")
+    db = np.empty(n, dtype=np.float32 if out_f32 else _elem(dtype))
+    if _load().or_bias_grad(_ptr(db), _ptr(dy), m, n, DTYPES[dtype], int(chunk), int(out_f32)):
+        raise MemoryError("oracle bias grad failed")
+    return db
 
 
 def grouped_segment(ids, m, e):

@@ -349,6 +349,32 @@ int or_backward_dw(void* dw, int dw_f32, const void* x, const void* dy,
     return or_backward_dw_cols(dw, x, dy, NULL, n, m, k, n, dtype, chunk, dw_f32);
 }
 
+/* Bias gradient: db[j] = down( tree_c p_c ) with p_c = sum over the rows r of
+ * chunk c (rows [c*chunk, min(M,(c+1)*chunk)), ascending) of dY[r, j], each
+ * step one f32 addition starting from +0.0f: the column sum that the bias's
+ * gradient is, reduced with the same chunks and tree as dW.  The sgemm-bi page
+ * leaves the bias gradient to a plain f32 column sum outside its engine; this
+ * is the fixed-order version of that sum.  out_f32 != 0 keeps the f32 root. */
+int or_bias_grad(void* db, const void* dy, int64_t m, int64_t n, int dtype, int64_t chunk, int out_f32)
+{
+    if (chunk <= 0) return -2;
+    int64_t J = (m + chunk - 1) / chunk;
+    int out_t = out_f32 ? OR_F32 : dtype;
+    float* parts = (float*)malloc((size_t)(J > 0 ? J : 1) * sizeof(float));
+    if (!parts) return -1;
+    for (int64_t j = 0; j < n; ++j) {
+        for (int64_t c = 0; c < J; ++c) {
+            float acc = 0.0f;
+            int64_t r_end = (c + 1) * chunk < m ? (c + 1) * chunk : m;
+            for (int64_t r = c * chunk; r < r_end; ++r) acc = acc + load_up(dy, dtype, r * n + j);
+            parts[c] = acc;
+        }
+        store_down(db, out_t, j, tree_sum(parts, J));
+    }
+    free(parts);
+    return 0;
+}
+
 /* ------------------------------------------------------------------------ */
 /* Grouped per-row-expert passes.  X[M,K], W[E,N,K], row_experts[M] (U32),   */
 /* Y[M,N], dY[M,N], dX[M,K], dW[E,N,K] (always f32).                         */

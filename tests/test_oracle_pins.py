@@ -426,3 +426,37 @@ def test_segment_matches_stable_argsort():
     assert np.array_equal(perm, np.argsort(bucket, kind="stable"))
     counts = np.bincount(bucket, minlength=e + 1)
     assert np.array_equal(offs, np.concatenate([[0], np.cumsum(counts)]).astype(np.uint32))
+
+
+# --------------------------------------------------------------------------- bias gradient
+
+@pytest.mark.parametrize("dtype", DT)
+def test_bias_grad_exact_integers_and_dw_identity(dtype):
+    m, n = 700, 37
+    dy = synth.to_np(synth.small_ints((m, n), -8, 8, dtype, 41))
+    want = dec(dy, dtype).sum(axis=0)
+    for chunk in (1, 7, 256):
+        assert np.array_equal(oracle.bias_grad(dy, m, n, dtype, out_f32=True, chunk=chunk),
+                              want.astype(np.float32))
+    # on any data it is dW with a column of ones for X (fmaf(1, g, acc) = acc + g)
+    g = synth.to_np(synth.normal((m, n), 1.0, dtype, 42))
+    ones = enc(np.ones(m), dtype)
+    for chunk in (5, 256):
+        dw = oracle.backward_dw(ones, g, m, 1, n, dtype, dw_f32=True, chunk=chunk)[0]
+        assert np.array_equal(oracle.bias_grad(g, m, n, dtype, out_f32=True, chunk=chunk), dw)
+    assert np.array_equal(oracle.bias_grad(g, m, n, dtype),
+                          oracle.backward_dw(ones, g, m, 1, n, dtype)[0])
+
+
+def test_bias_grad_golden_tree():
+    kv, _ = read_golden("dw_tree.txt")
+    for case in kv["case"]:
+        c, xs, dys, want = [s_.strip() for s_ in case.split("|")]
+        prod = [float(a) * float(b) for a, b in zip(xs.split(), dys.split())]
+        g = np.array(prod, dtype=np.float32)
+        got = oracle.bias_grad(g, g.size, 1, "f32", out_f32=True, chunk=int(c))
+        assert got[0] == float(want), case
+
+
+def test_bias_grad_empty_is_zero():
+    assert np.array_equal(oracle.bias_grad(np.zeros(0, np.float32), 0, 3, "f32"), np.zeros(3, np.float32))
