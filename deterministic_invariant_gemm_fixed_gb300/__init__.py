@@ -28,6 +28,7 @@ STATUS_NAMES = {0: "BI_OK", 1: "BI_ERR_INVALID_ARG", 2: "BI_ERR_MISALIGNED", 3: 
 (BI_PASS_FORWARD, BI_PASS_DX, BI_PASS_DW, BI_PASS_GROUPED_FORWARD, BI_PASS_GROUPED_DINPUT,
  BI_PASS_GROUPED_DWEIGHTS) = range(6)
 BI_DW_CHUNK = 256
+BI_STRATEGY_SCALAR, BI_STRATEGY_TENSOR_CORE, BI_STRATEGY_AUTO = 0, 1, 2
 
 # Every entry point declared in include/bi.h, with its ctypes signature.
 _p, _i64, _i32, _u64 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_uint64
@@ -47,6 +48,8 @@ SIGNATURES = {
     "bi_engine_set_wait_limit": (_i32, [_p, _u64]),
     "bi_selftest_wait_timeout": (_i32, [_p, _p]),
     "bi_version": (ctypes.c_char_p, []),
+    "bi_grouped_forward_segmented": (_i32, [_p, _p, _p, _p, _p, _i64, _i64, _i64, _i64, _i32, _p, _i32]),
+    "bi_grouped_backward_segmented": (_i32, [_p, _p, _p, _p, _p, _p, _p, _i64, _i64, _i64, _i64, _i32, _p, _i32]),
     "bi_grouped_forward_noalloc": (_i32, [_p, _p, _p, _p, _i64, _i64, _i64, _i64, _i32, _p]),
 }
 
@@ -171,6 +174,19 @@ def bi_grouped_backward(engine, dx, dw, x, w, dy, row_experts, m, k, n, e, dtype
                                     int(tensor_cores))
 
 
+def bi_grouped_forward_segmented(engine, y, x, w, offsets, m, k, n, e, dtype, stream=None,
+                                 strategy=BI_STRATEGY_SCALAR) -> int:
+    return _lib.bi_grouped_forward_segmented(engine, _ptr(y), _ptr(x), _ptr(w), _ptr(offsets), m, k, n, e,
+                                             dtype_code(dtype), _stream(stream), int(strategy))
+
+
+def bi_grouped_backward_segmented(engine, dx, dw, x, w, dy, offsets, m, k, n, e, dtype, stream=None,
+                                  strategy=BI_STRATEGY_SCALAR) -> int:
+    return _lib.bi_grouped_backward_segmented(engine, _ptr(dx), _ptr(dw), _ptr(x), _ptr(w), _ptr(dy),
+                                              _ptr(offsets), m, k, n, e, dtype_code(dtype), _stream(stream),
+                                              int(strategy))
+
+
 def bi_grouped_forward_noalloc(y, x, w, row_experts, m, k, n, e, dtype, stream=None) -> int:
     """Scalar-tier grouped forward with no allocation (see include/bi.h); errors
     are read with bi_last_error(None)."""
@@ -232,6 +248,15 @@ class Engine:
     def grouped_backward(self, dx, dw, x, w, dy, ids, m, k, n, e, dtype, stream=None, tensor_cores=1):
         self._ok(bi_grouped_backward(self.handle, dx, dw, x, w, dy, ids, m, k, n, e, dtype, stream,
                                      tensor_cores))
+
+    def grouped_forward_segmented(self, y, x, w, offsets, m, k, n, e, dtype, stream=None,
+                                  strategy=BI_STRATEGY_SCALAR):
+        self._ok(bi_grouped_forward_segmented(self.handle, y, x, w, offsets, m, k, n, e, dtype, stream, strategy))
+
+    def grouped_backward_segmented(self, dx, dw, x, w, dy, offsets, m, k, n, e, dtype, stream=None,
+                                   strategy=BI_STRATEGY_SCALAR):
+        self._ok(bi_grouped_backward_segmented(self.handle, dx, dw, x, w, dy, offsets, m, k, n, e, dtype,
+                                               stream, strategy))
 
     def check(self, stream=None):
         self._ok(bi_engine_check(self.handle, stream))

@@ -25,7 +25,8 @@ namespace bi {
 
 // Status codes written by kernels into the engine's status word.
 enum DeviceStatus : int { DEV_OK = 0, DEV_TIMEOUT_PRODUCER = 1, DEV_TIMEOUT_MMA = 2,
-                          DEV_TIMEOUT_EPILOGUE = 3, DEV_TIMEOUT_SELFTEST = 4 };
+                          DEV_TIMEOUT_EPILOGUE = 3, DEV_TIMEOUT_SELFTEST = 4,
+                          DEV_BAD_OFFSETS = 5 };
 
 // Everything a kernel launcher needs from the engine.
 struct LaunchCtx {
@@ -68,6 +69,11 @@ inline int64_t seg_table_len(int64_t E) { return 2 * E + 4; }
 int64_t segment_scratch_bytes(int64_t M, int64_t E);
 cudaError_t segment(const LaunchCtx& c, const uint32_t* ids, int64_t M, int64_t E, uint32_t* seg,
                     uint32_t* perm, void* scratch);
+// The same table from caller offsets [E+1] (rows already grouped); the
+// permutation is the identity.  Offsets are clamped into a nondecreasing
+// sequence from 0 to at most M; a clamp records DEV_BAD_OFFSETS.
+cudaError_t segment_from_offsets(const LaunchCtx& c, const uint32_t* offsets, int64_t M, int64_t E,
+                                 uint32_t* seg, uint32_t* perm);
 // Copy rows of src [M, L] into dst [Mp, L] in padded expert order (zeros in the gaps).
 cudaError_t gather_padded(const LaunchCtx& c, const void* src, int64_t M, int64_t L, int64_t E,
                           const uint32_t* seg, const uint32_t* perm, void* dst, int64_t Mp_max);

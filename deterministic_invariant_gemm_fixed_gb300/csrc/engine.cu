@@ -174,6 +174,9 @@ bi_status bi_engine_check(bi_engine eng, void* stream) {
         return cuda_fail(eng, e, "reading the status word");
     if (v != 0) {
         cudaMemset(eng->d_status, 0, sizeof(int));
+        if (v == bi::DEV_BAD_OFFSETS)
+            return fail(eng, BI_ERR_INVALID_ARG,
+                        "segment offsets were not nondecreasing from 0 to at most m; they were clamped");
         static const char* who[] = {"", "TMA producer", "MMA issuer", "epilogue", "self-test"};
         return fail(eng, BI_ERR_TIMEOUT,
                     std::string("a device pipeline wait ran out (") + (v > 0 && v < 5 ? who[v] : "unknown") + ")");
@@ -291,15 +294,28 @@ bi_status check_grouped(bi_engine eng, bi_dtype dt, int64_t m, int64_t k, int64_
 
 }  // namespace
 
-bi_status bi_grouped_forward(bi_engine eng, void* y, const void* x, const void* w,
-                             const uint32_t* row_experts, int64_t m, int64_t k, int64_t n, int64_t e,
-                             bi_dtype dtype, void* stream, int tensor_cores) {
-    bi_status st = check_grouped(eng, dtype, m, k, n, e);
-    if (st != BI_OK) return st;
-    if (m == 0) return BI_OK;
-    if (!y || !x || !w || !row_experts)
-        return fail(eng, BI_ERR_INVALID_ARG, "y, x, w and row_experts must not be NULL");
-    const int tier = bi_dispatch_tier(BI_PASS_GROUPED_FORWARD, dtype, tensor_cores, k, n);
+}  // extern "C"
+
+namespace {
+
+// Where the grouping of rows by expert comes from: expert ids (stable counting
+// sort on the device) or caller offsets (rows already grouped).
+struct Grouping {
+    const uint32_t* ids;
+    const uint32_t* offsets;
+};
+
+cudaError_t build_grouping(const bi::LaunchCtx& c, const Grouping& src, int64_t m, int64_t e,
+                           uint32_t* seg, uint32_t* perm, void* hist) {
+    if (src.ids) return bi::segment(c, src.ids, m, e, seg, perm, hist);
+    return bi::segment_from_offsets(c, src.offsets, m, e, seg, perm);
+}
+
+int64_t round256(int64_t b) { return (b + 255) / 256 * 256; }
+
+bi_status grouped_forward_impl(bi_engine eng, void* y, const void* x, const void* w, const Grouping& src,
+                               int64_t m, int64_t k, int64_t n, int64_t e, bi_dtype dtype,
+                               void* stream, int tier, const char* name) {
     if (tier && (!aligned16(y) || !aligned16(x) || !aligned16(w)))
         return fail(eng, BI_ERR_MISALIGNED, "tensor-core tier needs 16-byte aligned y, x, w");
     DeviceGuard g(eng->device);
@@ -307,9 +323,9 @@ bi_status bi_grouped_forward(bi_engine eng, void* y, const void* x, const void* 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const bi::LaunchCtx c = ctx(eng, stream);
     // scratch: seg table | perm | histogram | (padded X)
-    const int64_t seg_b = ((bi::seg_table_len(e) * 4 + 255) / 256) * 256;
-    const int64_t perm_b = ((m * 4 + 255) / 256) * 256;
-    const int64_t hist_b = ((bi::segment_scratch_bytes(m, e) + 255) / 256) * 256;
+    const int64_t seg_b = round256(bi::seg_table_len(e) * 4);
+    const int64_t perm_b = round256(m * 4);
+    const int64_t hist_b = src.ids ? round256(bi::segment_scratch_bytes(m, e)) : 0;
     const int64_t mp = bi::padded_rows_max(m, e);
     const int64_t pad_b = tier ? mp * k * 2 : 0;
     Scratch sc(eng, s, static_cast<size_t>(seg_b + perm_b + hist_b + pad_b));
@@ -319,7 +335,7 @@ bi_status bi_grouped_forward(bi_engine eng, void* y, const void* x, const void* 
     uint32_t* perm = reinterpret_cast<uint32_t*>(base + seg_b);
     void* hist = base + seg_b + perm_b;
     void* xpad = base + seg_b + perm_b + hist_b;
-    cudaError_t err = bi::segment(c, row_experts, m, e, seg, perm, hist);
+    cudaError_t err = build_grouping(c, src, m, e, seg, perm, hist);
     if (err == cudaSuccess) {
         if (tier) {
             err = bi::gather_padded(c, x, m, k, e, seg, perm, xpad, mp);
@@ -330,37 +346,31 @@ bi_status bi_grouped_forward(bi_engine eng, void* y, const void* x, const void* 
         }
     }
     if (err == cudaSuccess) err = bi::zero_padding_rows(c, y, n, static_cast<int>(dsize(dtype)), e, seg, perm);
-    return err == cudaSuccess ? BI_OK : cuda_fail(eng, err, "bi_grouped_forward");
+    return err == cudaSuccess ? BI_OK : cuda_fail(eng, err, name);
 }
 
-bi_status bi_grouped_backward(bi_engine eng, void* dx, float* dw, const void* x, const void* w,
-                              const void* dy, const uint32_t* row_experts, int64_t m, int64_t k,
-                              int64_t n, int64_t e, bi_dtype dtype, void* stream, int tensor_cores) {
-    bi_status st = check_grouped(eng, dtype, m, k, n, e);
-    if (st != BI_OK) return st;
-    if (!dw) return fail(eng, BI_ERR_INVALID_ARG, "dw must not be NULL");
+bi_status grouped_backward_impl(bi_engine eng, void* dx, float* dw, const void* x, const void* w,
+                                const void* dy, const Grouping& src, int64_t m, int64_t k, int64_t n,
+                                int64_t e, bi_dtype dtype, void* stream, int tier_dx, int tier_dw,
+                                const char* name) {
     DeviceGuard g(eng->device);
     if (!g.ok) return fail(eng, BI_ERR_CUDA, "cudaSetDevice failed");
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (m == 0) {
         cudaError_t err = cudaMemsetAsync(dw, 0, static_cast<size_t>(e * n * k * 4), s);
-        return err == cudaSuccess ? BI_OK : cuda_fail(eng, err, "bi_grouped_backward");
+        return err == cudaSuccess ? BI_OK : cuda_fail(eng, err, name);
     }
-    if (!x || !w || !dy || !row_experts)
-        return fail(eng, BI_ERR_INVALID_ARG, "x, w, dy and row_experts must not be NULL");
-    const int tier_dx = dx ? bi_dispatch_tier(BI_PASS_GROUPED_DINPUT, dtype, tensor_cores, k, n) : 0;
-    const int tier_dw = bi_dispatch_tier(BI_PASS_GROUPED_DWEIGHTS, dtype, tensor_cores, k, n);
     if ((tier_dx || tier_dw) &&
         (!aligned16(x) || !aligned16(w) || !aligned16(dy) || !aligned16(dw) || (dx && !aligned16(dx))))
         return fail(eng, BI_ERR_MISALIGNED, "tensor-core tier needs 16-byte aligned operands");
     const bi::LaunchCtx c = ctx(eng, stream);
-    const int64_t seg_b = ((bi::seg_table_len(e) * 4 + 255) / 256) * 256;
-    const int64_t perm_b = ((m * 4 + 255) / 256) * 256;
-    const int64_t hist_b = ((bi::segment_scratch_bytes(m, e) + 255) / 256) * 256;
+    const int64_t seg_b = round256(bi::seg_table_len(e) * 4);
+    const int64_t perm_b = round256(m * 4);
+    const int64_t hist_b = src.ids ? round256(bi::segment_scratch_bytes(m, e)) : 0;
     const int64_t mp = bi::padded_rows_max(m, e);
     const bool need_dy_pad = tier_dx || tier_dw;
-    const int64_t dypad_b = need_dy_pad ? ((mp * n * 2 + 255) / 256) * 256 : 0;
-    const int64_t xpad_b = tier_dw ? ((mp * k * 2 + 255) / 256) * 256 : 0;
+    const int64_t dypad_b = need_dy_pad ? round256(mp * n * 2) : 0;
+    const int64_t xpad_b = tier_dw ? round256(mp * k * 2) : 0;
     const int64_t max_chunks = (m + BI_DW_CHUNK - 1) / BI_DW_CHUNK + e;
     const int64_t part_b = tier_dw ? 0 : max_chunks * n * k * 4;
     Scratch sc(eng, s, static_cast<size_t>(seg_b + perm_b + hist_b + dypad_b + xpad_b + part_b));
@@ -372,7 +382,7 @@ bi_status bi_grouped_backward(bi_engine eng, void* dx, float* dw, const void* x,
     void* dypad = base + seg_b + perm_b + hist_b;
     void* xpad = static_cast<uint8_t*>(dypad) + dypad_b;
     float* part = reinterpret_cast<float*>(static_cast<uint8_t*>(xpad) + xpad_b);
-    cudaError_t err = bi::segment(c, row_experts, m, e, seg, perm, hist);
+    cudaError_t err = build_grouping(c, src, m, e, seg, perm, hist);
     if (err == cudaSuccess && need_dy_pad) err = bi::gather_padded(c, dy, m, n, e, seg, perm, dypad, mp);
     if (err == cudaSuccess && dx) {
         err = tier_dx ? bi::tc_grouped_rows(c, dtype, 1, dx, dypad, mp, w, m, k, n, e, seg, perm)
@@ -388,7 +398,85 @@ bi_status bi_grouped_backward(bi_engine eng, void* dx, float* dw, const void* x,
             err = bi::scalar_dw_grouped(c, dtype, dw, dy, x, m, n, k, e, seg, perm, part, max_chunks);
         }
     }
-    return err == cudaSuccess ? BI_OK : cuda_fail(eng, err, "bi_grouped_backward");
+    return err == cudaSuccess ? BI_OK : cuda_fail(eng, err, name);
+}
+
+// Strategy -> tier for one pass: -1 when the tensor cores were requested and
+// the pass cannot use them.
+int resolve_strategy(bi_strategy st, int pass, bi_dtype dt, int64_t k, int64_t n) {
+    const int avail = bi_dispatch_tier(pass, dt, 1, k, n);
+    switch (st) {
+        case BI_STRATEGY_SCALAR: return 0;
+        case BI_STRATEGY_TENSOR_CORE: return avail ? 1 : -1;
+        case BI_STRATEGY_AUTO: return avail;
+        default: return -2;
+    }
+}
+
+}  // namespace
+
+extern "C" {
+
+bi_status bi_grouped_forward(bi_engine eng, void* y, const void* x, const void* w,
+                             const uint32_t* row_experts, int64_t m, int64_t k, int64_t n, int64_t e,
+                             bi_dtype dtype, void* stream, int tensor_cores) {
+    bi_status st = check_grouped(eng, dtype, m, k, n, e);
+    if (st != BI_OK) return st;
+    if (m == 0) return BI_OK;
+    if (!y || !x || !w || !row_experts)
+        return fail(eng, BI_ERR_INVALID_ARG, "y, x, w and row_experts must not be NULL");
+    const int tier = bi_dispatch_tier(BI_PASS_GROUPED_FORWARD, dtype, tensor_cores, k, n);
+    return grouped_forward_impl(eng, y, x, w, Grouping{row_experts, nullptr}, m, k, n, e, dtype, stream,
+                                tier, "bi_grouped_forward");
+}
+
+bi_status bi_grouped_backward(bi_engine eng, void* dx, float* dw, const void* x, const void* w,
+                              const void* dy, const uint32_t* row_experts, int64_t m, int64_t k,
+                              int64_t n, int64_t e, bi_dtype dtype, void* stream, int tensor_cores) {
+    bi_status st = check_grouped(eng, dtype, m, k, n, e);
+    if (st != BI_OK) return st;
+    if (!dw) return fail(eng, BI_ERR_INVALID_ARG, "dw must not be NULL");
+    if (m > 0 && (!x || !w || !dy || !row_experts))
+        return fail(eng, BI_ERR_INVALID_ARG, "x, w, dy and row_experts must not be NULL");
+    const int tier_dx = dx ? bi_dispatch_tier(BI_PASS_GROUPED_DINPUT, dtype, tensor_cores, k, n) : 0;
+    const int tier_dw = bi_dispatch_tier(BI_PASS_GROUPED_DWEIGHTS, dtype, tensor_cores, k, n);
+    return grouped_backward_impl(eng, dx, dw, x, w, dy, Grouping{row_experts, nullptr}, m, k, n, e, dtype,
+                                 stream, tier_dx, tier_dw, "bi_grouped_backward");
+}
+
+bi_status bi_grouped_forward_segmented(bi_engine eng, void* y, const void* x, const void* w,
+                                       const uint32_t* offsets, int64_t m, int64_t k, int64_t n,
+                                       int64_t e, bi_dtype dtype, void* stream, bi_strategy strategy) {
+    bi_status st = check_grouped(eng, dtype, m, k, n, e);
+    if (st != BI_OK) return st;
+    const int tier = resolve_strategy(strategy, BI_PASS_GROUPED_FORWARD, dtype, k, n);
+    if (tier == -2) return fail(eng, BI_ERR_INVALID_ARG, "unknown strategy");
+    if (tier < 0)
+        return fail(eng, BI_ERR_UNSUPPORTED,
+                    "the tensor-core tier was requested but is unavailable for this dtype and shape");
+    if (m == 0) return BI_OK;
+    if (!y || !x || !w || !offsets) return fail(eng, BI_ERR_INVALID_ARG, "y, x, w and offsets must not be NULL");
+    return grouped_forward_impl(eng, y, x, w, Grouping{nullptr, offsets}, m, k, n, e, dtype, stream, tier,
+                                "bi_grouped_forward_segmented");
+}
+
+bi_status bi_grouped_backward_segmented(bi_engine eng, void* dx, float* dw, const void* x, const void* w,
+                                        const void* dy, const uint32_t* offsets, int64_t m, int64_t k,
+                                        int64_t n, int64_t e, bi_dtype dtype, void* stream,
+                                        bi_strategy strategy) {
+    bi_status st = check_grouped(eng, dtype, m, k, n, e);
+    if (st != BI_OK) return st;
+    if (!dw) return fail(eng, BI_ERR_INVALID_ARG, "dw must not be NULL");
+    int tier_dx = dx ? resolve_strategy(strategy, BI_PASS_GROUPED_DINPUT, dtype, k, n) : 0;
+    int tier_dw = resolve_strategy(strategy, BI_PASS_GROUPED_DWEIGHTS, dtype, k, n);
+    if (tier_dx == -2 || tier_dw == -2) return fail(eng, BI_ERR_INVALID_ARG, "unknown strategy");
+    if (tier_dx < 0 || tier_dw < 0)
+        return fail(eng, BI_ERR_UNSUPPORTED,
+                    "the tensor-core tier was requested but is unavailable for this dtype and shape");
+    if (m > 0 && (!x || !w || !dy || !offsets))
+        return fail(eng, BI_ERR_INVALID_ARG, "x, w, dy and offsets must not be NULL");
+    return grouped_backward_impl(eng, dx, dw, x, w, dy, Grouping{nullptr, offsets}, m, k, n, e, dtype,
+                                 stream, tier_dx, tier_dw, "bi_grouped_backward_segmented");
 }
 
 }  // extern "C"

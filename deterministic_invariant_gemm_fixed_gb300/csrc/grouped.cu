@@ -139,6 +139,38 @@ __global__ void __launch_bounds__(SEG_THREADS)
     }
 }
 
+// Segment table from caller offsets (block 0, thread 0) and the identity
+// permutation (all threads).  The clamp keeps every later index in bounds
+// whatever the caller passed.
+__global__ void seg_from_offsets_kernel(const uint32_t* offsets, int64_t M, uint32_t E, uint32_t* seg,
+                                        uint32_t* perm, int* status) {
+    if (blockIdx.x == 0 && threadIdx.x == 0) {
+        const uint32_t m = static_cast<uint32_t>(M);
+        bool bad = offsets[0] != 0;
+        uint32_t prev = 0;
+        seg[0] = 0;
+        for (uint32_t g = 1; g <= E; ++g) {
+            const uint32_t v = offsets[g];
+            const uint32_t cl = v < prev ? prev : (v > m ? m : v);
+            bad |= cl != v;
+            seg[g] = cl;
+            prev = cl;
+        }
+        seg[E + 1] = m;
+        uint32_t ps = 0;
+        for (uint32_t g = 0; g < E; ++g) {
+            seg[E + 2 + g] = ps;
+            ps += (seg[g + 1] - seg[g] + 127u) / 128u * 128u;
+        }
+        seg[E + 2 + E] = ps;
+        seg[2 * E + 3] = ps;
+        if (bad && status) *reinterpret_cast<volatile int*>(status) = DEV_BAD_OFFSETS;
+    }
+    for (int64_t r = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; r < M;
+         r += static_cast<int64_t>(gridDim.x) * blockDim.x)
+        perm[r] = static_cast<uint32_t>(r);
+}
+
 // dst row p (padded order): expert g with pstart[g] <= p < pstart[g+1];
 // rows past the expert's count are zero.
 __global__ void gather_padded_kernel(const uint4* src, int64_t L16, uint32_t E, const uint32_t* seg,
@@ -231,6 +263,17 @@ cudaError_t segment(const LaunchCtx& c, const uint32_t* ids, int64_t M, int64_t 
         seg_scatter_kernel<<<static_cast<unsigned>(NB), SEG_THREADS, 0, c.stream>>>(ids, M, static_cast<uint32_t>(E), hist, NB, perm);
         c.count();
     }
+    return cudaGetLastError();
+}
+
+cudaError_t segment_from_offsets(const LaunchCtx& c, const uint32_t* offsets, int64_t M, int64_t E,
+                                 uint32_t* seg, uint32_t* perm) {
+    int64_t blocks = (M + 255) / 256;
+    if (blocks > static_cast<int64_t>(c.sm_count) * 8) blocks = static_cast<int64_t>(c.sm_count) * 8;
+    if (blocks < 1) blocks = 1;
+    seg_from_offsets_kernel<<<static_cast<unsigned>(blocks), 256, 0, c.stream>>>(
+        offsets, M, static_cast<uint32_t>(E), seg, perm, c.status);
+    c.count();
     return cudaGetLastError();
 }
 

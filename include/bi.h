@@ -95,6 +95,13 @@ typedef enum {
     BI_PASS_GROUPED_FORWARD = 3, BI_PASS_GROUPED_DINPUT = 4, BI_PASS_GROUPED_DWEIGHTS = 5
 } bi_pass;
 
+/* Tier request of the segmented grouped calls.  Source: rublas 0.1.45
+ * src/tensor_grouped/mod.rs, enum GroupedStrategy and fn
+ * grouped_matmul_nt_backward_segmented_with_strategy: the scalar tier is the
+ * default, Auto takes the tensor cores only where they are supported, and an
+ * explicit tensor-core request that cannot be met is an error, not a fallback. */
+typedef enum { BI_STRATEGY_SCALAR = 0, BI_STRATEGY_TENSOR_CORE = 1, BI_STRATEGY_AUTO = 2 } bi_strategy;
+
 /* Rows per chunk of the dW reduction tree (scalar tier). */
 #define BI_DW_CHUNK 256
 
@@ -168,6 +175,31 @@ bi_status bi_grouped_backward(bi_engine engine, void* dx, float* dw, const void*
                               const void* dy, const uint32_t* row_experts,
                               int64_t m, int64_t k, int64_t n, int64_t e,
                               bi_dtype dtype, void* stream, int tensor_cores);
+
+/* Segmented grouped forward: the caller's rows are already grouped by expert.
+ * offsets [E+1] (u32, device) gives expert g the rows [offsets[g],
+ * offsets[g+1]); rows from offsets[E] to m are padding (+0 output rows).  The
+ * result equals bi_grouped_forward on row ids listing that grouping, bit for
+ * bit on either tier.  strategy: see bi_strategy; BI_ERR_UNSUPPORTED when the
+ * tensor cores are requested for a dtype or shape they cannot take.  The
+ * offsets are read on the device and not validated on the host: a sequence
+ * that does not start at 0, decreases or exceeds m is clamped into range
+ * (no out-of-bounds access) and bi_engine_check() then reports
+ * BI_ERR_INVALID_ARG.  Source: rublas 0.1.45 src/tensor_grouped/mod.rs, fn
+ * grouped_matmul_nt_segmented and its offsets invariant. */
+bi_status bi_grouped_forward_segmented(bi_engine engine, void* y, const void* x, const void* w,
+                                       const uint32_t* offsets, int64_t m, int64_t k, int64_t n,
+                                       int64_t e, bi_dtype dtype, void* stream, bi_strategy strategy);
+
+/* Segmented grouped backward: dx (nullable) and dw [E,N,K] f32 for rows
+ * grouped by offsets as in bi_grouped_forward_segmented.  With
+ * BI_STRATEGY_TENSOR_CORE both passes must be able to use the tensor cores.
+ * Source: rublas 0.1.45 src/tensor_grouped/mod.rs, fn
+ * grouped_matmul_nt_backward_segmented_with_strategy. */
+bi_status bi_grouped_backward_segmented(bi_engine engine, void* dx, float* dw, const void* x,
+                                        const void* w, const void* dy, const uint32_t* offsets,
+                                        int64_t m, int64_t k, int64_t n, int64_t e, bi_dtype dtype,
+                                        void* stream, bi_strategy strategy);
 
 /* Grouped forward that allocates nothing.  No counterpart on the pages: this
  * entry point exists for callers that cannot allocate GPU memory when they run
