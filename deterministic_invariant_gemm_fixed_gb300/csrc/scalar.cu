@@ -151,7 +151,9 @@ __global__ void __launch_bounds__(2 * TMV, TMV == 128 ? 2 : 4) scalar_rows_kerne
     if (rvalid > TMV) rvalid = TMV;
 
     // global -> register staging of one TK block
-    const int a_row = tid / 2, a_seg = (tid % 2) * 8;          // A: TMV rows x 16 steps
+    // A: TMV rows x 16 steps; a warp covers 32 different rows with the same
+    // 8-step half, so its transposing stores hit 32 different banks
+    const int a_row = tid % TMV, a_seg = (tid / TMV) * 8;
     int64_t a_src_row = -1;
     if (a_row < rvalid) a_src_row = GROUPED ? static_cast<int64_t>(p.perm[sbase + a_row]) : r0 + a_row;
     float ra[8], rb[SL][8];
@@ -165,7 +167,7 @@ __global__ void __launch_bounds__(2 * TMV, TMV == 128 ? 2 : 4) scalar_rows_kerne
         for (int q = 0; q < SL; ++q) {
             const int e = tid + q * NTV;  // 0..255
             if (BT) {  // b(l, c) = B[c * L + l]: 128 cols x 16 steps
-                const int c = e / 2, s = (e % 2) * 8;
+                const int c = e % TN, s = (e / TN) * 8;
                 const int64_t gc = c0 + c, l = l0 + s;
                 const int avail = gc < C ? static_cast<int>(lmin(8, lmax(0, L - l))) : 0;
                 load8<T, VEC>(B + (avail ? gc * L + l : 0), avail, rb[q]);
@@ -184,7 +186,7 @@ __global__ void __launch_bounds__(2 * TMV, TMV == 128 ? 2 : 4) scalar_rows_kerne
         for (int q = 0; q < SL; ++q) {
             const int e = tid + q * NTV;
             if (BT) {
-                const int c = e / 2, s = (e % 2) * 8;
+                const int c = e % TN, s = (e / TN) * 8;
 #pragma unroll
                 for (int i = 0; i < 8; ++i) sm.b[buf][s + i][c] = rb[q][i];
             } else {
@@ -384,23 +386,41 @@ __global__ void dw_tree_grouped_kernel(const float* partials, int64_t RC, const 
 // ------------------------------------------------------------------ bias gradient
 
 // Column sums of dY in the fixed order of the dW reduction: chunk c (blockIdx.y)
-// of BI_DW_CHUNK rows, f32 additions from +0.0f in row order; one thread per
-// column, so a warp reads consecutive columns of one row.  With `partials` the
+// of BI_DW_CHUNK rows, f32 additions from +0.0f in row order.  Each thread owns
+// V consecutive columns (V = 8 with 16-byte loads when the row length allows,
+// else 1), so a warp reads whole 16-byte pieces of a row.  With `partials` the
 // chunk sums go to the workspace for the tree; without it (one chunk) the
 // result is rounded and stored directly.
-template <typename T>
+template <typename T, int V>
 __global__ void bias_chunk_kernel(const T* dy, int64_t M, int64_t N, float* partials, void* out,
                                   int out_f32) {
-    const int64_t j = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x;
+    const int64_t j0 = (blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x) * V;
     const int64_t c = blockIdx.y;
-    if (j >= N) return;
+    if (j0 >= N) return;
     const int64_t r0 = c * BI_DW_CHUNK;
     const int64_t r1 = lmin(M, r0 + BI_DW_CHUNK);
-    float acc = 0.0f;
-    for (int64_t r = r0; r < r1; ++r) acc = __fadd_rn(acc, Elem<T>::up(dy[r * N + j]));
-    if (partials) partials[c * N + j] = acc;
-    else if (out_f32) static_cast<float*>(out)[j] = acc;
-    else static_cast<T*>(out)[j] = Elem<T>::down(acc);
+    float acc[V];
+#pragma unroll
+    for (int v = 0; v < V; ++v) acc[v] = 0.0f;
+    if (V == 8) {
+        // the additions stay in row order; unrolling lets 16 rows' loads be in flight
+#pragma unroll 16
+        for (int64_t r = r0; r < r1; ++r) {
+            float f[8];
+            load8<T, true>(dy + r * N + j0, 8, f);
+#pragma unroll
+            for (int v = 0; v < 8; ++v) acc[v] = __fadd_rn(acc[v], f[v]);
+        }
+    } else {
+        for (int64_t r = r0; r < r1; ++r) acc[0] = __fadd_rn(acc[0], Elem<T>::up(dy[r * N + j0]));
+    }
+#pragma unroll
+    for (int v = 0; v < V; ++v) {
+        const int64_t j = j0 + v;
+        if (partials) partials[c * N + j] = acc[v];
+        else if (out_f32) static_cast<float*>(out)[j] = acc[v];
+        else static_cast<T*>(out)[j] = Elem<T>::down(acc[v]);
+    }
 }
 
 // ------------------------------------------------------------------ host helpers
@@ -504,15 +524,29 @@ cudaError_t scalar_dw(const LaunchCtx& c, bi_dtype dt, void* out, int out_f32, c
     return cudaGetLastError();
 }
 
+template <typename T>
+void launch_bias_chunks(const LaunchCtx& c, const void* dy, int64_t M, int64_t N, int64_t J, float* part,
+                        void* out, int out_f32) {
+    const T* d = static_cast<const T*>(dy);
+    // 8 columns per thread when every row starts on a 16-byte boundary
+    const bool vec = sizeof(T) == 2 && N % 8 == 0 && aligned16(dy);
+    if (vec) {
+        dim3 grid(static_cast<unsigned>((N / 8 + 127) / 128), static_cast<unsigned>(J));
+        bias_chunk_kernel<T, 8><<<grid, 128, 0, c.stream>>>(d, M, N, part, out, out_f32);
+    } else {
+        dim3 grid(static_cast<unsigned>((N + 255) / 256), static_cast<unsigned>(J));
+        bias_chunk_kernel<T, 1><<<grid, 256, 0, c.stream>>>(d, M, N, part, out, out_f32);
+    }
+}
+
 cudaError_t bias_grad(const LaunchCtx& c, bi_dtype dt, void* out, int out_f32, const void* dy,
                       int64_t M, int64_t N, float* partials) {
     const int64_t J = (M + BI_DW_CHUNK - 1) / BI_DW_CHUNK;
     float* part = J > 1 ? partials : nullptr;
-    dim3 grid(static_cast<unsigned>((N + 255) / 256), static_cast<unsigned>(J));
     switch (dt) {
-        case BI_F32: bias_chunk_kernel<float><<<grid, 256, 0, c.stream>>>(static_cast<const float*>(dy), M, N, part, out, out_f32); break;
-        case BI_BF16: bias_chunk_kernel<__nv_bfloat16><<<grid, 256, 0, c.stream>>>(static_cast<const __nv_bfloat16*>(dy), M, N, part, out, out_f32); break;
-        default: bias_chunk_kernel<__half><<<grid, 256, 0, c.stream>>>(static_cast<const __half*>(dy), M, N, part, out, out_f32); break;
+        case BI_F32: launch_bias_chunks<float>(c, dy, M, N, J, part, out, out_f32); break;
+        case BI_BF16: launch_bias_chunks<__nv_bfloat16>(c, dy, M, N, J, part, out, out_f32); break;
+        default: launch_bias_chunks<__half>(c, dy, M, N, J, part, out, out_f32); break;
     }
     c.count();
     cudaError_t e = cudaGetLastError();

@@ -27,8 +27,8 @@ def eng():
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16", "f16"])
 @pytest.mark.parametrize("m", [1, 255, 256, 257, 3000])
-def test_bias_grad_bit_exact(eng, dtype, m):
-    n = 1000
+@pytest.mark.parametrize("n", [1000, 1001])  # 16-byte rows (vector path) and not
+def test_bias_grad_bit_exact(eng, dtype, m, n):
     dy = synth.normal((m, n), 1.0, dtype, 50 + m)
     dyn = synth.to_np(dy)
     D = dy.cuda()
