@@ -403,9 +403,20 @@ __global__ void bias_chunk_kernel(const T* dy, int64_t M, int64_t N, float* part
 #pragma unroll
     for (int v = 0; v < V; ++v) acc[v] = 0.0f;
     if (V == 8) {
-        // the additions stay in row order; unrolling lets 16 rows' loads be in flight
-#pragma unroll 16
-        for (int64_t r = r0; r < r1; ++r) {
+        // eight rows' loads are issued before their additions, which stay in row order
+        int64_t r = r0;
+        for (; r + 8 <= r1; r += 8) {
+            uint4 q[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) q[u] = __ldg(reinterpret_cast<const uint4*>(dy + (r + u) * N + j0));
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const T* h = reinterpret_cast<const T*>(&q[u]);
+#pragma unroll
+                for (int v = 0; v < 8; ++v) acc[v] = __fadd_rn(acc[v], Elem<T>::up(h[v]));
+            }
+        }
+        for (; r < r1; ++r) {
             float f[8];
             load8<T, true>(dy + r * N + j0, 8, f);
 #pragma unroll

@@ -23,6 +23,9 @@ What each function computes (the sources are the pages' own titles):
                      and summed by the fixed pairwise tree.
 * ``bias_grad``    - sgemm-bi 0.1.1.post2 (the bias gradient is an f32 column
                      sum, kept outside the engine there); here in fixed order.
+* ``fp8_*``        - AstrAI csrc/kernels/fp8_mm.cu: quantize_kernel (codes and
+                     amax), fp8_linear_forward_scaled / _backward_scaled (the
+                     per-tensor scales applied to the f32 product).
 * ``grouped_*``    - rublas 0.1.45 src/tensor_grouped/mod.rs: fn
                      grouped_matmul_nt (ids outside [0,E) give zero rows),
                      struct GroupedBackward (dweights always f32).
@@ -80,6 +83,9 @@ def _load():
                 "or_backward_dw_cols": [p, p, p, p, i64, i64, i64, i64, i32, i64, i32],
                 "or_grouped_segment": [p, i64, i64, p, p],
                 "or_bias_grad": [p, p, i64, i64, i32, i64, i32],
+                "or_fp8_forward_rows": [p, p, p, p, ctypes.c_float, ctypes.c_float, p, i64, i64, i64, i64, i32],
+                "or_fp8_backward_dx_rows": [p, p, p, ctypes.c_float, ctypes.c_float, p, i64, i64, i64, i64, i32],
+                "or_fp8_backward_dw": [p, p, p, ctypes.c_float, ctypes.c_float, i64, i64, i64, i32, i64],
                 "or_grouped_forward_rows": [p, p, p, p, p, i64, i64, i64, i64, i64, i32, i32],
                 "or_grouped_dinput_rows": [p, p, p, p, p, i64, i64, i64, i64, i64, i32, i32],
                 "or_grouped_dweights_sel": [p, p, p, p, p, p, i64, i64, i64, i64, i64, i32, i64],
@@ -99,6 +105,12 @@ def _load():
             lib.or_fmaf.restype = ctypes.c_float
             for name in ("or_set_num_threads", "or_rne_array", "or_rne_bits_range", "or_up_array"):
                 getattr(lib, name).restype = None
+            lib.or_e4m3_bits_range.argtypes = [p, ctypes.c_uint64, i64]
+            lib.or_e4m3_bits_range.restype = None
+            lib.or_up_e4m3_array.argtypes = [p, p, i64]
+            lib.or_up_e4m3_array.restype = None
+            lib.or_fp8_quantize.argtypes = [p, p, p, i32, ctypes.c_float, i64]
+            lib.or_fp8_quantize.restype = None
             _lib = lib
     return _lib
 
@@ -213,6 +225,55 @@ def bias_grad(dy, m, n, dtype, out_f32=False, chunk=DW_CHUNK):
     if _load().or_bias_grad(_ptr(db), _ptr(dy), m, n, DTYPES[dtype], int(chunk), int(out_f32)):
         raise MemoryError("oracle bias grad failed")
     return db
+
+
+def e4m3_bits_range(first_bits: int, count: int) -> np.ndarray:
+    """e4m3 encodings of the f32 patterns first_bits .. first_bits+count-1."""
+    out = np.empty(count, dtype=np.uint8)
+    _load().or_e4m3_bits_range(_ptr(out), first_bits, count)
+    return out
+
+
+def up_e4m3(q: np.ndarray) -> np.ndarray:
+    q = np.ascontiguousarray(q, dtype=np.uint8)
+    out = np.empty(q.shape, dtype=np.float32)
+    _load().or_up_e4m3_array(_ptr(out), _ptr(q), q.size)
+    return out
+
+
+def fp8_quantize(src, dtype, scale_inv):
+    """(e4m3 codes, amax) of src * scale_inv (AstrAI fp8_mm.cu quantize_kernel)."""
+    src = np.ascontiguousarray(src)
+    _check(src, dtype, src.size, "src")
+    q = np.empty(src.shape, dtype=np.uint8)
+    amax = np.zeros(1, dtype=np.float32)
+    _load().or_fp8_quantize(_ptr(q), _ptr(amax), _ptr(src), DTYPES[dtype], float(scale_inv), src.size)
+    return q, np.float32(amax[0])
+
+
+def fp8_forward(xq, wq, bias, sx, sw, m, k, n, out_dtype, rows=None):
+    r, nr = _index_arg(rows, m)
+    y = np.empty((nr, n), dtype=_elem(out_dtype))
+    _load().or_fp8_forward_rows(_ptr(y), _ptr(np.ascontiguousarray(xq)), _ptr(np.ascontiguousarray(wq)),
+                                _ptr(bias), float(sx), float(sw), _ptr(r), nr, m, k, n, DTYPES[out_dtype])
+    return y
+
+
+def fp8_backward_dx(gq, wq, sg, sw, m, k, n, out_dtype, rows=None):
+    r, nr = _index_arg(rows, m)
+    dx = np.empty((nr, k), dtype=_elem(out_dtype))
+    _load().or_fp8_backward_dx_rows(_ptr(dx), _ptr(np.ascontiguousarray(gq)), _ptr(np.ascontiguousarray(wq)),
+                                    float(sg), float(sw), _ptr(r), nr, m, k, n, DTYPES[out_dtype])
+    return dx
+
+
+def fp8_backward_dw(xq, gq, sx, sg, m, k, n, out_dtype, chunk=DW_CHUNK):
+    dw = np.empty((k, n), dtype=_elem(out_dtype))
+    rc = _load().or_fp8_backward_dw(_ptr(dw), _ptr(np.ascontiguousarray(xq)), _ptr(np.ascontiguousarray(gq)),
+                                    float(sx), float(sg), m, k, n, DTYPES[out_dtype], int(chunk))
+    if rc:
+        raise MemoryError("oracle fp8 dW failed")
+    return dw
 
 
 def grouped_segment(ids, m, e):

@@ -376,6 +376,151 @@ int or_bias_grad(void* db, const void* dy, int64_t m, int64_t n, int dtype, int6
 }
 
 /* ------------------------------------------------------------------------ */
+/* FP8 e4m3 per-tensor-scaled linear (AstrAI csrc/kernels/fp8_mm.cu:         */
+/* quantize_kernel, fp8_linear_forward_scaled, fp8_linear_backward_scaled).  */
+/* e4m3 ("fn" flavour): 1 sign, 4 exponent bits (bias 7), 3 fraction bits,  */
+/* no infinities, 0x7F/0xFF are NaN, largest finite 448.                     */
+/* ------------------------------------------------------------------------ */
+
+/* f32 -> e4m3, round to nearest even, saturating: anything whose rounding
+ * would exceed 448 (and +-inf) becomes +-448; NaN becomes 0x7F. */
+static uint8_t rne_e4m3(float f)
+{
+    uint32_t u = f32_bits(f);
+    uint8_t sign = (uint8_t)((u >> 24) & 0x80u);
+    uint32_t ef = (u >> 23) & 0xffu;
+    uint32_t frac = u & 0x7fffffu;
+    if (ef == 0xffu && frac) return 0x7fu;        /* NaN */
+    if (ef == 0xffu) return (uint8_t)(sign | 0x7eu); /* inf saturates */
+    if (ef == 0) return sign;                     /* f32 zero/subnormal: below 2^-10 */
+    int32_t e = (int32_t)ef - 127;
+    uint32_t sig = frac | 0x800000u;
+    if (e > 8) return (uint8_t)(sign | 0x7eu);
+    if (e >= -6) {
+        /* normal: keep 4 significant bits (implicit one + 3) */
+        uint32_t keep = sig >> 20, rem = sig & 0xfffffu;
+        uint32_t mag = ((uint32_t)(e + 7) << 3) + (keep - 8u);
+        mag += rne_increment(keep, rem, 0x80000u);
+        if (mag > 0x7eu) mag = 0x7eu;             /* 480 and above is out of range */
+        return (uint8_t)(sign | mag);
+    }
+    /* subnormal: the unit is 2^-9, keep sig >> (20 + (-6 - e)) */
+    int32_t shift = 20 + (-6 - e);
+    if (shift > 24) return sign;
+    uint32_t keep = sig >> shift;
+    uint32_t rem = sig & ((1u << shift) - 1u);
+    uint32_t half = 1u << (shift - 1);
+    return (uint8_t)(sign | (keep + rne_increment(keep, rem, half)));
+}
+
+static float up_e4m3(uint8_t q)
+{
+    uint32_t sign = (uint32_t)(q >> 7) << 31;
+    uint32_t e = (q >> 3) & 0xfu, m = q & 7u;
+    if (e == 0xfu && m == 7u) return bits_f32(sign | 0x7fc00000u);
+    if (e == 0) { float mag = ldexpf((float)m, -9); return sign ? -mag : mag; }
+    return bits_f32(sign | ((e - 7u + 127u) << 23) | (m << 20));
+}
+
+void or_e4m3_bits_range(uint8_t* out, uint64_t first_bits, int64_t count)
+{
+    #pragma omp parallel for schedule(static)
+    for (int64_t i = 0; i < count; ++i) out[i] = rne_e4m3(bits_f32((uint32_t)(first_bits + (uint64_t)i)));
+}
+
+void or_up_e4m3_array(float* out, const uint8_t* in, int64_t count)
+{
+    for (int64_t i = 0; i < count; ++i) out[i] = up_e4m3(in[i]);
+}
+
+/* q[i] = e4m3(up(src[i]) * scale_inv), one f32 multiply then one rounding;
+ * *amax = max |up(src[i])| over the unscaled values (+0 when count == 0). */
+void or_fp8_quantize(uint8_t* q, float* amax, const void* src, int dtype, float scale_inv, int64_t count)
+{
+    float mx = 0.0f;
+    for (int64_t i = 0; i < count; ++i) {
+        float v = load_up(src, dtype, i);
+        q[i] = rne_e4m3(v * scale_inv);
+        float a = fabsf(v);
+        if (a > mx) mx = a;
+    }
+    *amax = mx;
+}
+
+/* The scaled matmuls.  acc = chain over the contracted index of
+ * up(a_i) * up(b_i) (exact products of e4m3 values), then
+ * v = acc * (scale_a * scale_b) in f32, then (+ bias in f32), then one
+ * rounding to out_dtype.  Forward y[m,n] (xq [M,K], wq [K,N]); dX[m,k] from
+ * gq [M,N] and wq; dW[k,n] from xq and gq with the dW chunk tree over rows. */
+int or_fp8_forward_rows(void* y_rows, const uint8_t* xq, const uint8_t* wq, const void* bias,
+                        float sx, float sw, const int64_t* rows, int64_t nrows, int64_t m, int64_t k,
+                        int64_t n, int out_dtype)
+{
+    const float s = sx * sw;
+    #pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t i = 0; i < nrows; ++i) {
+        int64_t r = rows ? rows[i] : i;
+        if (r < 0 || r >= m) continue;
+        for (int64_t j = 0; j < n; ++j) {
+            float acc = 0.0f;
+            for (int64_t kk = 0; kk < k; ++kk)
+                acc = fmaf(up_e4m3(xq[r * k + kk]), up_e4m3(wq[kk * n + j]), acc);
+            float v = acc * s;
+            if (bias) v = v + load_up(bias, out_dtype, j);
+            store_down(y_rows, out_dtype, i * n + j, v);
+        }
+    }
+    return 0;
+}
+
+int or_fp8_backward_dx_rows(void* dx_rows, const uint8_t* gq, const uint8_t* wq, float sg, float sw,
+                            const int64_t* rows, int64_t nrows, int64_t m, int64_t k, int64_t n, int out_dtype)
+{
+    const float s = sg * sw;
+    #pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t i = 0; i < nrows; ++i) {
+        int64_t r = rows ? rows[i] : i;
+        if (r < 0 || r >= m) continue;
+        for (int64_t kk = 0; kk < k; ++kk) {
+            float acc = 0.0f;
+            for (int64_t j = 0; j < n; ++j)
+                acc = fmaf(up_e4m3(gq[r * n + j]), up_e4m3(wq[kk * n + j]), acc);
+            store_down(dx_rows, out_dtype, i * k + kk, acc * s);
+        }
+    }
+    return 0;
+}
+
+int or_fp8_backward_dw(void* dw, const uint8_t* xq, const uint8_t* gq, float sx, float sg,
+                       int64_t m, int64_t k, int64_t n, int out_dtype, int64_t chunk)
+{
+    if (chunk <= 0) return -2;
+    const float s = sx * sg;
+    int64_t J = (m + chunk - 1) / chunk;
+    int failed = 0;
+    #pragma omp parallel
+    {
+        float* parts = (float*)malloc((size_t)(J > 0 ? J : 1) * sizeof(float));
+        if (!parts) failed = 1;
+        #pragma omp for collapse(2) schedule(dynamic, 16)
+        for (int64_t kk = 0; kk < k; ++kk)
+            for (int64_t j = 0; j < n; ++j) {
+                if (!parts) continue;
+                for (int64_t c = 0; c < J; ++c) {
+                    float acc = 0.0f;
+                    int64_t r_end = (c + 1) * chunk < m ? (c + 1) * chunk : m;
+                    for (int64_t r = c * chunk; r < r_end; ++r)
+                        acc = fmaf(up_e4m3(xq[r * k + kk]), up_e4m3(gq[r * n + j]), acc);
+                    parts[c] = acc;
+                }
+                store_down(dw, out_dtype, kk * n + j, tree_sum(parts, J) * s);
+            }
+        free(parts);
+    }
+    return failed ? -1 : 0;
+}
+
+/* ------------------------------------------------------------------------ */
 /* Grouped per-row-expert passes.  X[M,K], W[E,N,K], row_experts[M] (U32),   */
 /* Y[M,N], dY[M,N], dX[M,K], dW[E,N,K] (always f32).                         */
 /* ------------------------------------------------------------------------ */

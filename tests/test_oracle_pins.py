@@ -460,3 +460,85 @@ def test_bias_grad_golden_tree():
 
 def test_bias_grad_empty_is_zero():
     assert np.array_equal(oracle.bias_grad(np.zeros(0, np.float32), 0, 3, "f32"), np.zeros(3, np.float32))
+
+
+# --------------------------------------------------------------------------- FP8 e4m3
+
+def test_golden_e4m3_points():
+    _, rows = read_golden("e4m3_points.txt")
+    assert len(rows) > 15
+    for fbits, want in rows:
+        got = oracle.e4m3_bits_range(int(fbits, 16), 1)[0]
+        assert got == int(want, 16), (fbits, hex(got), want)
+
+
+def test_e4m3_exhaustive_vs_torch():
+    """Every binary32 pattern: for exponents 2^-11 .. 2^9 (where e4m3 has distinct
+    codes) the result equals torch's float8_e4m3fn rounding wherever |v| <= 464;
+    beyond 464 (where torch gives NaN) this format saturates to +-448, the
+    saturating cast of the FP8 design; below 2^-11 everything rounds to +-0;
+    NaN stays NaN."""
+    frac = np.arange(1 << 23, dtype=np.uint32)
+    for sign in (0, 1):
+        for ef in range(256):
+            start = (sign << 31) | (ef << 23)
+            bits = frac | np.uint32(start)
+            ours = oracle.e4m3_bits_range(start, 1 << 23)
+            if ef == 255:  # inf (frac 0) saturates, NaN stays NaN
+                assert ours[0] == (0xfe if sign else 0x7e)
+                assert np.all((ours[1:] & 0x7f) == 0x7f)
+            elif ef < 116:  # |v| < 2^-11: below half the smallest subnormal
+                assert np.all(ours == (0x80 if sign else 0))
+            elif ef > 136:  # |v| >= 2^10 > 464
+                assert np.all(ours == (0xfe if sign else 0x7e))
+            else:
+                f = bits.view(np.float32)
+                theirs = torch.from_numpy(f).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+                inrange = np.abs(f) <= 464
+                assert np.array_equal(ours[inrange], theirs[inrange]), (sign, ef)
+                assert np.all((ours[~inrange] & 0x7f) == 0x7e)
+
+
+def test_up_e4m3_exhaustive_vs_torch():
+    q = np.arange(256, dtype=np.uint8)
+    ours = oracle.up_e4m3(q)
+    theirs = torch.from_numpy(q).view(torch.float8_e4m3fn).to(torch.float32).numpy()
+    nan = np.isnan(theirs)
+    assert np.array_equal(np.isnan(ours), nan)
+    assert np.array_equal(ours[~nan].view(np.uint32), theirs[~nan].view(np.uint32))
+
+
+def test_fp8_quantize_and_amax():
+    x = synth.normal((1000,), 3.0, "bf16", 70)
+    xn = synth.to_np(x)
+    q, amax = oracle.fp8_quantize(xn, "bf16", 0.5)
+    v = dec(xn, "bf16")
+    assert amax == np.float32(np.max(np.abs(v)))
+    # scale_inv a power of two: v * 0.5 is exact, so q is torch's e4m3 of v/2
+    want = torch.from_numpy((v * 0.5).astype(np.float32)).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(q, want)
+
+
+@pytest.mark.parametrize("out", ["bf16", "f32"])
+def test_fp8_matmuls_exact_on_small_integers(out):
+    # integers in [-16, 16] are exact in e4m3; scales are powers of two, so every
+    # step is exact and the result is the rounded exact integer matmul times s
+    m, k, n = 40, 96, 56
+    rng = np.random.default_rng(71)
+    xi = rng.integers(-16, 17, size=(m, k)).astype(np.float64)
+    wi = rng.integers(-16, 17, size=(k, n)).astype(np.float64)
+    gi = rng.integers(-16, 17, size=(m, n)).astype(np.float64)
+    e8 = lambda a: torch.from_numpy(a.astype(np.float32)).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    xq, wq, gq = e8(xi), e8(wi), e8(gi)
+    sx, sw, sg = 0.25, 2.0, 0.5
+    b = (rng.integers(-64, 64, size=n) / 4).astype(np.float64)
+    bias = enc(b, out)
+    y = oracle.fp8_forward(xq, wq, bias, sx, sw, m, k, n, out)
+    assert np.array_equal(y, round_exact((xi @ wi) * sx * sw + b, out))
+    dx = oracle.fp8_backward_dx(gq, wq, sg, sw, m, k, n, out)
+    assert np.array_equal(dx, round_exact((gi @ wi.T) * sg * sw, out))
+    for chunk in (7, 256):
+        dw = oracle.fp8_backward_dw(xq, gq, sx, sg, m, k, n, out, chunk=chunk)
+        assert np.array_equal(dw, round_exact((xi.T @ gi) * sx * sg, out))
+    rows = [3, 0, 39]
+    assert np.array_equal(oracle.fp8_forward(xq, wq, bias, sx, sw, m, k, n, out, rows=rows), y[rows])
