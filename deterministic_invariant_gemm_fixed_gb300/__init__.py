@@ -50,6 +50,10 @@ SIGNATURES = {
     "bi_version": (ctypes.c_char_p, []),
     "bi_grouped_forward_segmented": (_i32, [_p, _p, _p, _p, _p, _i64, _i64, _i64, _i64, _i32, _p, _i32]),
     "bi_grouped_backward_segmented": (_i32, [_p, _p, _p, _p, _p, _p, _p, _i64, _i64, _i64, _i64, _i32, _p, _i32]),
+    "bi_fp8_quantize": (_i32, [_p, _p, _p, _p, _p, _i64, _i32, _p]),
+    "bi_fp8_forward": (_i32, [_p, _p, _p, _p, _p, _p, _p, _i64, _i64, _i64, _i32, _p]),
+    "bi_fp8_backward_dx": (_i32, [_p, _p, _p, _p, _p, _p, _i64, _i64, _i64, _i32, _p]),
+    "bi_fp8_backward_dw": (_i32, [_p, _p, _p, _p, _p, _p, _i64, _i64, _i64, _i32, _p]),
     "bi_grouped_forward_noalloc": (_i32, [_p, _p, _p, _p, _i64, _i64, _i64, _i64, _i32, _p]),
 }
 
@@ -187,6 +191,26 @@ def bi_grouped_backward_segmented(engine, dx, dw, x, w, dy, offsets, m, k, n, e,
                                               int(strategy))
 
 
+def bi_fp8_quantize(engine, q, amax, src, scale_inv, count, src_dtype, stream=None) -> int:
+    return _lib.bi_fp8_quantize(engine, _ptr(q), _ptr(amax), _ptr(src), _ptr(scale_inv), count,
+                                dtype_code(src_dtype), _stream(stream))
+
+
+def bi_fp8_forward(engine, y, xq, wq, bias, scale_x, scale_w, m, k, n, out_dtype, stream=None) -> int:
+    return _lib.bi_fp8_forward(engine, _ptr(y), _ptr(xq), _ptr(wq), _ptr(bias), _ptr(scale_x), _ptr(scale_w),
+                               m, k, n, dtype_code(out_dtype), _stream(stream))
+
+
+def bi_fp8_backward_dx(engine, dx, gq, wq, scale_g, scale_w, m, k, n, out_dtype, stream=None) -> int:
+    return _lib.bi_fp8_backward_dx(engine, _ptr(dx), _ptr(gq), _ptr(wq), _ptr(scale_g), _ptr(scale_w),
+                                   m, k, n, dtype_code(out_dtype), _stream(stream))
+
+
+def bi_fp8_backward_dw(engine, dw, xq, gq, scale_x, scale_g, m, k, n, out_dtype, stream=None) -> int:
+    return _lib.bi_fp8_backward_dw(engine, _ptr(dw), _ptr(xq), _ptr(gq), _ptr(scale_x), _ptr(scale_g),
+                                   m, k, n, dtype_code(out_dtype), _stream(stream))
+
+
 def bi_grouped_forward_noalloc(y, x, w, row_experts, m, k, n, e, dtype, stream=None) -> int:
     """Scalar-tier grouped forward with no allocation (see include/bi.h); errors
     are read with bi_last_error(None)."""
@@ -257,6 +281,18 @@ class Engine:
                                    strategy=BI_STRATEGY_SCALAR):
         self._ok(bi_grouped_backward_segmented(self.handle, dx, dw, x, w, dy, offsets, m, k, n, e, dtype,
                                                stream, strategy))
+
+    def fp8_quantize(self, q, amax, src, scale_inv, count, src_dtype, stream=None):
+        self._ok(bi_fp8_quantize(self.handle, q, amax, src, scale_inv, count, src_dtype, stream))
+
+    def fp8_forward(self, y, xq, wq, bias, scale_x, scale_w, m, k, n, out_dtype, stream=None):
+        self._ok(bi_fp8_forward(self.handle, y, xq, wq, bias, scale_x, scale_w, m, k, n, out_dtype, stream))
+
+    def fp8_backward_dx(self, dx, gq, wq, scale_g, scale_w, m, k, n, out_dtype, stream=None):
+        self._ok(bi_fp8_backward_dx(self.handle, dx, gq, wq, scale_g, scale_w, m, k, n, out_dtype, stream))
+
+    def fp8_backward_dw(self, dw, xq, gq, scale_x, scale_g, m, k, n, out_dtype, stream=None):
+        self._ok(bi_fp8_backward_dw(self.handle, dw, xq, gq, scale_x, scale_g, m, k, n, out_dtype, stream))
 
     def check(self, stream=None):
         self._ok(bi_engine_check(self.handle, stream))

@@ -97,6 +97,14 @@ cudaError_t tc_grouped_rows(const LaunchCtx& c, bi_dtype dt, int pass_dinput, vo
 cudaError_t tc_grouped_dw(const LaunchCtx& c, bi_dtype dt, float* dw, const void* dy_padded,
                           const void* x_padded, int64_t Mp_max, int64_t M, int64_t K, int64_t N,
                           int64_t E, const uint32_t* seg);
+// FP8 e4m3 scaled matmuls on the CTA pair (pass 0 forward, 1 dX, 2 dW): the
+// f32 product is multiplied by *sa * *sb, then (+ bias), then rounded to out_dt.
+cudaError_t tc_fp8_pass(const LaunchCtx& c, int pass, bi_dtype out_dt, void* out, const uint8_t* a,
+                        const uint8_t* b, const void* bias, const float* sa, const float* sb, int64_t M,
+                        int64_t K, int64_t N);
+// FP8 quantize (fp8.cu): q = e4m3(up(src) * *scale_inv), amax = max |up(src)|.
+cudaError_t fp8_quantize(const LaunchCtx& c, bi_dtype dt, uint8_t* q, float* amax, const void* src,
+                         const float* scale_inv, int64_t count);
 // Upper bound on padded rows for M rows over E experts (multiples of 128 per expert).
 inline int64_t padded_rows_max(int64_t M, int64_t E) { return ((M + 127) / 128) * 128 + E * 128; }
 

@@ -277,6 +277,69 @@ bi_status bi_bias_grad(bi_engine eng, void* db, int db_f32, const void* dy, int6
     return e == cudaSuccess ? BI_OK : cuda_fail(eng, e, "bi_bias_grad");
 }
 
+bi_status bi_fp8_quantize(bi_engine eng, uint8_t* q, float* amax, const void* src, const float* scale_inv,
+                          int64_t count, bi_dtype src_dtype, void* stream) {
+    if (!eng) return fail(nullptr, BI_ERR_INVALID_ARG, "engine is NULL");
+    if (src_dtype != BI_F32 && src_dtype != BI_BF16 && src_dtype != BI_F16)
+        return fail(eng, BI_ERR_INVALID_ARG, "dtype must be BI_F32, BI_BF16 or BI_F16");
+    if (count < 0) return fail(eng, BI_ERR_INVALID_ARG, "count must be >= 0");
+    if (!amax || !scale_inv || (count > 0 && (!q || !src)))
+        return fail(eng, BI_ERR_INVALID_ARG, "q, amax, src and scale_inv must not be NULL");
+    DeviceGuard g(eng->device);
+    if (!g.ok) return fail(eng, BI_ERR_CUDA, "cudaSetDevice failed");
+    cudaError_t e = bi::fp8_quantize(ctx(eng, stream), src_dtype, q, amax, src, scale_inv, count);
+    return e == cudaSuccess ? BI_OK : cuda_fail(eng, e, "bi_fp8_quantize");
+}
+
+namespace {
+
+bi_status fp8_pass(bi_engine eng, int pass, void* out, const uint8_t* a, const uint8_t* b, const void* bias,
+                   const float* sa, const float* sb, int64_t m, int64_t k, int64_t n, bi_dtype out_dtype,
+                   void* stream, const char* name) {
+    bi_status st = check_common(eng, out_dtype, m, k, n);
+    if (st != BI_OK) return st;
+    if (k % 16 != 0 || n % 16 != 0)
+        return fail(eng, BI_ERR_UNSUPPORTED, "FP8 operands need k and n multiples of 16 (16-byte rows)");
+    if (bias && out_dtype == BI_F32)
+        return fail(eng, BI_ERR_UNSUPPORTED, "a bias is supported with bf16 or f16 output");
+    if (!out || !sa || !sb || (m > 0 && (!a || !b)))
+        return fail(eng, BI_ERR_INVALID_ARG, "outputs, operands and scales must not be NULL");
+    if (m == 0 && pass != 2) return BI_OK;
+    if (!aligned16(out) || (m > 0 && (!aligned16(a) || !aligned16(b))))
+        return fail(eng, BI_ERR_MISALIGNED, "FP8 operands and outputs need 16-byte alignment");
+    DeviceGuard g(eng->device);
+    if (!g.ok) return fail(eng, BI_ERR_CUDA, "cudaSetDevice failed");
+    if (m == 0) {
+        cudaError_t e = cudaMemsetAsync(out, 0, static_cast<size_t>(k * n * (out_dtype == BI_F32 ? 4 : 2)),
+                                        static_cast<cudaStream_t>(stream));
+        return e == cudaSuccess ? BI_OK : cuda_fail(eng, e, name);
+    }
+    cudaError_t e = bi::tc_fp8_pass(ctx(eng, stream), pass, out_dtype, out, a, b, bias, sa, sb, m, k, n);
+    return e == cudaSuccess ? BI_OK : cuda_fail(eng, e, name);
+}
+
+}  // namespace
+
+bi_status bi_fp8_forward(bi_engine eng, void* y, const uint8_t* xq, const uint8_t* wq, const void* bias,
+                         const float* scale_x, const float* scale_w, int64_t m, int64_t k, int64_t n,
+                         bi_dtype out_dtype, void* stream) {
+    return fp8_pass(eng, 0, y, xq, wq, bias, scale_x, scale_w, m, k, n, out_dtype, stream, "bi_fp8_forward");
+}
+
+bi_status bi_fp8_backward_dx(bi_engine eng, void* dx, const uint8_t* gq, const uint8_t* wq,
+                             const float* scale_g, const float* scale_w, int64_t m, int64_t k, int64_t n,
+                             bi_dtype out_dtype, void* stream) {
+    return fp8_pass(eng, 1, dx, gq, wq, nullptr, scale_g, scale_w, m, k, n, out_dtype, stream,
+                    "bi_fp8_backward_dx");
+}
+
+bi_status bi_fp8_backward_dw(bi_engine eng, void* dw, const uint8_t* xq, const uint8_t* gq,
+                             const float* scale_x, const float* scale_g, int64_t m, int64_t k, int64_t n,
+                             bi_dtype out_dtype, void* stream) {
+    return fp8_pass(eng, 2, dw, xq, gq, nullptr, scale_x, scale_g, m, k, n, out_dtype, stream,
+                    "bi_fp8_backward_dw");
+}
+
 namespace {
 
 bi_status check_grouped(bi_engine eng, bi_dtype dt, int64_t m, int64_t k, int64_t n, int64_t e) {

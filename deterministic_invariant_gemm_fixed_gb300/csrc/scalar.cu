@@ -386,52 +386,34 @@ __global__ void dw_tree_grouped_kernel(const float* partials, int64_t RC, const 
 // ------------------------------------------------------------------ bias gradient
 
 // Column sums of dY in the fixed order of the dW reduction: chunk c (blockIdx.y)
-// of BI_DW_CHUNK rows, f32 additions from +0.0f in row order.  Each thread owns
-// V consecutive columns (V = 8 with 16-byte loads when the row length allows,
-// else 1), so a warp reads whole 16-byte pieces of a row.  With `partials` the
-// chunk sums go to the workspace for the tree; without it (one chunk) the
-// result is rounded and stored directly.
-template <typename T, int V>
-__global__ void bias_chunk_kernel(const T* dy, int64_t M, int64_t N, float* partials, void* out,
-                                  int out_f32) {
-    const int64_t j0 = (blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x) * V;
+// of BI_DW_CHUNK rows, f32 additions from +0.0f in row order; one thread per
+// column, so a warp reads consecutive columns of one row.  Sixteen rows' loads
+// are issued before their additions, which keeps enough bytes in flight for
+// HBM while the additions stay in row order.  With `partials` the chunk sums go
+// to the workspace for the tree; without it (one chunk) the result is rounded
+// and stored directly.
+template <typename T>
+__global__ void __launch_bounds__(256) bias_chunk_kernel(const T* dy, int64_t M, int64_t N, float* partials,
+                                                        void* out, int out_f32) {
+    const int64_t j = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x;
     const int64_t c = blockIdx.y;
-    if (j0 >= N) return;
+    if (j >= N) return;
     const int64_t r0 = c * BI_DW_CHUNK;
     const int64_t r1 = lmin(M, r0 + BI_DW_CHUNK);
-    float acc[V];
+    const T* col = dy + j;
+    float acc = 0.0f;
+    int64_t r = r0;
+    for (; r + 16 <= r1; r += 16) {
+        T v[16];
 #pragma unroll
-    for (int v = 0; v < V; ++v) acc[v] = 0.0f;
-    if (V == 8) {
-        // eight rows' loads are issued before their additions, which stay in row order
-        int64_t r = r0;
-        for (; r + 8 <= r1; r += 8) {
-            uint4 q[8];
+        for (int u = 0; u < 16; ++u) v[u] = col[(r + u) * N];
 #pragma unroll
-            for (int u = 0; u < 8; ++u) q[u] = __ldg(reinterpret_cast<const uint4*>(dy + (r + u) * N + j0));
-#pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                const T* h = reinterpret_cast<const T*>(&q[u]);
-#pragma unroll
-                for (int v = 0; v < 8; ++v) acc[v] = __fadd_rn(acc[v], Elem<T>::up(h[v]));
-            }
-        }
-        for (; r < r1; ++r) {
-            float f[8];
-            load8<T, true>(dy + r * N + j0, 8, f);
-#pragma unroll
-            for (int v = 0; v < 8; ++v) acc[v] = __fadd_rn(acc[v], f[v]);
-        }
-    } else {
-        for (int64_t r = r0; r < r1; ++r) acc[0] = __fadd_rn(acc[0], Elem<T>::up(dy[r * N + j0]));
+        for (int u = 0; u < 16; ++u) acc = __fadd_rn(acc, Elem<T>::up(v[u]));
     }
-#pragma unroll
-    for (int v = 0; v < V; ++v) {
-        const int64_t j = j0 + v;
-        if (partials) partials[c * N + j] = acc[v];
-        else if (out_f32) static_cast<float*>(out)[j] = acc[v];
-        else static_cast<T*>(out)[j] = Elem<T>::down(acc[v]);
-    }
+    for (; r < r1; ++r) acc = __fadd_rn(acc, Elem<T>::up(col[r * N]));
+    if (partials) partials[c * N + j] = acc;
+    else if (out_f32) static_cast<float*>(out)[j] = acc;
+    else static_cast<T*>(out)[j] = Elem<T>::down(acc);
 }
 
 // ------------------------------------------------------------------ host helpers
@@ -538,16 +520,8 @@ cudaError_t scalar_dw(const LaunchCtx& c, bi_dtype dt, void* out, int out_f32, c
 template <typename T>
 void launch_bias_chunks(const LaunchCtx& c, const void* dy, int64_t M, int64_t N, int64_t J, float* part,
                         void* out, int out_f32) {
-    const T* d = static_cast<const T*>(dy);
-    // 8 columns per thread when every row starts on a 16-byte boundary
-    const bool vec = sizeof(T) == 2 && N % 8 == 0 && aligned16(dy);
-    if (vec) {
-        dim3 grid(static_cast<unsigned>((N / 8 + 127) / 128), static_cast<unsigned>(J));
-        bias_chunk_kernel<T, 8><<<grid, 128, 0, c.stream>>>(d, M, N, part, out, out_f32);
-    } else {
-        dim3 grid(static_cast<unsigned>((N + 255) / 256), static_cast<unsigned>(J));
-        bias_chunk_kernel<T, 1><<<grid, 256, 0, c.stream>>>(d, M, N, part, out, out_f32);
-    }
+    dim3 grid(static_cast<unsigned>((N + 255) / 256), static_cast<unsigned>(J));
+    bias_chunk_kernel<T><<<grid, 256, 0, c.stream>>>(static_cast<const T*>(dy), M, N, part, out, out_f32);
 }
 
 cudaError_t bias_grad(const LaunchCtx& c, bi_dtype dt, void* out, int out_f32, const void* dy,

@@ -26,6 +26,7 @@
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+#include <cuda_fp8.h>
 
 #include "bi_internal.h"
 
@@ -57,6 +58,8 @@ struct Params {
     const uint32_t* seg;     // grouped: segment table
     const uint32_t* perm;    // grouped rows: sorted position -> original row
     int E;
+    const float* scale_a;    // FP8: per-tensor scales applied to the f32 product
+    const float* scale_b;
     int* status;
     unsigned long long wait_limit;
 };
@@ -574,14 +577,24 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap
         : "memory");
 }
 
-__device__ __forceinline__ void mma_f16_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
-                                             uint32_t idesc, uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
-        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
-        : "memory");
+template <int IN>
+__device__ __forceinline__ void mma_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                         uint32_t accumulate) {
+    if (IN == 2) {  // e4m3 x e4m3 -> f32
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "setp.ne.b32 p, %4, 0;\n\t"
+            "tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+            "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+            : "memory");
+    } else {        // f16 x f16 or bf16 x bf16 -> f32
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "setp.ne.b32 p, %4, 0;\n\t"
+            "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+            "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+            : "memory");
+    }
 }
 
 __device__ __forceinline__ void mma_commit_pair_mc(uint32_t bar, uint16_t mask) {
@@ -601,17 +614,26 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar_cluster) {
                  : "memory");
 }
 
-template <int FMT, bool A_MN, bool B_MN>
+// kind::f16: format 0 = f16, 1 = bf16; kind::f8f6f4: format 0 = e4m3.
+template <int IN, bool A_MN, bool B_MN>
 __device__ __forceinline__ constexpr uint32_t instr_desc_pair() {
-    return (1u << 4) | (static_cast<uint32_t>(FMT) << 7) | (static_cast<uint32_t>(FMT) << 10) |
+    constexpr uint32_t FMT = IN == 1 ? 1u : 0u;
+    return (1u << 4) | (FMT << 7) | (FMT << 10) |
            (static_cast<uint32_t>(A_MN) << 15) | (static_cast<uint32_t>(B_MN) << 16) |
            (static_cast<uint32_t>(256 >> 3) << 17) | (static_cast<uint32_t>(256 >> 4) << 24);
 }
 
-template <int FMT, bool A_MN, bool B_MN, bool OUT_F32>
+// IN: 0 f16, 1 bf16, 2 e4m3 (scaled by *scale_a * *scale_b).  OUT: 0 f16,
+// 1 bf16, 2 f32.  A 64-wide (16-bit) or 128-wide (8-bit) contraction block is
+// one 128-byte swizzle row per tile row; four MMAs of K = 16 / 32 cover it.
+template <int IN, int OUT, bool A_MN, bool B_MN>
 __global__ void __launch_bounds__(THREADS, 1)
     tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         const Params p) {
+    constexpr int ES = IN == 2 ? 1 : 2;     // operand element size, bytes
+    constexpr int BKE = 128 / ES;           // contraction elements per block
+    constexpr int MN_ATOMS = ES;            // 128-byte atoms across a 128-wide MN-major tile
+    constexpr uint32_t MN_STEP = (32 / ES) * 128;  // one MMA's rows of an MN-major tile, bytes
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     uint8_t* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
@@ -685,16 +707,16 @@ __global__ void __launch_bounds__(THREADS, 1)
                 if (crank == 0) mbar_expect_tx(full_bar(s), 2 * P_STAGE_BYTES);
                 const uint32_t a_dst = sbase + s * P_STAGE_BYTES;
                 const uint32_t b_dst = a_dst + P_A_BYTES;
-                const int kofs = kb * BK;
+                const int kofs = kb * BKE;
                 if (A_MN) {
-                    for (int a = 0; a < 2; ++a)
-                        tma_load_2d_pair(a_dst + a * (BK * 128), &tmA, arow + a * 64, kofs, fb_leader);
+                    for (int a = 0; a < MN_ATOMS; ++a)
+                        tma_load_2d_pair(a_dst + a * (BKE * 128), &tmA, arow + a * (128 / ES), kofs, fb_leader);
                 } else {
                     tma_load_2d_pair(a_dst, &tmA, kofs, arow, fb_leader);
                 }
                 if (B_MN) {
-                    for (int b = 0; b < 2; ++b)
-                        tma_load_2d_pair(b_dst + b * (BK * 128), &tmB, bcol + b * 64, kofs, fb_leader);
+                    for (int b = 0; b < MN_ATOMS; ++b)
+                        tma_load_2d_pair(b_dst + b * (BKE * 128), &tmB, bcol + b * (128 / ES), kofs, fb_leader);
                 } else {
                     tma_load_2d_pair(b_dst, &tmB, kofs, bcol, fb_leader);
                 }
@@ -707,7 +729,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         // barrier below before either CTA releases its shared memory.
     } else if (warp == 1 && lane == 0 && crank == 0) {
         // ------------------------------------------------------------ MMA issuer (CTA 0)
-        constexpr uint32_t idesc = instr_desc_pair<FMT, A_MN, B_MN>();
+        constexpr uint32_t idesc = instr_desc_pair<IN, A_MN, B_MN>();
         int s = 0;
         uint32_t ph = 0;
         int ab = 0;
@@ -723,12 +745,14 @@ __global__ void __launch_bounds__(THREADS, 1)
                 const uint32_t a_s = sbase + s * P_STAGE_BYTES;
                 const uint32_t b_s = a_s + P_A_BYTES;
 #pragma unroll
-                for (int kk = 0; kk < BK / UK; ++kk) {
-                    const uint64_t ad = A_MN ? smem_desc(a_s + kk * 2048, BK * 128, 1024)
+                for (int kk = 0; kk < 4; ++kk) {
+                    // K-major: 32 bytes along the swizzled row per MMA;
+                    // MN-major: one MMA's worth of 128-byte rows
+                    const uint64_t ad = A_MN ? smem_desc(a_s + kk * MN_STEP, BKE * 128, 1024)
                                              : smem_desc(a_s + kk * 32, 16, 1024);
-                    const uint64_t bd = B_MN ? smem_desc(b_s + kk * 2048, BK * 128, 1024)
+                    const uint64_t bd = B_MN ? smem_desc(b_s + kk * MN_STEP, BKE * 128, 1024)
                                              : smem_desc(b_s + kk * 32, 16, 1024);
-                    mma_f16_pair(d_tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+                    mma_pair<IN>(d_tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
                 }
                 mma_commit_pair_mc(empty_bar(s), 0x3);
                 if (++s == P_STAGES) { s = 0; ph ^= 1u; }
@@ -747,6 +771,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         const uint32_t tempty_leader1 = mapa_rank(tempty_bar(1), 0);
         int ab = 0;
         uint32_t aph = 0;
+        const float scale = IN == 2 ? __fmul_rn(__ldg(p.scale_a), __ldg(p.scale_b)) : 1.0f;
         for (int t = cidx; t < total; t += ncl) {
             int mpair, nb;
             unit_tile(t, mpair, nb);
@@ -767,14 +792,18 @@ __global__ void __launch_bounds__(THREADS, 1)
                 float f[16];
 #pragma unroll
                 for (int i = 0; i < 16; ++i) f[i] = __uint_as_float(v[i]);
+                if (IN == 2) {
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) f[i] = __fmul_rn(f[i], scale);
+                }
                 const int64_t cb = col0 + c0;
-                if (p.bias != nullptr) {
+                if (p.bias != nullptr) {  // the bias has the output's type (16-bit outputs only)
 #pragma unroll
                     for (int i = 0; i < 16; ++i)
-                        if (cb + i < p.cols) f[i] = f[i] + OutT<FMT>::load(p.bias, cb + i);
+                        if (cb + i < p.cols) f[i] = __fadd_rn(f[i], OutT<OUT == 1 ? 1 : 0>::load(p.bias, cb + i));
                 }
                 const bool full = cb + 16 <= p.cols;
-                if (OUT_F32) {
+                if (OUT == 2) {
                     float* dst = static_cast<float*>(p.out) + orow * p.ldo + cb;
                     if (full) {
 #pragma unroll
@@ -785,23 +814,24 @@ __global__ void __launch_bounds__(THREADS, 1)
                             if (cb + i < p.cols) dst[i] = f[i];
                     }
                 } else {
-                    using T = typename OutT<FMT>::T;
+                    using O = OutT<OUT == 1 ? 1 : 0>;
+                    using T = typename O::T;
                     T* dst = static_cast<T*>(p.out) + orow * p.ldo + cb;
                     if (full) {
                         uint4 w0, w1;
-                        w0.x = OutT<FMT>::pack(f[0], f[1]);
-                        w0.y = OutT<FMT>::pack(f[2], f[3]);
-                        w0.z = OutT<FMT>::pack(f[4], f[5]);
-                        w0.w = OutT<FMT>::pack(f[6], f[7]);
-                        w1.x = OutT<FMT>::pack(f[8], f[9]);
-                        w1.y = OutT<FMT>::pack(f[10], f[11]);
-                        w1.z = OutT<FMT>::pack(f[12], f[13]);
-                        w1.w = OutT<FMT>::pack(f[14], f[15]);
+                        w0.x = O::pack(f[0], f[1]);
+                        w0.y = O::pack(f[2], f[3]);
+                        w0.z = O::pack(f[4], f[5]);
+                        w0.w = O::pack(f[6], f[7]);
+                        w1.x = O::pack(f[8], f[9]);
+                        w1.y = O::pack(f[10], f[11]);
+                        w1.z = O::pack(f[12], f[13]);
+                        w1.w = O::pack(f[14], f[15]);
                         reinterpret_cast<uint4*>(dst)[0] = w0;
                         reinterpret_cast<uint4*>(dst)[1] = w1;
                     } else {
                         for (int i = 0; i < 16; ++i)
-                            if (cb + i < p.cols) OutT<FMT>::store1(dst, i, f[i]);
+                            if (cb + i < p.cols) O::store1(dst, i, f[i]);
                     }
                 }
             }
@@ -881,9 +911,9 @@ cudaError_t launch(const LaunchCtx& c, const CUtensorMap& a, const CUtensorMap& 
 }
 
 
-template <int FMT, bool A_MN, bool B_MN, bool OUT_F32>
+template <int IN, int OUT, bool A_MN, bool B_MN>
 cudaError_t launch_pair(const LaunchCtx& c, const CUtensorMap& a, const CUtensorMap& b, Params p) {
-    auto kern = tc_gemm_pair_kernel<FMT, A_MN, B_MN, OUT_F32>;
+    auto kern = tc_gemm_pair_kernel<IN, OUT, A_MN, B_MN>;
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
     static int max_clusters = 0;
@@ -936,7 +966,7 @@ cudaError_t forward_t(const LaunchCtx& c, bi_dtype dt, void* y, const void* x, c
     p.num_m = static_cast<int>((M + BM - 1) / BM);
     p.num_n = static_cast<int>((N + BN - 1) / BN);
     p.num_kb = static_cast<int>((K + BK - 1) / BK);
-    return launch_pair<FMT, false, true, false>(c, a, b, p);
+    return launch_pair<FMT, FMT, false, true>(c, a, b, p);
 }
 
 template <int FMT>
@@ -951,7 +981,7 @@ cudaError_t dx_t(const LaunchCtx& c, bi_dtype dt, void* dx, const void* dy, cons
     p.num_m = static_cast<int>((M + BM - 1) / BM);
     p.num_n = static_cast<int>((K + BN - 1) / BN);
     p.num_kb = static_cast<int>((N + BK - 1) / BK);
-    return launch_pair<FMT, false, false, false>(c, a, b, p);
+    return launch_pair<FMT, FMT, false, false>(c, a, b, p);
 }
 
 template <int FMT, bool F32>
@@ -966,7 +996,7 @@ cudaError_t dw_t(const LaunchCtx& c, bi_dtype dt, void* dw, const void* x, const
     p.num_m = static_cast<int>((K + BM - 1) / BM);
     p.num_n = static_cast<int>((N + BN - 1) / BN);
     p.num_kb = static_cast<int>((M + BK - 1) / BK);
-    return launch_pair<FMT, true, true, F32>(c, a, b, p);
+    return launch_pair<FMT, F32 ? 2 : FMT, true, true>(c, a, b, p);
 }
 
 template <int FMT>
@@ -1015,6 +1045,55 @@ cudaError_t grouped_dw_t(const LaunchCtx& c, bi_dtype dt, float* dw, const void*
                                                             E * int64_t(p.num_m) * p.num_n);
 }
 
+// 8-bit row-major tensor [outer][inner], box {128, box_outer}, 128-byte swizzle.
+cudaError_t make_map8(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer, uint32_t box_outer) {
+    auto enc = encode_fn();
+    if (!enc) return cudaErrorNotSupported;
+    cuuint64_t dims[2] = {inner, outer};
+    cuuint64_t strides[1] = {inner};
+    cuuint32_t box[2] = {128, box_outer};
+    cuuint32_t es[2] = {1, 1};
+    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(ptr), dims, strides, box, es,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+template <int OUT>
+cudaError_t fp8_pass_t(const LaunchCtx& c, int pass, void* out, const uint8_t* a, const uint8_t* b,
+                       const void* bias, const float* sa, const float* sb, int64_t M, int64_t K, int64_t N) {
+    CUtensorMap ma, mb;
+    cudaError_t e;
+    Params p{};
+    p.scale_a = sa; p.scale_b = sb; p.bias = bias;
+    if (pass == 0) {         // y = xq wq: A = xq [M,K] K-major, B = wq [K,N] MN-major
+        if ((e = make_map8(&ma, a, K, M, 128)) != cudaSuccess) return e;
+        if ((e = make_map8(&mb, b, N, K, 128)) != cudaSuccess) return e;
+        p.out = out; p.ldo = N; p.rows = M; p.cols = N;
+        p.num_m = static_cast<int>((M + BM - 1) / BM);
+        p.num_n = static_cast<int>((N + BN - 1) / BN);
+        p.num_kb = static_cast<int>((K + 127) / 128);
+        return launch_pair<2, OUT, false, true>(c, ma, mb, p);
+    }
+    if (pass == 1) {         // dx = gq wq^T: A = gq [M,N] K-major, B = wq [K,N] rows k, contraction n
+        if ((e = make_map8(&ma, a, N, M, 128)) != cudaSuccess) return e;
+        if ((e = make_map8(&mb, b, N, K, 128)) != cudaSuccess) return e;
+        p.out = out; p.ldo = K; p.rows = M; p.cols = K;
+        p.num_m = static_cast<int>((M + BM - 1) / BM);
+        p.num_n = static_cast<int>((K + BN - 1) / BN);
+        p.num_kb = static_cast<int>((N + 127) / 128);
+        return launch_pair<2, OUT, false, false>(c, ma, mb, p);
+    }
+    // dw = xq^T gq: A = xq [M,K] (out k, contraction m), B = gq [M,N] (out n, contraction m)
+    if ((e = make_map8(&ma, a, K, M, 128)) != cudaSuccess) return e;
+    if ((e = make_map8(&mb, b, N, M, 128)) != cudaSuccess) return e;
+    p.out = out; p.ldo = N; p.rows = K; p.cols = N; p.bias = nullptr;
+    p.num_m = static_cast<int>((K + BM - 1) / BM);
+    p.num_n = static_cast<int>((N + BN - 1) / BN);
+    p.num_kb = static_cast<int>((M + 127) / 128);
+    return launch_pair<2, OUT, true, true>(c, ma, mb, p);
+}
+
 }  // namespace
 
 cudaError_t tc_forward(const LaunchCtx& c, bi_dtype dt, void* y, const void* x, const void* w,
@@ -1042,6 +1121,16 @@ cudaError_t tc_grouped_rows(const LaunchCtx& c, bi_dtype dt, int pass_dinput, vo
     return dt == BI_BF16
                ? grouped_rows_t<1>(c, dt, pass_dinput, out, a_padded, Mp_max, w, M, K, N, E, seg, perm)
                : grouped_rows_t<0>(c, dt, pass_dinput, out, a_padded, Mp_max, w, M, K, N, E, seg, perm);
+}
+
+cudaError_t tc_fp8_pass(const LaunchCtx& c, int pass, bi_dtype out_dt, void* out, const uint8_t* a,
+                       const uint8_t* b, const void* bias, const float* sa, const float* sb, int64_t M,
+                       int64_t K, int64_t N) {
+    switch (out_dt) {
+        case BI_BF16: return fp8_pass_t<1>(c, pass, out, a, b, bias, sa, sb, M, K, N);
+        case BI_F16: return fp8_pass_t<0>(c, pass, out, a, b, bias, sa, sb, M, K, N);
+        default: return fp8_pass_t<2>(c, pass, out, a, b, bias, sa, sb, M, K, N);
+    }
 }
 
 cudaError_t tc_grouped_dw(const LaunchCtx& c, bi_dtype dt, float* dw, const void* dy_padded,

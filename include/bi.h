@@ -155,6 +155,43 @@ bi_status bi_backward_dw(bi_engine engine, void* dw, int dw_f32, const void* x, 
 bi_status bi_bias_grad(bi_engine engine, void* db, int db_f32, const void* dy, int64_t m, int64_t n,
                        bi_dtype dtype, void* stream);
 
+/* ---- FP8 e4m3 per-tensor-scaled linear (tensor-core tier only) ---------
+ * Source: AstrAI csrc/kernels/fp8_mm.cu (quantize_kernel; fp8_linear_forward_scaled
+ * and fp8_linear_backward_scaled: operands quantized with 1/scale, the GEMM's
+ * f32 product multiplied by the two scales).  e4m3 here is the "fn" format: no
+ * infinities, largest finite 448, NaN 0x7F/0xFF. */
+
+/* q[i] = e4m3( up(src[i]) * (*scale_inv) ): one f32 multiply, then round to
+ * nearest even with saturation to +-448.  *amax = max |up(src[i])| over the
+ * unscaled values (NaN ignored; +0 for count = 0); it is zeroed first, then
+ * reduced with an exact, order-independent maximum, so it is bit-identical
+ * run to run.  src has src_dtype; q, amax, scale_inv are device pointers. */
+bi_status bi_fp8_quantize(bi_engine engine, uint8_t* q, float* amax, const void* src, const float* scale_inv,
+                          int64_t count, bi_dtype src_dtype, void* stream);
+
+/* y[M,N] = round( (chain_k xq[m,k] * wq[k,n]) * (*scale_x * *scale_w) + bias[n] ),
+ * xq [M,K] and wq [K,N] e4m3 codes, f32 accumulation, the scale product and
+ * the scaling each one f32 rounding, bias (nullable; out_dtype, bf16/f16 only)
+ * added in f32, one rounding to out_dtype (bf16, f16 or f32).  tcgen05
+ * kind::f8f6f4 on CTA pairs, fixed K order, no split: run-to-run and batch
+ * invariant like the bf16 tensor-core tier.  k and n multiples of 16;
+ * 16-byte aligned pointers. */
+bi_status bi_fp8_forward(bi_engine engine, void* y, const uint8_t* xq, const uint8_t* wq, const void* bias,
+                         const float* scale_x, const float* scale_w, int64_t m, int64_t k, int64_t n,
+                         bi_dtype out_dtype, void* stream);
+
+/* dx[M,K] = round( (chain_n gq[m,n] * wq[k,n]) * (*scale_g * *scale_w) ). */
+bi_status bi_fp8_backward_dx(bi_engine engine, void* dx, const uint8_t* gq, const uint8_t* wq,
+                             const float* scale_g, const float* scale_w, int64_t m, int64_t k, int64_t n,
+                             bi_dtype out_dtype, void* stream);
+
+/* dw[K,N] = round( (sum over m of xq[m,k] * gq[m,n]) * (*scale_x * *scale_g) ),
+ * the rows chained in ascending order in the tensor-memory accumulator; m = 0
+ * writes +0. */
+bi_status bi_fp8_backward_dw(bi_engine engine, void* dw, const uint8_t* xq, const uint8_t* gq,
+                             const float* scale_x, const float* scale_g, int64_t m, int64_t k, int64_t n,
+                             bi_dtype out_dtype, void* stream);
+
 /* Grouped forward: y[m,:] = round( X[m,:] * W[e(m)]^T ) with W [E,N,K] and
  * e(m) = row_experts[m]; rows with e(m) >= E are +0.  Rows need not be sorted.
  * Source: rublas 0.1.45 src/tensor_grouped/mod.rs, fn grouped_matmul_nt
