@@ -317,6 +317,26 @@ def secondary(eng, stream, reps=5):
     out["bias_grad"] = {"workload": "bf16 dY 8192x12288 column sums", "gbs": (g.nbytes + db.nbytes) / t_bg / 1e9,
                         "us": t_bg * 1e6}
     del g
+    # FP8 e4m3 per-tensor-scaled passes on the qkv projection (pre-quantized operands)
+    m, k, n = synth.SEVEN_B_M, 4096, 12288
+    xq = torch.randint(0, 0x70, (m, k), dtype=torch.uint8, device="cuda")
+    wq = torch.randint(0, 0x70, (k, n), dtype=torch.uint8, device="cuda")
+    gq = torch.randint(0, 0x70, (m, n), dtype=torch.uint8, device="cuda")
+    one = torch.ones(1, dtype=torch.float32, device="cuda")
+    y8 = torch.empty(m, n, dtype=torch.bfloat16, device="cuda")
+    dx8 = torch.empty(m, k, dtype=torch.bfloat16, device="cuda")
+    dw8 = torch.empty(k, n, dtype=torch.float32, device="cuda")
+
+    def fp8_step():
+        eng.fp8_forward(y8, xq, wq, None, one, one, m, k, n, "bf16", stream)
+        eng.fp8_backward_dx(dx8, gq, wq, one, one, m, k, n, "bf16", stream)
+        eng.fp8_backward_dw(dw8, xq, gq, one, one, m, k, n, "f32", stream)
+    t8 = timeit(fp8_step)
+    pk, _ = peaks()
+    fp8_peak = 2.0 * float(pk.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))  # nominal fp8:bf16 = 2:1
+    out["fp8_qkv"] = {"workload": "e4m3 qkv 8192x4096x12288 fwd+dX+dW", "tflops": 3 * 2.0 * m * k * n / t8 / 1e12,
+                      "peak_tflops": fp8_peak, "frac": 3 * 2.0 * m * k * n / t8 / 1e12 / fp8_peak}
+    del xq, wq, gq, y8, dx8, dw8
     # GEMV f16 1x4096x4096, tensor-core tier (HBM-bound): W rotated over 8 copies > L2
     k = n = 4096
     ws = [synth.uniform((k, n), -1, 1, "f16", 100 + i).cuda() for i in range(8)]
