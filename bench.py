@@ -337,6 +337,27 @@ def secondary(eng, stream, reps=5):
     out["fp8_qkv"] = {"workload": "e4m3 qkv 8192x4096x12288 fwd+dX+dW", "tflops": 3 * 2.0 * m * k * n / t8 / 1e12,
                       "peak_tflops": fp8_peak, "frac": 3 * 2.0 * m * k * n / t8 / 1e12 / fp8_peak}
     del xq, wq, gq, y8, dx8, dw8
+    # f32 operands on the tensor cores (3xTF32: split kernels + three tf32 MMAs per
+    # contraction step), the o-projection shape 8192x4096x4096 in f32
+    m, k, n = synth.SEVEN_B_M, 4096, 4096
+    x, w, dy, _ = synth.dense_inputs(m, k, n, "f32", b=None)
+    X, W, DY = x.cuda(), w.cuda(), dy.cuda()
+    del x, w, dy
+    Yf = torch.empty(m, n, device="cuda")
+    DXf = torch.empty(m, k, device="cuda")
+    DWf = torch.empty(k, n, device="cuda")
+
+    def tf32_step():
+        eng.forward(Yf, X, W, None, m, k, n, "f32", stream, 1)
+        eng.backward_dx(DXf, DY, W, m, k, n, "f32", stream, 1)
+        eng.backward_dw(DWf, 1, X, DY, m, k, n, "f32", stream, 1)
+    t32 = timeit(tf32_step)
+    # ceiling: measured bf16 peak x the nominal tf32:bf16 ratio (1.1 : 2.25), over 3 MMAs per product
+    tf32_ceiling = float(pk.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])) * (1.1 / 2.25) / 3
+    v32 = 3 * 2.0 * m * k * n / t32 / 1e12
+    out["tf32x3_f32_o"] = {"workload": "f32 o-projection 8192x4096x4096 fwd+dX+dW, 3xTF32", "tflops": v32,
+                           "ceiling_tflops": tf32_ceiling, "frac": v32 / tf32_ceiling}
+    del X, W, DY, Yf, DXf, DWf
     # GEMV f16 1x4096x4096, tensor-core tier (HBM-bound): W rotated over 8 copies > L2
     k = n = 4096
     ws = [synth.uniform((k, n), -1, 1, "f16", 100 + i).cuda() for i in range(8)]

@@ -79,6 +79,54 @@ bi::LaunchCtx ctx(bi_engine eng, void* stream) {
                          eng->wait_limit_ns};
 }
 
+// f32 operands on the tensor cores (3xTF32).  Each operand is a row-major
+// [rows][cols] f32 matrix; `transpose` says its contraction index runs down the
+// columns, so the split writes its TF32 parts transposed, rows padded to a
+// multiple of 4 (16-byte TMA strides at any batch size).  The pair kernel then
+// reads both operands K-major from stream-ordered scratch.
+struct Tf32Operand {
+    const void* src;
+    int64_t rows, cols;
+    bool transpose;
+    int64_t ld() const { return transpose ? (rows + 3) / 4 * 4 : cols; }
+    int64_t bytes() const { return ((transpose ? cols : rows) * ld() * 4 + 255) / 256 * 256; }
+};
+
+bi_status tf32x3(bi_engine eng, const bi::LaunchCtx& c, const Tf32Operand& a, const Tf32Operand& b, void* out,
+                 int64_t ldo, const void* bias, int64_t rows, int64_t cols, int64_t depth, const char* name) {
+    const int64_t a_b = a.bytes(), b_b = b.bytes();
+    // contractions longer than one piece: pieces into f32 partials, then their sum
+    const int64_t J = (depth + bi::TF32X3_PIECE - 1) / bi::TF32X3_PIECE;
+    const int64_t p_b = J > 1 ? (J * rows * cols * 4 + 255) / 256 * 256 : 0;
+    Scratch sc(eng, c.stream, static_cast<size_t>(2 * (a_b + b_b) + p_b));
+    if (sc.err != cudaSuccess) return cuda_fail(eng, sc.err, "3xTF32 scratch");
+    uint8_t* base = static_cast<uint8_t*>(sc.ptr);
+    float* ah = reinterpret_cast<float*>(base);
+    float* al = reinterpret_cast<float*>(base + a_b);
+    float* bh = reinterpret_cast<float*>(base + 2 * a_b);
+    float* bl = reinterpret_cast<float*>(base + 2 * a_b + b_b);
+    float* part = reinterpret_cast<float*>(base + 2 * (a_b + b_b));
+    cudaError_t e = bi::tf32_split(c, static_cast<const float*>(a.src), ah, al, a.rows, a.cols, a.transpose, a.ld());
+    if (e == cudaSuccess)
+        e = bi::tf32_split(c, static_cast<const float*>(b.src), bh, bl, b.rows, b.cols, b.transpose, b.ld());
+    if (J == 1) {
+        if (e == cudaSuccess)
+            e = bi::tc_tf32x3_pass(c, ah, al, a.ld(), bh, bl, b.ld(), static_cast<float*>(out), ldo,
+                                   static_cast<const float*>(bias), rows, cols, depth);
+        return e == cudaSuccess ? BI_OK : cuda_fail(eng, e, name);
+    }
+    for (int64_t j = 0; j < J && e == cudaSuccess; ++j) {
+        const int64_t d0 = j * bi::TF32X3_PIECE;  // a multiple of 4 elements: 16-byte aligned bases
+        const int64_t len = std::min(bi::TF32X3_PIECE, depth - d0);
+        e = bi::tc_tf32x3_pass(c, ah + d0, al + d0, a.ld(), bh + d0, bl + d0, b.ld(), part + j * rows * cols, cols,
+                               nullptr, rows, cols, len);
+    }
+    if (e == cudaSuccess)
+        e = bi::tf32_sum_partials(c, part, J, rows, cols, static_cast<const float*>(bias), static_cast<float*>(out),
+                                  ldo);
+    return e == cudaSuccess ? BI_OK : cuda_fail(eng, e, name);
+}
+
 }  // namespace
 
 namespace bi {
@@ -91,8 +139,12 @@ const char* bi_version(void) { return "bi 0.1.0 (sm_103a)"; }
 
 int bi_dispatch_tier(int pass, bi_dtype dtype, int tensor_cores, int64_t k, int64_t n) {
     if (!tensor_cores) return 0;
-    if (dtype != BI_BF16 && dtype != BI_F16) return 0;  // f32 operands: scalar tier
-    if (k <= 0 || n <= 0 || k % 8 != 0 || n % 8 != 0) return 0;  // 16-byte rows for TMA
+    if (dtype != BI_BF16 && dtype != BI_F16 && dtype != BI_F32) return 0;
+    // f32 operands reach the tensor cores through the 3xTF32 split, dense passes only
+    const bool f32 = dtype == BI_F32;
+    if (f32 && pass > BI_PASS_DW) return 0;
+    const int64_t unit = f32 ? 4 : 8;  // elements per 16-byte row unit, for TMA
+    if (k <= 0 || n <= 0 || k % unit != 0 || n % unit != 0) return 0;
     switch (pass) {
         case BI_PASS_FORWARD:
         case BI_PASS_GROUPED_FORWARD: return n >= 64 ? 1 : 0;
@@ -203,6 +255,8 @@ bi_status bi_forward(bi_engine eng, void* y, const void* x, const void* w, const
     DeviceGuard g(eng->device);
     if (!g.ok) return fail(eng, BI_ERR_CUDA, "cudaSetDevice failed");
     const bi::LaunchCtx c = ctx(eng, stream);
+    if (tier && dtype == BI_F32)  // y = x w: x K-major as stored, w transposed
+        return tf32x3(eng, c, {x, m, k, false}, {w, k, n, true}, y, n, bias, m, n, k, "bi_forward");
     cudaError_t e = tier ? bi::tc_forward(c, dtype, y, x, w, bias, m, k, n)
                          : bi::scalar_rows(c, dtype, y, x, w, bias, m, k, n, 0);
     return e == cudaSuccess ? BI_OK : cuda_fail(eng, e, "bi_forward");
@@ -220,6 +274,8 @@ bi_status bi_backward_dx(bi_engine eng, void* dx, const void* dy, const void* w,
     DeviceGuard g(eng->device);
     if (!g.ok) return fail(eng, BI_ERR_CUDA, "cudaSetDevice failed");
     const bi::LaunchCtx c = ctx(eng, stream);
+    if (tier && dtype == BI_F32)  // dx = dy w^T: both K-major as stored
+        return tf32x3(eng, c, {dy, m, n, false}, {w, k, n, false}, dx, k, nullptr, m, k, n, "bi_backward_dx");
     cudaError_t e = tier ? bi::tc_dx(c, dtype, dx, dy, w, m, k, n)
                          : bi::scalar_rows(c, dtype, dx, dy, w, nullptr, m, n, k, 1);
     return e == cudaSuccess ? BI_OK : cuda_fail(eng, e, "bi_backward_dx");
@@ -245,6 +301,8 @@ bi_status bi_backward_dw(bi_engine eng, void* dw, int dw_f32, const void* x, con
         return e == cudaSuccess ? BI_OK : cuda_fail(eng, e, "bi_backward_dw");
     }
     const bi::LaunchCtx c = ctx(eng, stream);
+    if (tier && dtype == BI_F32)  // dw = x^T dy: both transposed (contraction over m)
+        return tf32x3(eng, c, {x, m, k, true}, {dy, m, n, true}, dw, n, nullptr, k, n, m, "bi_backward_dw");
     if (tier) {
         cudaError_t e = bi::tc_dw(c, dtype, dw, out_f32, x, dy, m, k, n);
         return e == cudaSuccess ? BI_OK : cuda_fail(eng, e, "bi_backward_dw");

@@ -556,11 +556,14 @@ __global__ void __launch_bounds__(THREADS, 1)
 // empty[s] (each CTA, released by CTA 0's commit multicast to both), tfull[b]
 // (each CTA, commit multicast), tempty[b] (CTA 0, 8 arrivals: the 4 epilogue
 // warps of each CTA).
-constexpr int P_STAGES = 7;
-constexpr int P_A_BYTES = 128 * BK * 2;
+constexpr int P_A_BYTES = 128 * BK * 2;  // one 128 x 128-byte tile
 constexpr int P_B_BYTES = 128 * BK * 2;
-constexpr int P_STAGE_BYTES = P_A_BYTES + P_B_BYTES;
-constexpr int P_SMEM_BYTES = 1024 + P_STAGES * P_STAGE_BYTES + BAR_BYTES;
+// Stage layout per operand type: one A and one B tile, or for the 3xTF32 mode
+// (IN = 3) the high and low parts of both (A_hi, B_hi, A_lo, B_lo).
+__host__ __device__ constexpr int p_tiles(int in) { return in == 3 ? 2 : 1; }
+__host__ __device__ constexpr int p_stage_bytes(int in) { return p_tiles(in) * (P_A_BYTES + P_B_BYTES); }
+__host__ __device__ constexpr int p_stages(int in) { return in == 3 ? 3 : 7; }
+__host__ __device__ constexpr int p_smem_bytes(int in) { return 1024 + p_stages(in) * p_stage_bytes(in) + BAR_BYTES; }
 
 __device__ __forceinline__ uint32_t mapa_rank(uint32_t saddr, uint32_t rank) {
     uint32_t r;
@@ -580,7 +583,14 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap
 template <int IN>
 __device__ __forceinline__ void mma_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
                                          uint32_t accumulate) {
-    if (IN == 2) {  // e4m3 x e4m3 -> f32
+    if (IN == 3) {  // tf32 x tf32 -> f32
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "setp.ne.b32 p, %4, 0;\n\t"
+            "tcgen05.mma.cta_group::2.kind::tf32 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+            "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+            : "memory");
+    } else if (IN == 2) {  // e4m3 x e4m3 -> f32
         asm volatile(
             "{\n\t.reg .pred p;\n\t"
             "setp.ne.b32 p, %4, 0;\n\t"
@@ -614,24 +624,39 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar_cluster) {
                  : "memory");
 }
 
-// kind::f16: format 0 = f16, 1 = bf16; kind::f8f6f4: format 0 = e4m3.
+// kind::f16: format 0 = f16, 1 = bf16; kind::f8f6f4: 0 = e4m3; kind::tf32: 2 = tf32.
 template <int IN, bool A_MN, bool B_MN>
 __device__ __forceinline__ constexpr uint32_t instr_desc_pair() {
-    constexpr uint32_t FMT = IN == 1 ? 1u : 0u;
+    constexpr uint32_t FMT = IN == 1 ? 1u : (IN == 3 ? 2u : 0u);
     return (1u << 4) | (FMT << 7) | (FMT << 10) |
            (static_cast<uint32_t>(A_MN) << 15) | (static_cast<uint32_t>(B_MN) << 16) |
            (static_cast<uint32_t>(256 >> 3) << 17) | (static_cast<uint32_t>(256 >> 4) << 24);
 }
 
-// IN: 0 f16, 1 bf16, 2 e4m3 (scaled by *scale_a * *scale_b).  OUT: 0 f16,
-// 1 bf16, 2 f32.  A 64-wide (16-bit) or 128-wide (8-bit) contraction block is
-// one 128-byte swizzle row per tile row; four MMAs of K = 16 / 32 cover it.
+// IN: 0 f16, 1 bf16, 2 e4m3 (scaled by *scale_a * *scale_b), 3 f32 as a
+// 3xTF32 split (tmA/tmB hold the high parts, tmA2/tmB2 the low parts).  OUT:
+// 0 f16, 1 bf16, 2 f32.  A contraction block is one 128-byte swizzle row per
+// tile row (64, 128 or 32 elements); four MMAs of K = 16 / 32 / 8 cover it
+// (three per K step in the 3xTF32 mode).
+//
+// Accumulators: two 256-column TMEM buffers, so the epilogue of one tile
+// overlaps the MMAs of the next.  The 3xTF32 mode uses both halves of TMEM for
+// one tile instead: hi*hi accumulates in columns 0-255, lo*hi + hi*lo in
+// columns 256-511, and the epilogue adds the two (one rounding).  The tensor
+// core's accumulation rounding then hits the large sum once per K step rather
+// than three times, and the small sum's rounding is 2^-11 smaller.
 template <int IN, int OUT, bool A_MN, bool B_MN>
 __global__ void __launch_bounds__(THREADS, 1)
     tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                        const __grid_constant__ CUtensorMap tmA2, const __grid_constant__ CUtensorMap tmB2,
                         const Params p) {
-    constexpr int ES = IN == 2 ? 1 : 2;     // operand element size, bytes
+    constexpr int ES = IN == 2 ? 1 : (IN == 3 ? 4 : 2);  // operand element size, bytes
+    // the tf32 operands are always staged K-major (the split kernel transposes)
+    static_assert(IN != 3 || (!A_MN && !B_MN), "3xTF32 takes K-major operands only");
+    constexpr int P_STAGES = p_stages(IN);
+    constexpr int P_STAGE_BYTES = p_stage_bytes(IN);
     constexpr int BKE = 128 / ES;           // contraction elements per block
+    constexpr int NACC = IN == 3 ? 1 : 2;   // accumulator buffers in flight
     constexpr int MN_ATOMS = ES;            // 128-byte atoms across a 128-wide MN-major tile
     constexpr uint32_t MN_STEP = (32 / ES) * 128;  // one MMA's rows of an MN-major tile, bytes
     extern __shared__ uint8_t smem_raw[];
@@ -705,20 +730,25 @@ __global__ void __launch_bounds__(THREADS, 1)
                 if (!mbar_wait(empty_bar(s), ph ^ 1u, abort_flag, p, DEV_TIMEOUT_PRODUCER)) goto done_p;
                 const uint32_t fb_leader = mapa_rank(full_bar(s), 0);
                 if (crank == 0) mbar_expect_tx(full_bar(s), 2 * P_STAGE_BYTES);
-                const uint32_t a_dst = sbase + s * P_STAGE_BYTES;
-                const uint32_t b_dst = a_dst + P_A_BYTES;
                 const int kofs = kb * BKE;
-                if (A_MN) {
-                    for (int a = 0; a < MN_ATOMS; ++a)
-                        tma_load_2d_pair(a_dst + a * (BKE * 128), &tmA, arow + a * (128 / ES), kofs, fb_leader);
-                } else {
-                    tma_load_2d_pair(a_dst, &tmA, kofs, arow, fb_leader);
-                }
-                if (B_MN) {
-                    for (int b = 0; b < MN_ATOMS; ++b)
-                        tma_load_2d_pair(b_dst + b * (BKE * 128), &tmB, bcol + b * (128 / ES), kofs, fb_leader);
-                } else {
-                    tma_load_2d_pair(b_dst, &tmB, kofs, bcol, fb_leader);
+#pragma unroll
+                for (int part = 0; part < p_tiles(IN); ++part) {
+                    const uint32_t a_dst = sbase + s * P_STAGE_BYTES + part * (P_A_BYTES + P_B_BYTES);
+                    const uint32_t b_dst = a_dst + P_A_BYTES;
+                    const CUtensorMap* ma = part ? &tmA2 : &tmA;
+                    const CUtensorMap* mb = part ? &tmB2 : &tmB;
+                    if (A_MN) {
+                        for (int a = 0; a < MN_ATOMS; ++a)
+                            tma_load_2d_pair(a_dst + a * (BKE * 128), ma, arow + a * (128 / ES), kofs, fb_leader);
+                    } else {
+                        tma_load_2d_pair(a_dst, ma, kofs, arow, fb_leader);
+                    }
+                    if (B_MN) {
+                        for (int b = 0; b < MN_ATOMS; ++b)
+                            tma_load_2d_pair(b_dst + b * (BKE * 128), mb, bcol + b * (128 / ES), kofs, fb_leader);
+                    } else {
+                        tma_load_2d_pair(b_dst, mb, kofs, bcol, fb_leader);
+                    }
                 }
                 if (++s == P_STAGES) { s = 0; ph ^= 1u; }
             }
@@ -744,22 +774,32 @@ __global__ void __launch_bounds__(THREADS, 1)
                 tc_fence_after();
                 const uint32_t a_s = sbase + s * P_STAGE_BYTES;
                 const uint32_t b_s = a_s + P_A_BYTES;
-#pragma unroll
-                for (int kk = 0; kk < 4; ++kk) {
+                auto desc_a = [&](uint32_t base, int kk) {
                     // K-major: 32 bytes along the swizzled row per MMA;
                     // MN-major: one MMA's worth of 128-byte rows
-                    const uint64_t ad = A_MN ? smem_desc(a_s + kk * MN_STEP, BKE * 128, 1024)
-                                             : smem_desc(a_s + kk * 32, 16, 1024);
-                    const uint64_t bd = B_MN ? smem_desc(b_s + kk * MN_STEP, BKE * 128, 1024)
-                                             : smem_desc(b_s + kk * 32, 16, 1024);
-                    mma_pair<IN>(d_tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+                    return A_MN ? smem_desc(base + kk * MN_STEP, BKE * 128, 1024) : smem_desc(base + kk * 32, 16, 1024);
+                };
+                auto desc_b = [&](uint32_t base, int kk) {
+                    return B_MN ? smem_desc(base + kk * MN_STEP, BKE * 128, 1024) : smem_desc(base + kk * 32, 16, 1024);
+                };
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk) {
+                    if (IN == 3) {
+                        const uint32_t a_lo = a_s + (P_A_BYTES + P_B_BYTES), b_lo = a_lo + P_A_BYTES;
+                        const uint32_t acc = (kb | kk) != 0 ? 1u : 0u;
+                        mma_pair<IN>(d_tmem + BN, desc_a(a_lo, kk), desc_b(b_s, kk), idesc, acc);
+                        mma_pair<IN>(d_tmem + BN, desc_a(a_s, kk), desc_b(b_lo, kk), idesc, 1u);
+                        mma_pair<IN>(d_tmem, desc_a(a_s, kk), desc_b(b_s, kk), idesc, acc);
+                    } else {
+                        mma_pair<IN>(d_tmem, desc_a(a_s, kk), desc_b(b_s, kk), idesc, (kb | kk) != 0 ? 1u : 0u);
+                    }
                 }
                 mma_commit_pair_mc(empty_bar(s), 0x3);
                 if (++s == P_STAGES) { s = 0; ph ^= 1u; }
             }
             if (!ok) break;
             mma_commit_pair_mc(tfull_bar(ab), 0x3);
-            if (++ab == 2) { ab = 0; aph ^= 1u; }
+            if (++ab == NACC) { ab = 0; aph ^= 1u; }
         }
         mma_commit_pair(drain_bar);
         mbar_wait(drain_bar, 0, abort_flag, p, DEV_TIMEOUT_MMA);
@@ -788,19 +828,27 @@ __global__ void __launch_bounds__(THREADS, 1)
                 if (col0 + c0 >= p.cols) break;
                 uint32_t v[16];
                 tmem_ld16(tbase + c0, v);
+                uint32_t v2[16];
+                if (IN == 3) tmem_ld16(tbase + BN + c0, v2);
                 if (orow < 0) continue;
                 float f[16];
 #pragma unroll
                 for (int i = 0; i < 16; ++i) f[i] = __uint_as_float(v[i]);
+                if (IN == 3) {
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) f[i] = __fadd_rn(f[i], __uint_as_float(v2[i]));
+                }
                 if (IN == 2) {
 #pragma unroll
                     for (int i = 0; i < 16; ++i) f[i] = __fmul_rn(f[i], scale);
                 }
                 const int64_t cb = col0 + c0;
-                if (p.bias != nullptr) {  // the bias has the output's type (16-bit outputs only)
+                if (p.bias != nullptr) {  // the bias has the output's type
 #pragma unroll
                     for (int i = 0; i < 16; ++i)
-                        if (cb + i < p.cols) f[i] = __fadd_rn(f[i], OutT<OUT == 1 ? 1 : 0>::load(p.bias, cb + i));
+                        if (cb + i < p.cols)
+                            f[i] = __fadd_rn(f[i], OUT == 2 ? static_cast<const float*>(p.bias)[cb + i]
+                                                            : OutT<OUT == 1 ? 1 : 0>::load(p.bias, cb + i));
                 }
                 const bool full = cb + 16 <= p.cols;
                 if (OUT == 2) {
@@ -838,7 +886,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive_cluster(ab ? tempty_leader1 : tempty_leader0);
-            if (++ab == 2) { ab = 0; aph ^= 1u; }
+            if (++ab == NACC) { ab = 0; aph ^= 1u; }
         }
     }
 
@@ -912,8 +960,10 @@ cudaError_t launch(const LaunchCtx& c, const CUtensorMap& a, const CUtensorMap& 
 
 
 template <int IN, int OUT, bool A_MN, bool B_MN>
-cudaError_t launch_pair(const LaunchCtx& c, const CUtensorMap& a, const CUtensorMap& b, Params p) {
+cudaError_t launch_pair(const LaunchCtx& c, const CUtensorMap& a, const CUtensorMap& b, Params p,
+                        const CUtensorMap* a2 = nullptr, const CUtensorMap* b2 = nullptr) {
     auto kern = tc_gemm_pair_kernel<IN, OUT, A_MN, B_MN>;
+    constexpr int P_SMEM_BYTES = p_smem_bytes(IN);
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
     static int max_clusters = 0;
@@ -948,7 +998,7 @@ cudaError_t launch_pair(const LaunchCtx& c, const CUtensorMap& a, const CUtensor
     cfg.stream = c.stream;
     cfg.attrs = at;
     cfg.numAttrs = 1;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, a, b, p);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, a, b, a2 ? *a2 : a, b2 ? *b2 : b, p);
     if (e != cudaSuccess) return e;
     c.count();
     return cudaGetLastError();
@@ -1094,6 +1144,21 @@ cudaError_t fp8_pass_t(const LaunchCtx& c, int pass, void* out, const uint8_t* a
     return launch_pair<2, OUT, true, true>(c, ma, mb, p);
 }
 
+// 32-bit K-major tensor [outer][inner] with row stride ld elements (ld >= inner,
+// a multiple of 4), box {32, 128}, 128-byte swizzle.
+cudaError_t make_map32(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer, uint64_t ld) {
+    auto enc = encode_fn();
+    if (!enc) return cudaErrorNotSupported;
+    cuuint64_t dims[2] = {inner, outer};
+    cuuint64_t strides[1] = {ld * 4};
+    cuuint32_t box[2] = {32, 128};
+    cuuint32_t es[2] = {1, 1};
+    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(ptr), dims, strides, box, es,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 }  // namespace
 
 cudaError_t tc_forward(const LaunchCtx& c, bi_dtype dt, void* y, const void* x, const void* w,
@@ -1121,6 +1186,23 @@ cudaError_t tc_grouped_rows(const LaunchCtx& c, bi_dtype dt, int pass_dinput, vo
     return dt == BI_BF16
                ? grouped_rows_t<1>(c, dt, pass_dinput, out, a_padded, Mp_max, w, M, K, N, E, seg, perm)
                : grouped_rows_t<0>(c, dt, pass_dinput, out, a_padded, Mp_max, w, M, K, N, E, seg, perm);
+}
+
+cudaError_t tc_tf32x3_pass(const LaunchCtx& c, const float* a_hi, const float* a_lo, int64_t lda,
+                           const float* b_hi, const float* b_lo, int64_t ldb, float* out, int64_t ldo,
+                           const float* bias, int64_t rows, int64_t cols, int64_t depth) {
+    CUtensorMap ah, al, bh, bl;
+    cudaError_t e;
+    if ((e = make_map32(&ah, a_hi, depth, rows, lda)) != cudaSuccess) return e;
+    if ((e = make_map32(&al, a_lo, depth, rows, lda)) != cudaSuccess) return e;
+    if ((e = make_map32(&bh, b_hi, depth, cols, ldb)) != cudaSuccess) return e;
+    if ((e = make_map32(&bl, b_lo, depth, cols, ldb)) != cudaSuccess) return e;
+    Params p{};
+    p.out = out; p.ldo = ldo; p.rows = rows; p.cols = cols; p.bias = bias;
+    p.num_m = static_cast<int>((rows + BM - 1) / BM);
+    p.num_n = static_cast<int>((cols + BN - 1) / BN);
+    p.num_kb = static_cast<int>((depth + 31) / 32);
+    return launch_pair<3, 2, false, false>(c, ah, bh, p, &al, &bl);
 }
 
 cudaError_t tc_fp8_pass(const LaunchCtx& c, int pass, bi_dtype out_dt, void* out, const uint8_t* a,

@@ -52,10 +52,14 @@ def test_dispatch_is_shape_only(bi):
     # dW: both output dims
     assert bi.bi_dispatch_tier(P.BI_PASS_DW, "f16", 1, 1024, 48) == 0
     assert bi.bi_dispatch_tier(P.BI_PASS_DW, "bf16", 1, 4096, 12288) == 1
-    # f32 operands and tensor_cores=0 always take the scalar tier
+    # tensor_cores=0 always takes the scalar tier; f32 operands reach the tensor
+    # cores (3xTF32) on the dense passes only, with rows in 16-byte units
     for p in range(6):
-        assert bi.bi_dispatch_tier(p, "f32", 1, 4096, 4096) == 0
         assert bi.bi_dispatch_tier(p, "bf16", 0, 4096, 4096) == 0
+        assert bi.bi_dispatch_tier(p, "f32", 0, 4096, 4096) == 0
+        assert bi.bi_dispatch_tier(p, "f32", 1, 4096, 4096) == (1 if p <= P.BI_PASS_DW else 0)
+    assert bi.bi_dispatch_tier(P.BI_PASS_FORWARD, "f32", 1, 1002, 1000) == 0
+    assert bi.bi_dispatch_tier(P.BI_PASS_FORWARD, "f32", 1, 1004, 1000) == 1
     # rows that are not whole 16-byte units cannot be fed by TMA
     assert bi.bi_dispatch_tier(P.BI_PASS_FORWARD, "bf16", 1, 1001, 1000) == 0
     assert bi.bi_dispatch_tier(P.BI_PASS_FORWARD, "bf16", 1, 1000, 1000) == 1

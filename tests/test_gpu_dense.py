@@ -78,8 +78,8 @@ def test_scalar_tier_bit_exact(eng, case):
 @pytest.mark.parametrize("case", SCALAR_CASES, ids=lambda c: c[0])
 def test_tc_flag_on_scalar_shapes_is_scalar(eng, case):
     """With tensor_cores=1, passes whose shape the dispatcher keeps on the scalar
-    tier (f32 operands, an output dim < 64, rows not multiples of 8) give the
-    scalar results bit for bit."""
+    tier (an output dim < 64, rows not whole 16-byte units) give the scalar
+    results bit for bit."""
     _, dtype, m, k, n, spec = case
     x, w, dy, b = synth.dense_inputs(m, k, n, dtype, x=spec, w=spec, dy=spec, b=("normal", 0.1))
     a = run_dense(eng, x, w, dy, b, m, k, n, dtype, tc=0)
@@ -103,6 +103,9 @@ def test_scalar_gpt2_up_sampled(eng):
 
 
 TC_CASES = [
+    ("ragged_f32", "f32", 300, 200, 520),       # 3xTF32
+    ("multi_tile_f32", "f32", 520, 1004, 776),  # 3xTF32, long contraction
+    ("odd_m_f32", "f32", 301, 260, 132),        # 3xTF32: M not a multiple of 4, N not of 8
     ("ragged_bf16", "bf16", 300, 200, 520),
     ("multi_tile_bf16", "bf16", 520, 264, 776),
     ("ragged_1000_f16", "f16", 1000, 1000, 1000),
@@ -119,7 +122,8 @@ def test_tc_tier_within_tolerance(eng, case):
     for p in (bi.BI_PASS_FORWARD, bi.BI_PASS_DX, bi.BI_PASS_DW):
         assert bi.bi_dispatch_tier(p, dtype, 1, k, n) == (0 if (p != bi.BI_PASS_FORWARD and k < 64) else 1)
     got = run_dense(eng, x, w, dy, b, m, k, n, dtype, tc=1)
-    got_r = run_dense(eng, x, w, dy, b, m, k, n, dtype, tc=1, dw_f32=False, passes=("dw",))
+    got_r = got if dtype == "f32" else run_dense(eng, x, w, dy, b, m, k, n, dtype, tc=1, dw_f32=False,
+                                                  passes=("dw",))
     xn, wn, dyn, bn = np_in(x, w, dy, b)
     x64, w64, dy64, b64 = (f64(a, dtype) for a in (xn, wn, dyn, bn))
     r = oracle.forward(xn, wn, bn, m, k, n, dtype, out_f32=True)
@@ -136,7 +140,7 @@ def test_tc_tier_within_tolerance(eng, case):
     assert ok, ("dw rounded", st)
 
 
-@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+@pytest.mark.parametrize("dtype", ["f32", "bf16", "f16"])
 def test_tc_tier_exact_on_small_integers(eng, dtype):
     """Integer operands in [-8, 8] (f16: [-16, 16]) make every partial sum exact in
     f32, so the tensor-core result must equal the oracle bit for bit, bias and
@@ -148,7 +152,8 @@ def test_tc_tier_exact_on_small_integers(eng, dtype):
     dy = synth.small_ints((m, n), -hi, hi, dtype, 13)
     b = (synth.small_ints((n,), -128, 127, "f32", 14) / 2).to(synth.TORCH_DTYPES[dtype])
     got = run_dense(eng, x, w, dy, b, m, k, n, dtype, tc=1)
-    got_r = run_dense(eng, x, w, dy, b, m, k, n, dtype, tc=1, dw_f32=False, passes=("dw",))
+    got_r = got if dtype == "f32" else run_dense(eng, x, w, dy, b, m, k, n, dtype, tc=1, dw_f32=False,
+                                                  passes=("dw",))
     xn, wn, dyn, bn = np_in(x, w, dy, b)
     assert np.array_equal(got["y"], oracle.forward(xn, wn, bn, m, k, n, dtype))
     assert np.array_equal(got["dx"], oracle.backward_dx(dyn, wn, m, k, n, dtype))
@@ -198,6 +203,54 @@ def test_tc_7b_layer_sampled(eng, proj):
     assert ok, st
 
 
+def test_tc_f32_o_proj_sampled(eng):
+    """3xTF32 at the f32 o-projection size 8192 x 4096 x 4096 (the bench's f32
+    figure), sampled rows of Y / dX and columns of dW against the oracle."""
+    m, k, n, dtype = synth.SEVEN_B_M, 4096, 4096, "f32"
+    x, w, dy, b = synth.dense_inputs(m, k, n, dtype, b=("normal", 0.1))
+    got = run_dense(eng, x, w, dy, b, m, k, n, dtype, tc=1)
+    xn, wn, dyn, bn = np_in(x, w, dy, b)
+    x64, w64, dy64, b64 = (f64(a, dtype) for a in (xn, wn, dyn, bn))
+    rows = sample_rows(m, 6, seed=4)
+    cols = sample_rows(n, 3, seed=5)
+    r = oracle.forward(xn, wn, bn, m, k, n, dtype, rows=rows)
+    ok, st = check_tc(got["y"][rows], r, abs_sum(x64[rows], w64, b64), dtype)
+    assert ok, st
+    r = oracle.backward_dx(dyn, wn, m, k, n, dtype, rows=rows)
+    ok, st = check_tc(got["dx"][rows], r, abs_sum(dy64[rows], w64.T), dtype)
+    assert ok, st
+    r = oracle.backward_dw(xn, dyn, m, k, n, dtype, dw_f32=True, cols=cols)
+    ok, st = check_tc(got["dw"][:, cols], r, abs_sum(x64.T, dy64[:, cols]), dtype)
+    assert ok, st
+
+
+@pytest.mark.parametrize("m,k,n", [(256, 13288, 264),   # forward: pieces 4096 x 3 + 1000
+                                   (200, 136, 9000),    # dX: pieces 4096 x 2 + 808
+                                   (8201, 132, 136)])   # dW: pieces 4096 x 2 + 9, padded ld
+def test_tc_f32_long_contractions(eng, m, k, n):
+    """3xTF32 over contractions longer than one 4096-element piece: every pass
+    stays within the tolerance, and rows of Y / dX still do not depend on M."""
+    dtype = "f32"
+    x, w, dy, b = synth.dense_inputs(m, k, n, dtype, w=("normal", 1.0), b=("normal", 0.1))
+    got = run_dense(eng, x, w, dy, b, m, k, n, dtype, tc=1)
+    xn, wn, dyn, bn = np_in(x, w, dy, b)
+    x64, w64, dy64, b64 = (f64(a, dtype) for a in (xn, wn, dyn, bn))
+    rows = sample_rows(m, min(m, 24), seed=6)
+    cols = sample_rows(n, min(n, 8), seed=7)
+    r = oracle.forward(xn, wn, bn, m, k, n, dtype, rows=rows)
+    ok, st = check_tc(got["y"][rows], r, abs_sum(x64[rows], w64, b64), dtype)
+    assert ok, ("y", st)
+    r = oracle.backward_dx(dyn, wn, m, k, n, dtype, rows=rows)
+    ok, st = check_tc(got["dx"][rows], r, abs_sum(dy64[rows], w64.T), dtype)
+    assert ok, ("dx", st)
+    r = oracle.backward_dw(xn, dyn, m, k, n, dtype, dw_f32=True, cols=cols)
+    ok, st = check_tc(got["dw"][:, cols], r, abs_sum(x64.T, dy64[:, cols]), dtype)
+    assert ok, ("dw", st)
+    mp = 3
+    part = run_dense(eng, x[:mp].contiguous(), w, dy[:mp].contiguous(), b, mp, k, n, dtype, tc=1, passes=("y", "dx"))
+    assert np.array_equal(part["y"], got["y"][:mp]) and np.array_equal(part["dx"], got["dx"][:mp])
+
+
 @pytest.mark.parametrize("tc", [0, 1])
 def test_ten_runs_bit_identical(eng, tc):
     m, k, n, dtype = 1024, 768, 1536, "bf16"
@@ -222,7 +275,7 @@ def test_batch_invariance_tc_7b_qkv(eng):
         assert np.array_equal(part["dx"], full["dx"][:mp]), mp
 
 
-@pytest.mark.parametrize("dtype,tc", [("f32", 0), ("bf16", 0), ("f16", 1), ("bf16", 1)])
+@pytest.mark.parametrize("dtype,tc", [("f32", 0), ("bf16", 0), ("f16", 1), ("bf16", 1), ("f32", 1)])
 def test_batch_invariance_prefixes(eng, dtype, tc):
     m, k, n = 64, 256, 512
     x, w, dy, b = synth.dense_inputs(m, k, n, dtype, w=("normal", 1.0))
