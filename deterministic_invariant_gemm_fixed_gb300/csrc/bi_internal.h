@@ -108,16 +108,14 @@ cudaError_t tc_fp8_pass(const LaunchCtx& c, int pass, bi_dtype out_dt, void* out
 // multiple of 4; the columns past rows are not written).
 cudaError_t tf32_split(const LaunchCtx& c, const float* x, float* hi, float* lo, int64_t rows, int64_t cols,
                        bool transpose, int64_t ld);
-// Contractions longer than this many elements run as pieces of this length into
-// f32 partials, summed in piece order by tf32_sum_partials: the tensor core's
-// accumulation error grows with the contraction length, and a fixed piece
-// length (independent of the batch) bounds it.
+// Contractions longer than this many elements run as pieces of this length, one
+// launch each, every launch after the first adding its result to the output in
+// piece order: the tensor core's accumulation error grows with the contraction
+// length, and a fixed piece length (independent of the batch) bounds it.
 constexpr int64_t TF32X3_PIECE = 4096;
-// out[r * ldo + c] = sum over j < J of partials[j][r][c] (left to right), + bias[c]
-cudaError_t tf32_sum_partials(const LaunchCtx& c, const float* partials, int64_t J, int64_t rows, int64_t cols,
-                              const float* bias, float* out, int64_t ldo);
-// out[r][c] (+ bias[c]) = sum over d of a[r][d] * b[c][d], both operands K-major
-// (a: rows x depth, leading dim lda; b: cols x depth, ldb); f32 out, leading dim ldo.
+// out[r][c] = sum over pieces (in order) of the piece's sum over d of
+// a[r][d] * b[c][d], + bias[c]; both operands K-major (a: rows x depth, leading
+// dim lda; b: cols x depth, ldb); f32 out, leading dim ldo.
 cudaError_t tc_tf32x3_pass(const LaunchCtx& c, const float* a_hi, const float* a_lo, int64_t lda,
                            const float* b_hi, const float* b_lo, int64_t ldb, float* out, int64_t ldo,
                            const float* bias, int64_t rows, int64_t cols, int64_t depth);

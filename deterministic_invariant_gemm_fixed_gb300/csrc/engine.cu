@@ -95,35 +95,19 @@ struct Tf32Operand {
 bi_status tf32x3(bi_engine eng, const bi::LaunchCtx& c, const Tf32Operand& a, const Tf32Operand& b, void* out,
                  int64_t ldo, const void* bias, int64_t rows, int64_t cols, int64_t depth, const char* name) {
     const int64_t a_b = a.bytes(), b_b = b.bytes();
-    // contractions longer than one piece: pieces into f32 partials, then their sum
-    const int64_t J = (depth + bi::TF32X3_PIECE - 1) / bi::TF32X3_PIECE;
-    const int64_t p_b = J > 1 ? (J * rows * cols * 4 + 255) / 256 * 256 : 0;
-    Scratch sc(eng, c.stream, static_cast<size_t>(2 * (a_b + b_b) + p_b));
+    Scratch sc(eng, c.stream, static_cast<size_t>(2 * (a_b + b_b)));
     if (sc.err != cudaSuccess) return cuda_fail(eng, sc.err, "3xTF32 scratch");
     uint8_t* base = static_cast<uint8_t*>(sc.ptr);
     float* ah = reinterpret_cast<float*>(base);
     float* al = reinterpret_cast<float*>(base + a_b);
     float* bh = reinterpret_cast<float*>(base + 2 * a_b);
     float* bl = reinterpret_cast<float*>(base + 2 * a_b + b_b);
-    float* part = reinterpret_cast<float*>(base + 2 * (a_b + b_b));
     cudaError_t e = bi::tf32_split(c, static_cast<const float*>(a.src), ah, al, a.rows, a.cols, a.transpose, a.ld());
     if (e == cudaSuccess)
         e = bi::tf32_split(c, static_cast<const float*>(b.src), bh, bl, b.rows, b.cols, b.transpose, b.ld());
-    if (J == 1) {
-        if (e == cudaSuccess)
-            e = bi::tc_tf32x3_pass(c, ah, al, a.ld(), bh, bl, b.ld(), static_cast<float*>(out), ldo,
-                                   static_cast<const float*>(bias), rows, cols, depth);
-        return e == cudaSuccess ? BI_OK : cuda_fail(eng, e, name);
-    }
-    for (int64_t j = 0; j < J && e == cudaSuccess; ++j) {
-        const int64_t d0 = j * bi::TF32X3_PIECE;  // a multiple of 4 elements: 16-byte aligned bases
-        const int64_t len = std::min(bi::TF32X3_PIECE, depth - d0);
-        e = bi::tc_tf32x3_pass(c, ah + d0, al + d0, a.ld(), bh + d0, bl + d0, b.ld(), part + j * rows * cols, cols,
-                               nullptr, rows, cols, len);
-    }
     if (e == cudaSuccess)
-        e = bi::tf32_sum_partials(c, part, J, rows, cols, static_cast<const float*>(bias), static_cast<float*>(out),
-                                  ldo);
+        e = bi::tc_tf32x3_pass(c, ah, al, a.ld(), bh, bl, b.ld(), static_cast<float*>(out), ldo,
+                               static_cast<const float*>(bias), rows, cols, depth);
     return e == cudaSuccess ? BI_OK : cuda_fail(eng, e, name);
 }
 

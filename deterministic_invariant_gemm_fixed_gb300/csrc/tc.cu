@@ -60,6 +60,7 @@ struct Params {
     int E;
     const float* scale_a;    // FP8: per-tensor scales applied to the f32 product
     const float* scale_b;
+    int accum_out;           // 3xTF32 contraction piece after the first: out += result
     int* status;
     unsigned long long wait_limit;
 };
@@ -837,6 +838,12 @@ __global__ void __launch_bounds__(THREADS, 1)
                 if (IN == 3) {
 #pragma unroll
                     for (int i = 0; i < 16; ++i) f[i] = __fadd_rn(f[i], __uint_as_float(v2[i]));
+                    if (p.accum_out) {  // earlier pieces' sum, left by the previous launch
+                        const float* prev = static_cast<const float*>(p.out) + orow * p.ldo + col0 + c0;
+#pragma unroll
+                        for (int i = 0; i < 16; ++i)
+                            if (col0 + c0 + i < p.cols) f[i] = __fadd_rn(prev[i], f[i]);
+                    }
                 }
                 if (IN == 2) {
 #pragma unroll
@@ -1191,18 +1198,26 @@ cudaError_t tc_grouped_rows(const LaunchCtx& c, bi_dtype dt, int pass_dinput, vo
 cudaError_t tc_tf32x3_pass(const LaunchCtx& c, const float* a_hi, const float* a_lo, int64_t lda,
                            const float* b_hi, const float* b_lo, int64_t ldb, float* out, int64_t ldo,
                            const float* bias, int64_t rows, int64_t cols, int64_t depth) {
-    CUtensorMap ah, al, bh, bl;
-    cudaError_t e;
-    if ((e = make_map32(&ah, a_hi, depth, rows, lda)) != cudaSuccess) return e;
-    if ((e = make_map32(&al, a_lo, depth, rows, lda)) != cudaSuccess) return e;
-    if ((e = make_map32(&bh, b_hi, depth, cols, ldb)) != cudaSuccess) return e;
-    if ((e = make_map32(&bl, b_lo, depth, cols, ldb)) != cudaSuccess) return e;
-    Params p{};
-    p.out = out; p.ldo = ldo; p.rows = rows; p.cols = cols; p.bias = bias;
-    p.num_m = static_cast<int>((rows + BM - 1) / BM);
-    p.num_n = static_cast<int>((cols + BN - 1) / BN);
-    p.num_kb = static_cast<int>((depth + 31) / 32);
-    return launch_pair<3, 2, false, false>(c, ah, bh, p, &al, &bl);
+    // one launch per contraction piece: the first writes out, each later one adds
+    // its result to out (in piece order), the last one adds the bias
+    for (int64_t d0 = 0; d0 < depth; d0 += TF32X3_PIECE) {  // d0 % 4 == 0: 16-byte aligned bases
+        const int64_t len = lmin(TF32X3_PIECE, depth - d0);
+        CUtensorMap ah, al, bh, bl;
+        cudaError_t e;
+        if ((e = make_map32(&ah, a_hi + d0, len, rows, lda)) != cudaSuccess) return e;
+        if ((e = make_map32(&al, a_lo + d0, len, rows, lda)) != cudaSuccess) return e;
+        if ((e = make_map32(&bh, b_hi + d0, len, cols, ldb)) != cudaSuccess) return e;
+        if ((e = make_map32(&bl, b_lo + d0, len, cols, ldb)) != cudaSuccess) return e;
+        Params p{};
+        p.out = out; p.ldo = ldo; p.rows = rows; p.cols = cols;
+        p.bias = d0 + len == depth ? bias : nullptr;
+        p.accum_out = d0 > 0 ? 1 : 0;
+        p.num_m = static_cast<int>((rows + BM - 1) / BM);
+        p.num_n = static_cast<int>((cols + BN - 1) / BN);
+        p.num_kb = static_cast<int>((len + 31) / 32);
+        if ((e = launch_pair<3, 2, false, false>(c, ah, bh, p, &al, &bl)) != cudaSuccess) return e;
+    }
+    return cudaSuccess;
 }
 
 cudaError_t tc_fp8_pass(const LaunchCtx& c, int pass, bi_dtype out_dt, void* out, const uint8_t* a,

@@ -68,34 +68,7 @@ __global__ void __launch_bounds__(256) tf32_split_t_kernel(const float* __restri
     }
 }
 
-__global__ void tf32_sum_partials_kernel(const float* __restrict__ partials, int64_t J, int64_t rows,
-                                         int64_t cols, const float* __restrict__ bias, float* __restrict__ out,
-                                         int64_t ldo) {
-    const int64_t count = rows * cols;
-    for (int64_t e = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; e < count;
-         e += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-        float v = partials[e];
-        for (int64_t j = 1; j < J; ++j) v = __fadd_rn(v, partials[j * count + e]);
-        const int64_t col = e % cols;
-        if (bias != nullptr) v = __fadd_rn(v, bias[col]);
-        out[(e / cols) * ldo + col] = v;
-    }
-}
-
 }  // namespace
-
-cudaError_t tf32_sum_partials(const LaunchCtx& c, const float* partials, int64_t J, int64_t rows, int64_t cols,
-                              const float* bias, float* out, int64_t ldo) {
-    const int64_t count = rows * cols;
-    if (count == 0) return cudaSuccess;
-    int64_t blocks = (count + 255) / 256;
-    const int64_t cap = static_cast<int64_t>(c.sm_count) * 16;
-    if (blocks > cap) blocks = cap;
-    tf32_sum_partials_kernel<<<static_cast<unsigned>(blocks), 256, 0, c.stream>>>(partials, J, rows, cols, bias,
-                                                                                 out, ldo);
-    c.count();
-    return cudaGetLastError();
-}
 
 cudaError_t tf32_split(const LaunchCtx& c, const float* x, float* hi, float* lo, int64_t rows, int64_t cols,
                        bool transpose, int64_t ld) {

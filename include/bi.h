@@ -20,7 +20,7 @@
  * ------------------------------------------------------------------------
  * Arithmetic contract
  * ------------------------------------------------------------------------
- * Scalar tier (tensor_cores = 0, or any f32 call, or a shape below the
+ * Scalar tier (tensor_cores = 0, a grouped f32 call, or a shape below the
  * tensor-core threshold): every output is one chain
  *      acc = +0.0f;  for i ascending: acc = fmaf(up(a_i), up(b_i), acc)
  * over the contracted index, where up() is the exact widening to f32.  The
@@ -42,6 +42,17 @@
  * scalar tier (they are not bit-equal to it).  dW and grouped dweights chain
  * the row blocks in ascending order inside the accumulator (the degenerate,
  * single-chunk case of the fixed tree).
+ *
+ * f32 operands on the tensor-core tier (dense passes, K and N multiples of 4)
+ * run as 3xTF32: each operand x is split into hi = tf32(x) and
+ * lo = tf32(x - hi) (round to nearest, ties away), and each product is taken
+ * as hi*hi + (lo*hi + hi*lo), the two sums in separate f32 accumulators added
+ * once at the end.  The contraction is cut into fixed pieces of 4096 elements
+ * counted from 0 (a length independent of M); each piece's f32 result is added
+ * to the sum of the pieces before it, in piece order, then the bias.  Same
+ * guarantees as above: run-to-run identical, M-invariant rows, within the
+ * published f32 tolerance of the scalar tier.  Scratch for the parts comes
+ * from the engine's stream-ordered pool.
  *
  * Dispatch looks only at (pass, dtype, tensor_cores, K, N): never at M.
  *
@@ -262,7 +273,9 @@ bi_status bi_grouped_forward_noalloc(void* y, const void* x, const void* w,
 /* The dispatcher's choice for a call: 0 = scalar tier, 1 = tensor-core tier.
  * A pure function of its arguments (M is not one of them).  Source:
  * sgemm-bi 0.1.1.post2, "Determinism contracts" (shapes with an output
- * dimension below 64 go to the scalar tier, decided from the shape alone). */
+ * dimension below 64 go to the scalar tier, decided from the shape alone).
+ * Tensor cores take bf16/f16 with K, N multiples of 8, and f32 (3xTF32, the
+ * dense passes only) with K, N multiples of 4; everything else is scalar. */
 int bi_dispatch_tier(int pass, bi_dtype dtype, int tensor_cores, int64_t k, int64_t n);
 
 /* Number of kernels this engine has launched since it was created. */
