@@ -62,9 +62,15 @@ cudaError_t bias_grad(const LaunchCtx& c, bi_dtype dt, void* out, int out_f32, c
                       int64_t M, int64_t N, float* partials);
 
 // ---- grouping (grouped.cu) ------------------------------------------------
-// Segment table layout (u32): [0, E+2) offsets of groups 0..E (group E =
-// padding) plus M; [E+2, 2E+3) padded starts of experts 0..E (rows rounded up
-// to 128 per expert); then tc_rows (1 entry).
+// The tensor-core grouped passes cut each expert's sorted rows into tiles of
+// GROUPED_TILE_ROWS rows, and read the expert's partial last block of
+// GROUPED_TAIL_ROWS rows (dweights) from a zero-padded tail buffer.
+constexpr int GROUPED_TILE_ROWS = 256;
+constexpr int GROUPED_TAIL_ROWS = 64;
+// Segment table layout (u32): [0, E+2) sorted offsets of groups 0..E (group E
+// = padding) plus M; [E+2, 2E+3) first tile of experts 0..E, a prefix sum of
+// ceil(count / GROUPED_TILE_ROWS) (entry E = all tiles); then the same total
+// once more.
 inline int64_t seg_table_len(int64_t E) { return 2 * E + 4; }
 int64_t segment_scratch_bytes(int64_t M, int64_t E);
 cudaError_t segment(const LaunchCtx& c, const uint32_t* ids, int64_t M, int64_t E, uint32_t* seg,
@@ -74,9 +80,14 @@ cudaError_t segment(const LaunchCtx& c, const uint32_t* ids, int64_t M, int64_t 
 // sequence from 0 to at most M; a clamp records DEV_BAD_OFFSETS.
 cudaError_t segment_from_offsets(const LaunchCtx& c, const uint32_t* offsets, int64_t M, int64_t E,
                                  uint32_t* seg, uint32_t* perm);
-// Copy rows of src [M, L] into dst [Mp, L] in padded expert order (zeros in the gaps).
-cudaError_t gather_padded(const LaunchCtx& c, const void* src, int64_t M, int64_t L, int64_t E,
-                          const uint32_t* seg, const uint32_t* perm, void* dst, int64_t Mp_max);
+// 16-bit rows of length L (a multiple of 8).  gather_sorted: dst[s] = src[perm[s]]
+// for the sorted rows of experts 0..E-1 (s < offsets[E]).  build_tails: for each
+// expert g, rows [g*64, g*64+64) of dst hold its sorted rows from the last
+// multiple of 64 on, then zeros.
+cudaError_t gather_sorted(const LaunchCtx& c, const void* src, int64_t M, int64_t L, int64_t E,
+                          const uint32_t* seg, const uint32_t* perm, void* dst);
+cudaError_t build_tails(const LaunchCtx& c, const void* src, int64_t L, int64_t E, const uint32_t* seg,
+                        const uint32_t* perm, void* dst);
 // Zero the rows of out [M, C] (element size esize) whose ids are padding.
 cudaError_t zero_padding_rows(const LaunchCtx& c, void* out, int64_t C, int esize, int64_t E,
                               const uint32_t* seg, const uint32_t* perm);
@@ -89,14 +100,15 @@ cudaError_t tc_dx(const LaunchCtx& c, bi_dtype dt, void* dx, const void* dy, con
                   int64_t M, int64_t K, int64_t N);
 cudaError_t tc_dw(const LaunchCtx& c, bi_dtype dt, void* dw, int dw_f32, const void* x,
                   const void* dy, int64_t M, int64_t K, int64_t N);
-// Grouped, on padded gathered operands (rows of expert g start at pstart[g]).
-cudaError_t tc_grouped_rows(const LaunchCtx& c, bi_dtype dt, int pass_dinput, void* out,
-                            const void* a_padded, int64_t Mp_max, const void* w, int64_t M,
-                            int64_t K, int64_t N, int64_t E, const uint32_t* seg,
+// Grouped forward / dinput on a row-sorted operand a_sorted [M, K or N] (row
+// s = original row perm[s]); output row perm[s] for every sorted row of an expert.
+cudaError_t tc_grouped_rows(const LaunchCtx& c, bi_dtype dt, int pass_dinput, void* out, const void* a_sorted,
+                            const void* w, int64_t M, int64_t K, int64_t N, int64_t E, const uint32_t* seg,
                             const uint32_t* perm);
-cudaError_t tc_grouped_dw(const LaunchCtx& c, bi_dtype dt, float* dw, const void* dy_padded,
-                          const void* x_padded, int64_t Mp_max, int64_t M, int64_t K, int64_t N,
-                          int64_t E, const uint32_t* seg);
+// Grouped dweights [E,N,K] f32 from row-sorted dY and X plus their tail buffers.
+cudaError_t tc_grouped_dw(const LaunchCtx& c, bi_dtype dt, float* dw, const void* dy_sorted, const void* x_sorted,
+                          const void* dy_tail, const void* x_tail, int64_t M, int64_t K, int64_t N, int64_t E,
+                          const uint32_t* seg);
 // FP8 e4m3 scaled matmuls on the CTA pair (pass 0 forward, 1 dX, 2 dW): the
 // f32 product is multiplied by *sa * *sb, then (+ bias), then rounded to out_dt.
 cudaError_t tc_fp8_pass(const LaunchCtx& c, int pass, bi_dtype out_dt, void* out, const uint8_t* a,
@@ -122,8 +134,6 @@ cudaError_t tc_tf32x3_pass(const LaunchCtx& c, const float* a_hi, const float* a
 // FP8 quantize (fp8.cu): q = e4m3(up(src) * *scale_inv), amax = max |up(src)|.
 cudaError_t fp8_quantize(const LaunchCtx& c, bi_dtype dt, uint8_t* q, float* amax, const void* src,
                          const float* scale_inv, int64_t count);
-// Upper bound on padded rows for M rows over E experts (multiples of 128 per expert).
-inline int64_t padded_rows_max(int64_t M, int64_t E) { return ((M + 127) / 128) * 128 + E * 128; }
 
 }  // namespace bi
 

@@ -427,25 +427,29 @@ bi_status grouped_forward_impl(bi_engine eng, void* y, const void* x, const void
     if (!g.ok) return fail(eng, BI_ERR_CUDA, "cudaSetDevice failed");
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const bi::LaunchCtx c = ctx(eng, stream);
-    // scratch: seg table | perm | histogram | (padded X)
+    // scratch: seg table | perm | histogram | (row-sorted X).  Caller-grouped rows
+    // (offsets) are already sorted: the tensor cores read X in place.
+    const bool sorted_in_place = src.ids == nullptr;
     const int64_t seg_b = round256(bi::seg_table_len(e) * 4);
     const int64_t perm_b = round256(m * 4);
     const int64_t hist_b = src.ids ? round256(bi::segment_scratch_bytes(m, e)) : 0;
-    const int64_t mp = bi::padded_rows_max(m, e);
-    const int64_t pad_b = tier ? mp * k * 2 : 0;
-    Scratch sc(eng, s, static_cast<size_t>(seg_b + perm_b + hist_b + pad_b));
+    const int64_t xs_b = tier && !sorted_in_place ? round256(m * k * 2) : 0;
+    Scratch sc(eng, s, static_cast<size_t>(seg_b + perm_b + hist_b + xs_b));
     if (sc.err != cudaSuccess) return cuda_fail(eng, sc.err, "grouped scratch");
     uint8_t* base = static_cast<uint8_t*>(sc.ptr);
     uint32_t* seg = reinterpret_cast<uint32_t*>(base);
     uint32_t* perm = reinterpret_cast<uint32_t*>(base + seg_b);
     void* hist = base + seg_b + perm_b;
-    void* xpad = base + seg_b + perm_b + hist_b;
+    void* xs = base + seg_b + perm_b + hist_b;
     cudaError_t err = build_grouping(c, src, m, e, seg, perm, hist);
     if (err == cudaSuccess) {
         if (tier) {
-            err = bi::gather_padded(c, x, m, k, e, seg, perm, xpad, mp);
-            if (err == cudaSuccess)
-                err = bi::tc_grouped_rows(c, dtype, 0, y, xpad, mp, w, m, k, n, e, seg, perm);
+            const void* a = x;
+            if (!sorted_in_place) {
+                err = bi::gather_sorted(c, x, m, k, e, seg, perm, xs);
+                a = xs;
+            }
+            if (err == cudaSuccess) err = bi::tc_grouped_rows(c, dtype, 0, y, a, w, m, k, n, e, seg, perm);
         } else {
             err = bi::scalar_rows_grouped(c, dtype, y, x, w, m, k, n, e, 1, seg, perm);
         }
@@ -469,36 +473,60 @@ bi_status grouped_backward_impl(bi_engine eng, void* dx, float* dw, const void* 
         (!aligned16(x) || !aligned16(w) || !aligned16(dy) || !aligned16(dw) || (dx && !aligned16(dx))))
         return fail(eng, BI_ERR_MISALIGNED, "tensor-core tier needs 16-byte aligned operands");
     const bi::LaunchCtx c = ctx(eng, stream);
+    // scratch: seg table | perm | histogram | row-sorted dY, X (unless the caller
+    // grouped the rows) | dY, X tail blocks (tensor-core dweights) | chunk partials
+    // (scalar dweights)
+    const bool sorted_in_place = src.ids == nullptr;
     const int64_t seg_b = round256(bi::seg_table_len(e) * 4);
     const int64_t perm_b = round256(m * 4);
     const int64_t hist_b = src.ids ? round256(bi::segment_scratch_bytes(m, e)) : 0;
-    const int64_t mp = bi::padded_rows_max(m, e);
-    const bool need_dy_pad = tier_dx || tier_dw;
-    const int64_t dypad_b = need_dy_pad ? round256(mp * n * 2) : 0;
-    const int64_t xpad_b = tier_dw ? round256(mp * k * 2) : 0;
+    const bool need_dys = (tier_dx || tier_dw) && !sorted_in_place;
+    const int64_t dys_b = need_dys ? round256(m * n * 2) : 0;
+    const int64_t xs_b = tier_dw && !sorted_in_place ? round256(m * k * 2) : 0;
+    const int64_t tails_b = tier_dw ? round256(e * bi::GROUPED_TAIL_ROWS * n * 2) +
+                                          round256(e * bi::GROUPED_TAIL_ROWS * k * 2)
+                                    : 0;
     const int64_t max_chunks = (m + BI_DW_CHUNK - 1) / BI_DW_CHUNK + e;
     const int64_t part_b = tier_dw ? 0 : max_chunks * n * k * 4;
-    Scratch sc(eng, s, static_cast<size_t>(seg_b + perm_b + hist_b + dypad_b + xpad_b + part_b));
+    Scratch sc(eng, s, static_cast<size_t>(seg_b + perm_b + hist_b + dys_b + xs_b + tails_b + part_b));
     if (sc.err != cudaSuccess) return cuda_fail(eng, sc.err, "grouped scratch");
     uint8_t* base = static_cast<uint8_t*>(sc.ptr);
     uint32_t* seg = reinterpret_cast<uint32_t*>(base);
     uint32_t* perm = reinterpret_cast<uint32_t*>(base + seg_b);
-    void* hist = base + seg_b + perm_b;
-    void* dypad = base + seg_b + perm_b + hist_b;
-    void* xpad = static_cast<uint8_t*>(dypad) + dypad_b;
-    float* part = reinterpret_cast<float*>(static_cast<uint8_t*>(xpad) + xpad_b);
+    uint8_t* q = base + seg_b + perm_b;
+    void* hist = q;
+    q += hist_b;
+    void* dys = q;
+    q += dys_b;
+    void* xs = q;
+    q += xs_b;
+    void* dyt = q;
+    void* xt = q + (tier_dw ? round256(e * bi::GROUPED_TAIL_ROWS * n * 2) : 0);
+    q += tails_b;
+    float* part = reinterpret_cast<float*>(q);
     cudaError_t err = build_grouping(c, src, m, e, seg, perm, hist);
-    if (err == cudaSuccess && need_dy_pad) err = bi::gather_padded(c, dy, m, n, e, seg, perm, dypad, mp);
+    const void* dy_sorted = dy;
+    const void* x_sorted = x;
+    if (err == cudaSuccess && need_dys) {
+        err = bi::gather_sorted(c, dy, m, n, e, seg, perm, dys);
+        dy_sorted = dys;
+    }
     if (err == cudaSuccess && dx) {
-        err = tier_dx ? bi::tc_grouped_rows(c, dtype, 1, dx, dypad, mp, w, m, k, n, e, seg, perm)
+        err = tier_dx ? bi::tc_grouped_rows(c, dtype, 1, dx, dy_sorted, w, m, k, n, e, seg, perm)
                       : bi::scalar_rows_grouped(c, dtype, dx, dy, w, m, n, k, e, 0, seg, perm);
         if (err == cudaSuccess)
             err = bi::zero_padding_rows(c, dx, k, static_cast<int>(dsize(dtype)), e, seg, perm);
     }
     if (err == cudaSuccess) {
         if (tier_dw) {
-            err = bi::gather_padded(c, x, m, k, e, seg, perm, xpad, mp);
-            if (err == cudaSuccess) err = bi::tc_grouped_dw(c, dtype, dw, dypad, xpad, mp, m, k, n, e, seg);
+            if (!sorted_in_place) {
+                err = bi::gather_sorted(c, x, m, k, e, seg, perm, xs);
+                x_sorted = xs;
+            }
+            if (err == cudaSuccess) err = bi::build_tails(c, dy, n, e, seg, perm, dyt);
+            if (err == cudaSuccess) err = bi::build_tails(c, x, k, e, seg, perm, xt);
+            if (err == cudaSuccess)
+                err = bi::tc_grouped_dw(c, dtype, dw, dy_sorted, x_sorted, dyt, xt, m, k, n, e, seg);
         } else {
             err = bi::scalar_dw_grouped(c, dtype, dw, dy, x, m, n, k, e, seg, perm, part, max_chunks);
         }

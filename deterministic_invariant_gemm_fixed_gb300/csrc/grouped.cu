@@ -10,7 +10,7 @@
 //               (bucket = id for id < E, bucket E = padding);
 //   2. scan:    exclusive prefix over (bucket, block) in bucket-major order gives
 //               every block its first output position per bucket, the group
-//               offsets, and the padded starts used by the tensor-core tier;
+//               offsets, and each expert's first 256-row tile (tensor-core tier);
 //   3. scatter: each block walks its slice in row order, 256 rows at a time; a
 //               row's position is its block's running base for its bucket plus
 //               the number of earlier rows of that bucket in the same 256-row
@@ -65,9 +65,20 @@ __global__ void __launch_bounds__(SEG_THREADS)
     }
 }
 
+// First tile of each expert in the tensor-core grouped passes: the prefix sum of
+// ceil(count / GROUPED_TILE_ROWS), written after the offsets (one thread).
+__device__ void write_tile_starts(uint32_t* seg, uint32_t E) {
+    uint32_t ts = 0;
+    for (uint32_t g = 0; g < E; ++g) {
+        seg[E + 2 + g] = ts;
+        ts += (seg[g + 1] - seg[g] + GROUPED_TILE_ROWS - 1) / GROUPED_TILE_ROWS;
+    }
+    seg[E + 2 + E] = ts;
+    seg[2 * E + 3] = ts;
+}
+
 // One block.  hist (bucket-major, (E+1)*NB entries) becomes its exclusive
-// prefix sum; seg receives offsets[0..E+1], padded starts pstart[0..E] and the
-// total padded row count.
+// prefix sum; seg receives offsets[0..E+1] and the tile starts.
 __global__ void __launch_bounds__(1024)
     seg_scan_kernel(uint32_t* hist, int64_t NB, uint32_t E, int64_t M, uint32_t* seg) {
     __shared__ uint32_t warp_sums[32];
@@ -104,14 +115,7 @@ __global__ void __launch_bounds__(1024)
     if (threadIdx.x == 0) {
         for (uint32_t g = 0; g <= E; ++g) seg[g] = hist[static_cast<int64_t>(g) * NB];
         seg[E + 1] = static_cast<uint32_t>(M);
-        uint32_t ps = 0;
-        for (uint32_t g = 0; g < E; ++g) {
-            seg[E + 2 + g] = ps;
-            const uint32_t cnt = seg[g + 1] - seg[g];
-            ps += (cnt + 127u) / 128u * 128u;
-        }
-        seg[E + 2 + E] = ps;
-        seg[2 * E + 3] = ps;
+        write_tile_starts(seg, E);
     }
 }
 
@@ -157,13 +161,7 @@ __global__ void seg_from_offsets_kernel(const uint32_t* offsets, int64_t M, uint
             prev = cl;
         }
         seg[E + 1] = m;
-        uint32_t ps = 0;
-        for (uint32_t g = 0; g < E; ++g) {
-            seg[E + 2 + g] = ps;
-            ps += (seg[g + 1] - seg[g] + 127u) / 128u * 128u;
-        }
-        seg[E + 2 + E] = ps;
-        seg[2 * E + 3] = ps;
+        write_tile_starts(seg, E);
         if (bad && status) *reinterpret_cast<volatile int*>(status) = DEV_BAD_OFFSETS;
     }
     for (int64_t r = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; r < M;
@@ -171,26 +169,31 @@ __global__ void seg_from_offsets_kernel(const uint32_t* offsets, int64_t M, uint
         perm[r] = static_cast<uint32_t>(r);
 }
 
-// dst row p (padded order): expert g with pstart[g] <= p < pstart[g+1];
-// rows past the expert's count are zero.
-__global__ void gather_padded_kernel(const uint4* src, int64_t L16, uint32_t E, const uint32_t* seg,
-                                     const uint32_t* perm, uint4* dst, int64_t Mp_max) {
-    const uint32_t* off = seg;
-    const uint32_t* pst = seg + E + 2;
-    const int64_t total = pst[E];
-    for (int64_t p = blockIdx.x; p < total && p < Mp_max; p += gridDim.x) {
-        uint32_t lo = 0, hi = E;  // largest g with pst[g] <= p
-        while (hi - lo > 1) {
-            const uint32_t mid = (lo + hi) / 2;
-            if (pst[mid] <= p) lo = mid; else hi = mid;
-        }
-        const uint32_t g = lo;
-        const int64_t l = p - pst[g];
-        const int64_t cnt = off[g + 1] - off[g];
-        uint4* d = dst + p * L16;
-        if (l < cnt) {
-            const uint4* s = src + static_cast<int64_t>(perm[off[g] + l]) * L16;
-            for (int64_t i = threadIdx.x; i < L16; i += blockDim.x) d[i] = __ldg(s + i);
+// dst row s (s < offsets[E]) = src row perm[s]; one row per block step.
+__global__ void gather_sorted_kernel(const uint4* src, int64_t L16, uint32_t E, const uint32_t* seg,
+                                     const uint32_t* perm, uint4* dst) {
+    const int64_t rows = seg[E];
+    for (int64_t r = blockIdx.x; r < rows; r += gridDim.x) {
+        const uint4* sp = src + static_cast<int64_t>(perm[r]) * L16;
+        uint4* d = dst + r * L16;
+        for (int64_t i = threadIdx.x; i < L16; i += blockDim.x) d[i] = __ldg(sp + i);
+    }
+}
+
+// dst row q = g*64 + l: expert g's sorted row (its last multiple of 64) + l, if
+// the expert has it, else zeros.
+__global__ void build_tails_kernel(const uint4* src, int64_t L16, uint32_t E, const uint32_t* seg,
+                                   const uint32_t* perm, uint4* dst) {
+    const int64_t rows = static_cast<int64_t>(E) * GROUPED_TAIL_ROWS;
+    for (int64_t q = blockIdx.x; q < rows; q += gridDim.x) {
+        const uint32_t g = static_cast<uint32_t>(q / GROUPED_TAIL_ROWS);
+        const uint32_t l = static_cast<uint32_t>(q % GROUPED_TAIL_ROWS);
+        const uint32_t cnt = seg[g + 1] - seg[g];
+        const uint32_t pos = cnt / GROUPED_TAIL_ROWS * GROUPED_TAIL_ROWS + l;
+        uint4* d = dst + q * L16;
+        if (pos < cnt) {
+            const uint4* sp = src + static_cast<int64_t>(perm[seg[g] + pos]) * L16;
+            for (int64_t i = threadIdx.x; i < L16; i += blockDim.x) d[i] = __ldg(sp + i);
         } else {
             const uint4 z = make_uint4(0, 0, 0, 0);
             for (int64_t i = threadIdx.x; i < L16; i += blockDim.x) d[i] = z;
@@ -277,14 +280,26 @@ cudaError_t segment_from_offsets(const LaunchCtx& c, const uint32_t* offsets, in
     return cudaGetLastError();
 }
 
-cudaError_t gather_padded(const LaunchCtx& c, const void* src, int64_t M, int64_t L, int64_t E,
-                          const uint32_t* seg, const uint32_t* perm, void* dst, int64_t Mp_max) {
-    (void)M;
+cudaError_t gather_sorted(const LaunchCtx& c, const void* src, int64_t M, int64_t L, int64_t E,
+                          const uint32_t* seg, const uint32_t* perm, void* dst) {
+    if (M == 0) return cudaSuccess;
     const int64_t L16 = L * 2 / 16;  // 16-bit data, L a multiple of 8
-    int64_t blocks = Mp_max < static_cast<int64_t>(c.sm_count) * 16 ? Mp_max : static_cast<int64_t>(c.sm_count) * 16;
-    if (blocks < 1) blocks = 1;
-    gather_padded_kernel<<<static_cast<unsigned>(blocks), 256, 0, c.stream>>>(
-        static_cast<const uint4*>(src), L16, static_cast<uint32_t>(E), seg, perm, static_cast<uint4*>(dst), Mp_max);
+    const int64_t cap = static_cast<int64_t>(c.sm_count) * 16;
+    const int64_t blocks = M < cap ? M : cap;
+    gather_sorted_kernel<<<static_cast<unsigned>(blocks), 256, 0, c.stream>>>(
+        static_cast<const uint4*>(src), L16, static_cast<uint32_t>(E), seg, perm, static_cast<uint4*>(dst));
+    c.count();
+    return cudaGetLastError();
+}
+
+cudaError_t build_tails(const LaunchCtx& c, const void* src, int64_t L, int64_t E, const uint32_t* seg,
+                        const uint32_t* perm, void* dst) {
+    const int64_t L16 = L * 2 / 16;
+    const int64_t rows = E * GROUPED_TAIL_ROWS;
+    const int64_t cap = static_cast<int64_t>(c.sm_count) * 16;
+    const int64_t blocks = rows < cap ? rows : cap;
+    build_tails_kernel<<<static_cast<unsigned>(blocks), 256, 0, c.stream>>>(
+        static_cast<const uint4*>(src), L16, static_cast<uint32_t>(E), seg, perm, static_cast<uint4*>(dst));
     c.count();
     return cudaGetLastError();
 }

@@ -3,11 +3,9 @@
 // Contract (sgemm-bi 0.1.1.post2, "Determinism contracts", row "tensor cores"):
 // f32 accumulation, bit-identical across runs, each output row independent of M.
 // Every arithmetic choice is fixed by (pass, dtype, K, N):
-//   - one MMA shape per pass family: the dense passes run
-//     tcgen05.mma.cta_group::2 M256 x N256 x K16 on a CTA pair
-//     (tc_gemm_pair_kernel), the grouped passes run tcgen05.mma.cta_group::1
-//     M128 x N256 x K16 on single CTAs (tc_gemm_kernel); f32 accumulators live
-//     in tensor memory;
+//   - one MMA shape per operand type: every pass, dense and grouped, runs
+//     tcgen05.mma.cta_group::2 M256 x N256 on a CTA pair (tc_gemm_pair_kernel;
+//     K16 per instruction for bf16/f16); f32 accumulators live in tensor memory;
 //   - the contracted index is walked in 64-wide blocks in ascending order, four
 //     K16 instructions per block, accumulating into the same TMEM tile;
 //   - no split of the contraction, no atomics, no stream-K;
@@ -37,15 +35,12 @@ constexpr int BM = 128;        // tile rows = MMA M
 constexpr int BN = 256;        // tile cols = MMA N
 constexpr int BK = 64;         // contraction block = one 128-byte swizzle row of 16-bit data
 constexpr int UK = 16;         // contraction per MMA instruction
-constexpr int STAGES = 4;
-constexpr int A_BYTES = BM * BK * 2;
-constexpr int B_BYTES = BN * BK * 2;
-constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int THREADS = 192;
 constexpr int TMEM_COLS = 2 * BN;
 constexpr int BAR_BYTES = 256;
-constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + BAR_BYTES;
 constexpr int GROUP_M = 16;    // raster: 16 row-tiles share the column sweep (L2 reuse)
+static_assert(GROUPED_TILE_ROWS == 256 && GROUPED_TAIL_ROWS == BK,
+              "the grouping's tile and tail sizes are the pair kernel's");
 
 enum Mode { DENSE = 0, GROUPED_ROWS = 1, GROUPED_DW = 2 };
 
@@ -123,24 +118,6 @@ __device__ __noinline__ bool mbar_wait_impl(uint32_t bar, uint32_t parity, volat
 #define mbar_wait(bar, parity, abort_flag, p, code) \
     mbar_wait_impl((bar), (parity), (abort_flag), (p).status, (p).wait_limit, (code))
 
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y,
-                                            uint32_t bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
-        : "memory");
-}
-
-__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int x, int y,
-                                            int z, uint32_t bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar)
-        : "memory");
-}
-
 __device__ __forceinline__ void cluster_sync() {
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
@@ -162,31 +139,6 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint
     d |= 1ull << 46;
     d |= 2ull << 61;
     return d;
-}
-
-// Instruction descriptor for kind::f16: D f32 (bit 4), A/B format (bits 7, 10),
-// A/B major (bits 15, 16: 1 = MN-major), N >> 3 (bits 17..22), M >> 4 (bits 24..28).
-template <int FMT, bool A_MN, bool B_MN>
-__device__ __forceinline__ constexpr uint32_t instr_desc() {
-    return (1u << 4) | (static_cast<uint32_t>(FMT) << 7) | (static_cast<uint32_t>(FMT) << 10) |
-           (static_cast<uint32_t>(A_MN) << 15) | (static_cast<uint32_t>(B_MN) << 16) |
-           (static_cast<uint32_t>(BN >> 3) << 17) | (static_cast<uint32_t>(BM >> 4) << 24);
-}
-
-__device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
-                                        uint32_t idesc, uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
-        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-
-__device__ __forceinline__ void mma_commit(uint32_t bar) {
-    asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-        : "memory");
 }
 
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&v)[16]) {
@@ -230,328 +182,27 @@ template <> struct OutT<1> {
     }
 };
 
-// ---------------------------------------------------------------- tile schedule
-
-struct Tile {
-    int m_blk, n_blk, g, nkb;
-    int row0;       // grouped: first padded row of the A tile / of the expert
-    int valid;      // grouped rows: rows of this tile that belong to the expert
-    uint32_t sbase; // grouped rows: sorted position of the tile's first row
-};
-
-template <int MODE>
-__device__ __forceinline__ bool get_tile(const Params& p, int t, Tile& ti) {
-    if (MODE == DENSE) {
-        const int total = p.num_m * p.num_n;
-        if (t >= total) return false;
-        const int span = GROUP_M * p.num_n;
-        const int grp = t / span;
-        const int first_m = grp * GROUP_M;
-        const int gsize = min(p.num_m - first_m, GROUP_M);
-        const int r = t - grp * span;
-        ti.m_blk = first_m + r % gsize;
-        ti.n_blk = r / gsize;
-        ti.g = 0;
-        ti.nkb = p.num_kb;
-        ti.row0 = ti.m_blk * BM;
-        ti.valid = BM;
-        ti.sbase = 0;
-        return true;
-    } else if (MODE == GROUPED_ROWS) {
-        const uint32_t* off = p.seg;
-        const uint32_t* pst = p.seg + p.E + 2;
-        for (int g = 0; g < p.E; ++g) {
-            const int cnt = static_cast<int>(off[g + 1] - off[g]);
-            const int mt = (cnt + BM - 1) / BM;
-            const int tiles = mt * p.num_n;
-            if (t < tiles) {
-                ti.m_blk = t / p.num_n;
-                ti.n_blk = t % p.num_n;
-                ti.g = g;
-                ti.nkb = p.num_kb;
-                ti.row0 = static_cast<int>(pst[g]) + ti.m_blk * BM;
-                ti.valid = min(BM, cnt - ti.m_blk * BM);
-                ti.sbase = off[g] + static_cast<uint32_t>(ti.m_blk * BM);
-                return true;
-            }
-            t -= tiles;
-        }
-        return false;
-    } else {
-        const int per = p.num_m * p.num_n;
-        const int g = t / per;
-        if (g >= p.E) return false;
-        const int r = t - g * per;
-        const uint32_t* off = p.seg;
-        const uint32_t* pst = p.seg + p.E + 2;
-        const int cnt = static_cast<int>(off[g + 1] - off[g]);
-        ti.m_blk = r / p.num_n;
-        ti.n_blk = r % p.num_n;
-        ti.g = g;
-        ti.nkb = 2 * ((cnt + BM - 1) / BM);  // padded rows / BK
-        ti.row0 = static_cast<int>(pst[g]);
-        ti.valid = BM;
-        ti.sbase = 0;
-        return true;
-    }
-}
-
-// ---------------------------------------------------------------- the kernel
-
-template <int FMT, bool A_MN, bool B_MN, bool B3D, int MODE, bool OUT_F32>
-__global__ void __launch_bounds__(THREADS, 1)
-    tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                   const Params p) {
-    extern __shared__ uint8_t smem_raw[];
-    const uint32_t raw = smem_u32(smem_raw);
-    uint8_t* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
-    const uint32_t sbase = smem_u32(smem);
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
-    const uint32_t bar0 = smem_u32(bars);
-    auto full_bar = [&](int s) { return bar0 + 8u * s; };
-    auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
-    auto tfull_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + b); };
-    auto tempty_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + 2 + b); };
-    const uint32_t drain_bar = bar0 + 8u * (2 * STAGES + 4);
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 5);
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-
-    const int warp = threadIdx.x >> 5;
-    const int lane = threadIdx.x & 31;
-
-    if (threadIdx.x == 0) {
-        for (int s = 0; s < STAGES; ++s) {
-            mbar_init(full_bar(s), 1);
-            mbar_init(empty_bar(s), 1);
-        }
-        for (int b = 0; b < 2; ++b) {
-            mbar_init(tfull_bar(b), 1);
-            mbar_init(tempty_bar(b), 4);  // one arrival per epilogue warp
-        }
-        mbar_init(drain_bar, 1);
-        *abort_flag = 0;
-        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    }
-    if (warp == 1) {
-        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
-                         smem_u32(tmem_slot)),
-                     "r"(TMEM_COLS)
-                     : "memory");
-        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-    }
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
-
-    if (warp == 0 && lane == 0) {
-        // ------------------------------------------------------------ producer
-        int s = 0;
-        uint32_t ph = 0;
-        uint32_t used = 0, last_par = 0;  // per stage: ever issued / parity of the last issue
-        Tile ti;
-        for (int t = blockIdx.x; get_tile<MODE>(p, t, ti); t += gridDim.x) {
-            if (ti.nkb == 0) continue;
-            for (int kb = 0; kb < ti.nkb; ++kb) {
-                if (!mbar_wait(empty_bar(s), ph ^ 1u, abort_flag, p, DEV_TIMEOUT_PRODUCER)) goto drain;
-                const uint32_t fb = full_bar(s);
-                mbar_expect_tx(fb, STAGE_BYTES);
-                const uint32_t a_dst = sbase + s * STAGE_BYTES;
-                const uint32_t b_dst = a_dst + A_BYTES;
-                const int kofs = kb * BK;
-                // A operand
-                if (MODE == GROUPED_DW) {
-                    // dY rows of the expert, MN-major: out index n contiguous
-                    for (int a = 0; a < BM / 64; ++a)
-                        tma_load_2d(a_dst + a * (BK * 128), &tmA, ti.m_blk * BM + a * 64,
-                                    ti.row0 + kofs, fb);
-                } else if (A_MN) {
-                    for (int a = 0; a < BM / 64; ++a)
-                        tma_load_2d(a_dst + a * (BK * 128), &tmA, ti.m_blk * BM + a * 64, kofs, fb);
-                } else {
-                    tma_load_2d(a_dst, &tmA, kofs, ti.row0, fb);
-                }
-                // B operand
-                if (MODE == GROUPED_DW) {
-                    for (int b = 0; b < BN / 64; ++b)
-                        tma_load_2d(b_dst + b * (BK * 128), &tmB, ti.n_blk * BN + b * 64,
-                                    ti.row0 + kofs, fb);
-                } else if (B3D) {
-                    if (B_MN) {
-                        for (int b = 0; b < BN / 64; ++b)
-                            tma_load_3d(b_dst + b * (BK * 128), &tmB, ti.n_blk * BN + b * 64, kofs,
-                                        ti.g, fb);
-                    } else {
-                        tma_load_3d(b_dst, &tmB, kofs, ti.n_blk * BN, ti.g, fb);
-                    }
-                } else if (B_MN) {
-                    for (int b = 0; b < BN / 64; ++b)
-                        tma_load_2d(b_dst + b * (BK * 128), &tmB, ti.n_blk * BN + b * 64, kofs, fb);
-                } else {
-                    tma_load_2d(b_dst, &tmB, kofs, ti.n_blk * BN, fb);
-                }
-                used |= 1u << s;
-                last_par = (last_par & ~(1u << s)) | (ph << s);
-                if (++s == STAGES) { s = 0; ph ^= 1u; }
-            }
-        }
-    drain:
-        // make sure no copy into this CTA's shared memory is still in flight
-        for (int q = 0; q < STAGES; ++q)
-            if (used & (1u << q))
-                mbar_wait(full_bar(q), (last_par >> q) & 1u, abort_flag, p, DEV_TIMEOUT_PRODUCER);
-    } else if (warp == 1 && lane == 0) {
-        // ------------------------------------------------------------ MMA issuer
-        constexpr uint32_t idesc = instr_desc<FMT, A_MN || MODE == GROUPED_DW,
-                                              B_MN || MODE == GROUPED_DW>();
-        constexpr bool AM = A_MN || MODE == GROUPED_DW;
-        constexpr bool BMN = B_MN || MODE == GROUPED_DW;
-        int s = 0;
-        uint32_t ph = 0;
-        int ab = 0;
-        uint32_t aph = 0;
-        Tile ti;
-        for (int t = blockIdx.x; get_tile<MODE>(p, t, ti); t += gridDim.x) {
-            if (ti.nkb == 0) continue;
-            if (!mbar_wait(tempty_bar(ab), aph ^ 1u, abort_flag, p, DEV_TIMEOUT_MMA)) break;
-            tc_fence_after();
-            const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(ab * BN);
-            bool ok = true;
-            for (int kb = 0; kb < ti.nkb; ++kb) {
-                if (!mbar_wait(full_bar(s), ph, abort_flag, p, DEV_TIMEOUT_MMA)) { ok = false; break; }
-                tc_fence_after();
-                const uint32_t a_s = sbase + s * STAGE_BYTES;
-                const uint32_t b_s = a_s + A_BYTES;
-#pragma unroll
-                for (int kk = 0; kk < BK / UK; ++kk) {
-                    // K-major: step 32 bytes along the swizzled 128-byte row;
-                    // MN-major: step 16 rows = 2048 bytes (2 swizzle atoms of 8 rows).
-                    const uint64_t ad = AM ? smem_desc(a_s + kk * 2048, BK * 128, 1024)
-                                           : smem_desc(a_s + kk * 32, 16, 1024);
-                    const uint64_t bd = BMN ? smem_desc(b_s + kk * 2048, BK * 128, 1024)
-                                            : smem_desc(b_s + kk * 32, 16, 1024);
-                    mma_f16(d_tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
-                }
-                mma_commit(empty_bar(s));  // frees the stage once these MMAs have read it
-                if (++s == STAGES) { s = 0; ph ^= 1u; }
-            }
-            if (!ok) break;
-            mma_commit(tfull_bar(ab));
-            if (++ab == 2) { ab = 0; aph ^= 1u; }
-        }
-        // wait for every MMA this thread issued before TMEM can be released
-        mma_commit(drain_bar);
-        mbar_wait(drain_bar, 0, abort_flag, p, DEV_TIMEOUT_MMA);
-    } else if (warp >= 2) {
-        // ------------------------------------------------------------ epilogue
-        const int q = warp & 3;              // TMEM lane quarter this warp may access
-        const int r = q * 32 + lane;         // tile row owned by this thread
-        int ab = 0;
-        uint32_t aph = 0;
-        Tile ti;
-        for (int t = blockIdx.x; get_tile<MODE>(p, t, ti); t += gridDim.x) {
-            // output row of this thread (or -1)
-            int64_t orow = -1;
-            void* out = p.out;
-            if (MODE == DENSE) {
-                const int64_t gr = static_cast<int64_t>(ti.m_blk) * BM + r;
-                if (gr < p.rows) orow = gr;
-            } else if (MODE == GROUPED_ROWS) {
-                if (r < ti.valid) orow = p.perm[ti.sbase + r];
-            } else {
-                const int64_t gr = static_cast<int64_t>(ti.m_blk) * BM + r;
-                if (gr < p.rows) orow = gr;
-                out = static_cast<float*>(p.out) + static_cast<int64_t>(ti.g) * p.rows * p.ldo;
-            }
-            const int64_t col0 = static_cast<int64_t>(ti.n_blk) * BN;
-            if (ti.nkb == 0) {  // empty expert: +0 everywhere, no accumulator involved
-                if (orow >= 0)
-                    for (int64_t c = col0; c < col0 + BN && c < p.cols; ++c)
-                        static_cast<float*>(out)[orow * p.ldo + c] = 0.0f;
-                continue;
-            }
-            bool ok = mbar_wait(tfull_bar(ab), aph, abort_flag, p, DEV_TIMEOUT_EPILOGUE);
-            ok = __all_sync(0xffffffffu, ok);
-            if (!ok) break;
-            tc_fence_after();
-            const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
-                                   static_cast<uint32_t>(ab * BN);
-            for (int c0 = 0; c0 < BN; c0 += 16) {
-                if (col0 + c0 >= p.cols) break;  // uniform across the warp
-                uint32_t v[16];
-                tmem_ld16(tbase + c0, v);
-                if (orow < 0) continue;
-                float f[16];
-#pragma unroll
-                for (int i = 0; i < 16; ++i) f[i] = __uint_as_float(v[i]);
-                const int64_t cb = col0 + c0;
-                if (MODE == DENSE && p.bias != nullptr) {
-#pragma unroll
-                    for (int i = 0; i < 16; ++i)
-                        if (cb + i < p.cols) f[i] = f[i] + OutT<FMT>::load(p.bias, cb + i);
-                }
-                const bool full = cb + 16 <= p.cols;
-                if (OUT_F32) {
-                    float* dst = static_cast<float*>(out) + orow * p.ldo + cb;
-                    if (full) {
-#pragma unroll
-                        for (int i = 0; i < 16; i += 4)
-                            *reinterpret_cast<float4*>(dst + i) = make_float4(f[i], f[i + 1], f[i + 2], f[i + 3]);
-                    } else {
-                        for (int i = 0; i < 16; ++i)
-                            if (cb + i < p.cols) dst[i] = f[i];
-                    }
-                } else {
-                    using T = typename OutT<FMT>::T;
-                    T* dst = static_cast<T*>(out) + orow * p.ldo + cb;
-                    if (full) {
-                        uint4 w0, w1;
-                        w0.x = OutT<FMT>::pack(f[0], f[1]);
-                        w0.y = OutT<FMT>::pack(f[2], f[3]);
-                        w0.z = OutT<FMT>::pack(f[4], f[5]);
-                        w0.w = OutT<FMT>::pack(f[6], f[7]);
-                        w1.x = OutT<FMT>::pack(f[8], f[9]);
-                        w1.y = OutT<FMT>::pack(f[10], f[11]);
-                        w1.z = OutT<FMT>::pack(f[12], f[13]);
-                        w1.w = OutT<FMT>::pack(f[14], f[15]);
-                        reinterpret_cast<uint4*>(dst)[0] = w0;
-                        reinterpret_cast<uint4*>(dst)[1] = w1;
-                    } else {
-                        for (int i = 0; i < 16; ++i)
-                            if (cb + i < p.cols) OutT<FMT>::store1(dst, i, f[i]);
-                    }
-                }
-            }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(tempty_bar(ab));
-            if (++ab == 2) { ab = 0; aph ^= 1u; }
-        }
-    }
-
-    // ---------------------------------------------------------------- teardown
-    tc_fence_before();
-    __syncthreads();
-    if (warp == 1) {
-        __syncwarp();
-        tc_fence_after();
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
-                     "r"(TMEM_COLS)
-                     : "memory");
-    }
-}
-
 // ---------------------------------------------------------------- CTA-pair kernel
 //
-// Dense passes on a pair of CTAs (a 2-CTA cluster) that run one
+// Every pass runs on a pair of CTAs (a 2-CTA cluster) that run one
 // tcgen05.mma.cta_group::2 of shape M256 x N256 x K16: CTA r of the pair holds
 // rows [128r, 128r+128) of the A tile and columns [128r, 128r+128) of the B
 // tile in its own shared memory, and receives rows [128r, 128r+128) of the
 // 256 x 256 accumulator in its own tensor memory.  Only CTA 0 issues MMAs.
 // Per CTA a 64-wide contraction block is 32 KB (A 16 KB + B 16 KB), so a
-// 7-stage ring fits.  The arithmetic of each output element is the same
-// ascending chain of K16 blocks as in tc_gemm_kernel; only the instruction
-// shape and the CTA mapping differ, both fixed by the pass, never by M.
+// 7-stage ring fits.  Each output element is one ascending chain of K16 blocks
+// in its accumulator; the instruction shape and the CTA mapping are fixed by
+// the pass, never by M.
+//
+// Work units (256 x 256 output tiles), by mode:
+//   DENSE         a grouped raster over (row pair-tile, column tile);
+//   GROUPED_ROWS  forward / dinput: 256 consecutive rows of one expert in the
+//                 row-sorted operand, starting at any row (rows past the
+//                 expert's end are computed and discarded); the epilogue writes
+//                 row perm[s] of the output;
+//   GROUPED_DW    dweights: (expert, n tile, k tile), contraction over the
+//                 expert's rows in 64-row blocks read in place, the partial
+//                 last block read from a zero-padded tail buffer (tmA2/tmB2).
 //
 // Barriers: full[s] (CTA 0, count 1, 64 KB expected from both CTAs' copies),
 // empty[s] (each CTA, released by CTA 0's commit multicast to both), tfull[b]
@@ -579,6 +230,79 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap
         " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar_cluster)
         : "memory");
+}
+
+__device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const CUtensorMap* map, int x, int y, int z,
+                                                 uint32_t bar_cluster) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar_cluster)
+        : "memory");
+}
+
+// One work unit of the pair kernel.
+struct PairTile {
+    int g;        // expert (grouped modes)
+    int mpair;    // 256-row output tile (dense, dweights); tile within the expert (rows)
+    int nb;       // 256-column output tile
+    int nkb;      // contraction blocks
+    int row0;     // grouped: first sorted row of the unit (rows) / of the expert (dweights)
+    int row_end;  // grouped: end of the expert's sorted rows
+    int full_kb;  // dweights: blocks read in place; block full_kb is the tail block
+};
+
+template <int MODE>
+__device__ __forceinline__ bool pair_tile(const Params& p, int t, PairTile& u) {
+    const int units_m = (p.num_m + 1) / 2;
+    if (MODE == DENSE) {
+        if (t >= units_m * p.num_n) return false;
+        const int span = GROUP_M * p.num_n;
+        const int grp = t / span;
+        const int first = grp * GROUP_M;
+        const int gsize = min(units_m - first, GROUP_M);
+        const int r = t - grp * span;
+        u.g = 0;
+        u.mpair = first + r % gsize;
+        u.nb = r / gsize;
+        u.nkb = p.num_kb;
+        u.row0 = 0;
+        u.row_end = 0;
+        u.full_kb = p.num_kb;
+        return true;
+    }
+    const uint32_t* off = p.seg;            // sorted offsets of buckets 0..E, then m
+    const uint32_t* tst = p.seg + p.E + 2;  // first 256-row tile of each expert; tst[E] = all
+    if (MODE == GROUPED_ROWS) {
+        const int rt = t / p.num_n;
+        if (rt >= static_cast<int>(tst[p.E])) return false;
+        int lo = 0, hi = p.E - 1;  // the largest g < E with tst[g] <= rt
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (static_cast<int>(tst[mid]) <= rt) lo = mid; else hi = mid - 1;
+        }
+        u.g = lo;
+        u.nb = t - rt * p.num_n;
+        u.mpair = rt - static_cast<int>(tst[lo]);
+        u.row0 = static_cast<int>(off[lo]) + u.mpair * 256;
+        u.row_end = static_cast<int>(off[lo + 1]);
+        u.nkb = p.num_kb;
+        u.full_kb = p.num_kb;
+        return true;
+    }
+    const int per = units_m * p.num_n;
+    const int g = t / per;
+    if (g >= p.E) return false;
+    const int r = t - g * per;
+    const int cnt = static_cast<int>(off[g + 1] - off[g]);
+    u.g = g;
+    u.mpair = r / p.num_n;
+    u.nb = r - u.mpair * p.num_n;
+    u.row0 = static_cast<int>(off[g]);
+    u.row_end = u.row0 + cnt;
+    u.full_kb = cnt / BK;
+    u.nkb = (cnt + BK - 1) / BK;
+    return true;
 }
 
 template <int IN>
@@ -646,7 +370,7 @@ __device__ __forceinline__ constexpr uint32_t instr_desc_pair() {
 // columns 256-511, and the epilogue adds the two (one rounding).  The tensor
 // core's accumulation rounding then hits the large sum once per K step rather
 // than three times, and the small sum's rounding is 2^-11 smaller.
-template <int IN, int OUT, bool A_MN, bool B_MN>
+template <int IN, int OUT, bool A_MN, bool B_MN, int MODE>
 __global__ void __launch_bounds__(THREADS, 1)
     tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ CUtensorMap tmA2, const __grid_constant__ CUtensorMap tmB2,
@@ -654,6 +378,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     constexpr int ES = IN == 2 ? 1 : (IN == 3 ? 4 : 2);  // operand element size, bytes
     // the tf32 operands are always staged K-major (the split kernel transposes)
     static_assert(IN != 3 || (!A_MN && !B_MN), "3xTF32 takes K-major operands only");
+    static_assert(MODE == DENSE || IN <= 1, "grouped passes take bf16 / f16 operands");
     constexpr int P_STAGES = p_stages(IN);
     constexpr int P_STAGE_BYTES = p_stage_bytes(IN);
     constexpr int BKE = 128 / ES;           // contraction elements per block
@@ -706,45 +431,46 @@ __global__ void __launch_bounds__(THREADS, 1)
     tc_fence_after();
     const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
 
-    const int units_m = (p.num_m + 1) / 2;  // 256-row pair tiles
-    const int total = units_m * p.num_n;
-    auto unit_tile = [&](int t, int& mpair, int& nb) {
-        const int span = GROUP_M * p.num_n;
-        const int grp = t / span;
-        const int first = grp * GROUP_M;
-        const int gsize = min(units_m - first, GROUP_M);
-        const int r = t - grp * span;
-        mpair = first + r % gsize;
-        nb = r / gsize;
-    };
-
     if (warp == 0 && lane == 0) {
         // ------------------------------------------------------------ producer (both CTAs)
         int s = 0;
         uint32_t ph = 0;
-        for (int t = cidx; t < total; t += ncl) {
-            int mpair, nb;
-            unit_tile(t, mpair, nb);
-            const int arow = mpair * 256 + static_cast<int>(crank) * 128;  // A rows of this CTA
-            const int bcol = nb * BN + static_cast<int>(crank) * 128;      // B cols of this CTA
-            for (int kb = 0; kb < p.num_kb; ++kb) {
+        PairTile u;
+        for (int t = cidx; pair_tile<MODE>(p, t, u); t += ncl) {
+            // A rows (MN-major: A columns) and B columns of this CTA
+            const int arow = (MODE == GROUPED_ROWS ? u.row0 : u.mpair * 256) + static_cast<int>(crank) * 128;
+            const int bcol = u.nb * BN + static_cast<int>(crank) * 128;
+            for (int kb = 0; kb < u.nkb; ++kb) {
                 if (!mbar_wait(empty_bar(s), ph ^ 1u, abort_flag, p, DEV_TIMEOUT_PRODUCER)) goto done_p;
                 const uint32_t fb_leader = mapa_rank(full_bar(s), 0);
                 if (crank == 0) mbar_expect_tx(full_bar(s), 2 * P_STAGE_BYTES);
-                const int kofs = kb * BKE;
+                int kofs = kb * BKE;  // contraction coordinate
+                bool tail = false;
+                if (MODE == GROUPED_DW) {  // the expert's rows in place, or its tail block
+                    tail = kb == u.full_kb;
+                    kofs = tail ? u.g * BKE : u.row0 + kofs;
+                }
 #pragma unroll
                 for (int part = 0; part < p_tiles(IN); ++part) {
                     const uint32_t a_dst = sbase + s * P_STAGE_BYTES + part * (P_A_BYTES + P_B_BYTES);
                     const uint32_t b_dst = a_dst + P_A_BYTES;
-                    const CUtensorMap* ma = part ? &tmA2 : &tmA;
-                    const CUtensorMap* mb = part ? &tmB2 : &tmB;
+                    const CUtensorMap* ma = (part || tail) ? &tmA2 : &tmA;
+                    const CUtensorMap* mb = (part || tail) ? &tmB2 : &tmB;
                     if (A_MN) {
                         for (int a = 0; a < MN_ATOMS; ++a)
                             tma_load_2d_pair(a_dst + a * (BKE * 128), ma, arow + a * (128 / ES), kofs, fb_leader);
                     } else {
                         tma_load_2d_pair(a_dst, ma, kofs, arow, fb_leader);
                     }
-                    if (B_MN) {
+                    if (MODE == GROUPED_ROWS) {  // W[g] through a 3-D map
+                        if (B_MN) {
+                            for (int b = 0; b < MN_ATOMS; ++b)
+                                tma_load_3d_pair(b_dst + b * (BKE * 128), mb, bcol + b * (128 / ES), kofs, u.g,
+                                                 fb_leader);
+                        } else {
+                            tma_load_3d_pair(b_dst, mb, kofs, bcol, u.g, fb_leader);
+                        }
+                    } else if (B_MN) {
                         for (int b = 0; b < MN_ATOMS; ++b)
                             tma_load_2d_pair(b_dst + b * (BKE * 128), mb, bcol + b * (128 / ES), kofs, fb_leader);
                     } else {
@@ -765,12 +491,14 @@ __global__ void __launch_bounds__(THREADS, 1)
         uint32_t ph = 0;
         int ab = 0;
         uint32_t aph = 0;
-        for (int t = cidx; t < total; t += ncl) {
+        PairTile u;
+        for (int t = cidx; pair_tile<MODE>(p, t, u); t += ncl) {
+            if (u.nkb == 0) continue;  // empty expert: the epilogue writes +0
             if (!mbar_wait(tempty_bar(ab), aph ^ 1u, abort_flag, p, DEV_TIMEOUT_MMA)) break;
             tc_fence_after();
             const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(ab * BN);
             bool ok = true;
-            for (int kb = 0; kb < p.num_kb; ++kb) {
+            for (int kb = 0; kb < u.nkb; ++kb) {
                 if (!mbar_wait(full_bar(s), ph, abort_flag, p, DEV_TIMEOUT_MMA)) { ok = false; break; }
                 tc_fence_after();
                 const uint32_t a_s = sbase + s * P_STAGE_BYTES;
@@ -813,12 +541,25 @@ __global__ void __launch_bounds__(THREADS, 1)
         int ab = 0;
         uint32_t aph = 0;
         const float scale = IN == 2 ? __fmul_rn(__ldg(p.scale_a), __ldg(p.scale_b)) : 1.0f;
-        for (int t = cidx; t < total; t += ncl) {
-            int mpair, nb;
-            unit_tile(t, mpair, nb);
-            const int64_t gr = static_cast<int64_t>(mpair) * 256 + crank * 128 + r;
-            const int64_t orow = gr < p.rows ? gr : -1;
-            const int64_t col0 = static_cast<int64_t>(nb) * BN;
+        PairTile u;
+        for (int t = cidx; pair_tile<MODE>(p, t, u); t += ncl) {
+            int64_t orow = -1;  // output row of this thread, or -1
+            void* out = p.out;
+            if (MODE == GROUPED_ROWS) {
+                const int srow = u.row0 + static_cast<int>(crank) * 128 + r;  // sorted row
+                if (srow < u.row_end) orow = p.perm[srow];
+            } else {
+                const int64_t gr = static_cast<int64_t>(u.mpair) * 256 + crank * 128 + r;
+                if (gr < p.rows) orow = gr;
+                if (MODE == GROUPED_DW) out = static_cast<float*>(p.out) + static_cast<int64_t>(u.g) * p.rows * p.ldo;
+            }
+            const int64_t col0 = static_cast<int64_t>(u.nb) * BN;
+            if (u.nkb == 0) {  // empty expert (dweights): +0, no accumulator involved
+                if (orow >= 0)
+                    for (int64_t c = col0; c < col0 + BN && c < p.cols; ++c)
+                        static_cast<float*>(out)[orow * p.ldo + c] = 0.0f;
+                continue;
+            }
             bool ok = mbar_wait(tfull_bar(ab), aph, abort_flag, p, DEV_TIMEOUT_EPILOGUE);
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) break;
@@ -839,7 +580,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
                     for (int i = 0; i < 16; ++i) f[i] = __fadd_rn(f[i], __uint_as_float(v2[i]));
                     if (p.accum_out) {  // earlier pieces' sum, left by the previous launch
-                        const float* prev = static_cast<const float*>(p.out) + orow * p.ldo + col0 + c0;
+                        const float* prev = static_cast<const float*>(out) + orow * p.ldo + col0 + c0;
 #pragma unroll
                         for (int i = 0; i < 16; ++i)
                             if (col0 + c0 + i < p.cols) f[i] = __fadd_rn(prev[i], f[i]);
@@ -859,7 +600,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 }
                 const bool full = cb + 16 <= p.cols;
                 if (OUT == 2) {
-                    float* dst = static_cast<float*>(p.out) + orow * p.ldo + cb;
+                    float* dst = static_cast<float*>(out) + orow * p.ldo + cb;
                     if (full) {
 #pragma unroll
                         for (int i = 0; i < 16; i += 4)
@@ -871,7 +612,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 } else {
                     using O = OutT<OUT == 1 ? 1 : 0>;
                     using T = typename O::T;
-                    T* dst = static_cast<T*>(p.out) + orow * p.ldo + cb;
+                    T* dst = static_cast<T*>(out) + orow * p.ldo + cb;
                     if (full) {
                         uint4 w0, w1;
                         w0.x = O::pack(f[0], f[1]);
@@ -946,30 +687,12 @@ cudaError_t make_map(CUtensorMap* m, bi_dtype dt, const void* ptr, uint64_t inne
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-template <int FMT, bool A_MN, bool B_MN, bool B3D, int MODE, bool OUT_F32>
-cudaError_t launch(const LaunchCtx& c, const CUtensorMap& a, const CUtensorMap& b, Params p,
-                   int64_t tiles_upper) {
-    auto kern = tc_gemm_kernel<FMT, A_MN, B_MN, B3D, MODE, OUT_F32>;
-    static std::once_flag once;
-    static cudaError_t attr_err = cudaSuccess;
-    std::call_once(once, [&] {
-        attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
-    });
-    if (attr_err != cudaSuccess) return attr_err;
-    if (tiles_upper <= 0) return cudaSuccess;
-    const int grid = static_cast<int>(tiles_upper < c.sm_count ? tiles_upper : c.sm_count);
-    p.status = c.status;
-    p.wait_limit = c.wait_limit_ns;
-    kern<<<grid, THREADS, SMEM_BYTES, c.stream>>>(a, b, p);
-    c.count();
-    return cudaGetLastError();
-}
-
-
-template <int IN, int OUT, bool A_MN, bool B_MN>
+// units: work units (or an upper bound, for the grouped modes, whose count is
+// known only on the device); -1 = the dense count.
+template <int IN, int OUT, bool A_MN, bool B_MN, int MODE = DENSE>
 cudaError_t launch_pair(const LaunchCtx& c, const CUtensorMap& a, const CUtensorMap& b, Params p,
-                        const CUtensorMap* a2 = nullptr, const CUtensorMap* b2 = nullptr) {
-    auto kern = tc_gemm_pair_kernel<IN, OUT, A_MN, B_MN>;
+                        const CUtensorMap* a2 = nullptr, const CUtensorMap* b2 = nullptr, int64_t units = -1) {
+    auto kern = tc_gemm_pair_kernel<IN, OUT, A_MN, B_MN, MODE>;
     constexpr int P_SMEM_BYTES = p_smem_bytes(IN);
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
@@ -993,7 +716,7 @@ cudaError_t launch_pair(const LaunchCtx& c, const CUtensorMap& a, const CUtensor
         }
     });
     if (attr_err != cudaSuccess) return attr_err;
-    const int64_t units = int64_t((p.num_m + 1) / 2) * p.num_n;
+    if (units < 0) units = int64_t((p.num_m + 1) / 2) * p.num_n;
     if (units <= 0) return cudaSuccess;
     p.status = c.status;
     p.wait_limit = c.wait_limit_ns;
@@ -1057,49 +780,49 @@ cudaError_t dw_t(const LaunchCtx& c, bi_dtype dt, void* dw, const void* x, const
 }
 
 template <int FMT>
-cudaError_t grouped_rows_t(const LaunchCtx& c, bi_dtype dt, int dinput, void* out,
-                           const void* a_pad, int64_t Mp, const void* w, int64_t M, int64_t K,
-                           int64_t N, int64_t E, const uint32_t* seg, const uint32_t* perm) {
+cudaError_t grouped_rows_t(const LaunchCtx& c, bi_dtype dt, int dinput, void* out, const void* a_sorted,
+                           const void* w, int64_t M, int64_t K, int64_t N, int64_t E, const uint32_t* seg,
+                           const uint32_t* perm) {
+    const int64_t L = dinput ? N : K;  // contraction
+    const int64_t C = dinput ? K : N;  // output columns
     CUtensorMap a, b;
     cudaError_t e;
+    // A = the row-sorted operand [M,L], K-major, 128 rows per CTA
+    if ((e = make_map(&a, dt, a_sorted, L, M, 1, BM)) != cudaSuccess) return e;
+    // B = W[g] [N,K] (3-D map): forward reads rows n (K-major, 128 per CTA);
+    // dinput reads it with the output index k contiguous (MN-major)
+    if ((e = make_map(&b, dt, w, K, N, E, dinput ? BK : BN / 2, true)) != cudaSuccess) return e;
     Params p{};
     p.seg = seg; p.perm = perm; p.E = static_cast<int>(E);
-    if (!dinput) {
-        // Y = X W[g]^T: A = padded X [Mp,K] K-major; B = W[g] [N,K] K-major (3-D map)
-        if ((e = make_map(&a, dt, a_pad, K, Mp, 1, BM)) != cudaSuccess) return e;
-        if ((e = make_map(&b, dt, w, K, N, E, BN, true)) != cudaSuccess) return e;
-        p.out = out; p.ldo = N; p.rows = M; p.cols = N;
-        p.num_n = static_cast<int>((N + BN - 1) / BN);
-        p.num_kb = static_cast<int>((K + BK - 1) / BK);
-        const int64_t up = ((M + BM - 1) / BM + E) * p.num_n;
-        return launch<FMT, false, false, true, GROUPED_ROWS, false>(c, a, b, p, up);
-    }
-    // dX = dY W[g]: A = padded dY [Mp,N] K-major; B = W[g] [N,K]: out k contiguous, contraction n
-    if ((e = make_map(&a, dt, a_pad, N, Mp, 1, BM)) != cudaSuccess) return e;
-    if ((e = make_map(&b, dt, w, K, N, E, BK, true)) != cudaSuccess) return e;
-    p.out = out; p.ldo = K; p.rows = M; p.cols = K;
-    p.num_n = static_cast<int>((K + BN - 1) / BN);
-    p.num_kb = static_cast<int>((N + BK - 1) / BK);
-    const int64_t up = ((M + BM - 1) / BM + E) * p.num_n;
-    return launch<FMT, false, true, true, GROUPED_ROWS, false>(c, a, b, p, up);
+    p.out = out; p.ldo = C; p.rows = M; p.cols = C;
+    p.num_m = 0;
+    p.num_n = static_cast<int>((C + BN - 1) / BN);
+    p.num_kb = static_cast<int>((L + BK - 1) / BK);
+    // the experts' 256-row tiles number at most floor(M / 256) + E
+    const int64_t units = (M / GROUPED_TILE_ROWS + E) * p.num_n;
+    return dinput ? launch_pair<FMT, FMT, false, true, GROUPED_ROWS>(c, a, b, p, nullptr, nullptr, units)
+                  : launch_pair<FMT, FMT, false, false, GROUPED_ROWS>(c, a, b, p, nullptr, nullptr, units);
 }
 
 template <int FMT>
-cudaError_t grouped_dw_t(const LaunchCtx& c, bi_dtype dt, float* dw, const void* dy_pad,
-                         const void* x_pad, int64_t Mp, int64_t K, int64_t N, int64_t E,
+cudaError_t grouped_dw_t(const LaunchCtx& c, bi_dtype dt, float* dw, const void* dy_sorted, const void* x_sorted,
+                         const void* dy_tail, const void* x_tail, int64_t M, int64_t K, int64_t N, int64_t E,
                          const uint32_t* seg) {
-    CUtensorMap a, b;
+    // dW[g] [N,K] = sum over the expert's rows of dY^T X: both operands MN-major
+    CUtensorMap a, b, a2, b2;
     cudaError_t e;
-    if ((e = make_map(&a, dt, dy_pad, N, Mp, 1, BK)) != cudaSuccess) return e;
-    if ((e = make_map(&b, dt, x_pad, K, Mp, 1, BK)) != cudaSuccess) return e;
+    if ((e = make_map(&a, dt, dy_sorted, N, M, 1, BK)) != cudaSuccess) return e;
+    if ((e = make_map(&b, dt, x_sorted, K, M, 1, BK)) != cudaSuccess) return e;
+    if ((e = make_map(&a2, dt, dy_tail, N, E * GROUPED_TAIL_ROWS, 1, BK)) != cudaSuccess) return e;
+    if ((e = make_map(&b2, dt, x_tail, K, E * GROUPED_TAIL_ROWS, 1, BK)) != cudaSuccess) return e;
     Params p{};
     p.out = dw; p.ldo = K; p.rows = N; p.cols = K;
     p.seg = seg; p.E = static_cast<int>(E);
     p.num_m = static_cast<int>((N + BM - 1) / BM);
     p.num_n = static_cast<int>((K + BN - 1) / BN);
     p.num_kb = 0;
-    return launch<FMT, true, true, false, GROUPED_DW, true>(c, a, b, p,
-                                                            E * int64_t(p.num_m) * p.num_n);
+    const int64_t units = E * int64_t((p.num_m + 1) / 2) * p.num_n;
+    return launch_pair<FMT, 2, true, true, GROUPED_DW>(c, a, b, p, &a2, &b2, units);
 }
 
 // 8-bit row-major tensor [outer][inner], box {128, box_outer}, 128-byte swizzle.
@@ -1186,13 +909,11 @@ cudaError_t tc_dw(const LaunchCtx& c, bi_dtype dt, void* dw, int dw_f32, const v
     return dw_f32 ? dw_t<0, true>(c, dt, dw, x, dy, M, K, N) : dw_t<0, false>(c, dt, dw, x, dy, M, K, N);
 }
 
-cudaError_t tc_grouped_rows(const LaunchCtx& c, bi_dtype dt, int pass_dinput, void* out,
-                            const void* a_padded, int64_t Mp_max, const void* w, int64_t M,
-                            int64_t K, int64_t N, int64_t E, const uint32_t* seg,
+cudaError_t tc_grouped_rows(const LaunchCtx& c, bi_dtype dt, int pass_dinput, void* out, const void* a_sorted,
+                            const void* w, int64_t M, int64_t K, int64_t N, int64_t E, const uint32_t* seg,
                             const uint32_t* perm) {
-    return dt == BI_BF16
-               ? grouped_rows_t<1>(c, dt, pass_dinput, out, a_padded, Mp_max, w, M, K, N, E, seg, perm)
-               : grouped_rows_t<0>(c, dt, pass_dinput, out, a_padded, Mp_max, w, M, K, N, E, seg, perm);
+    return dt == BI_BF16 ? grouped_rows_t<1>(c, dt, pass_dinput, out, a_sorted, w, M, K, N, E, seg, perm)
+                         : grouped_rows_t<0>(c, dt, pass_dinput, out, a_sorted, w, M, K, N, E, seg, perm);
 }
 
 cudaError_t tc_tf32x3_pass(const LaunchCtx& c, const float* a_hi, const float* a_lo, int64_t lda,
@@ -1230,12 +951,11 @@ cudaError_t tc_fp8_pass(const LaunchCtx& c, int pass, bi_dtype out_dt, void* out
     }
 }
 
-cudaError_t tc_grouped_dw(const LaunchCtx& c, bi_dtype dt, float* dw, const void* dy_padded,
-                          const void* x_padded, int64_t Mp_max, int64_t M, int64_t K, int64_t N,
-                          int64_t E, const uint32_t* seg) {
-    (void)M;
-    return dt == BI_BF16 ? grouped_dw_t<1>(c, dt, dw, dy_padded, x_padded, Mp_max, K, N, E, seg)
-                         : grouped_dw_t<0>(c, dt, dw, dy_padded, x_padded, Mp_max, K, N, E, seg);
+cudaError_t tc_grouped_dw(const LaunchCtx& c, bi_dtype dt, float* dw, const void* dy_sorted, const void* x_sorted,
+                          const void* dy_tail, const void* x_tail, int64_t M, int64_t K, int64_t N, int64_t E,
+                          const uint32_t* seg) {
+    return dt == BI_BF16 ? grouped_dw_t<1>(c, dt, dw, dy_sorted, x_sorted, dy_tail, x_tail, M, K, N, E, seg)
+                         : grouped_dw_t<0>(c, dt, dw, dy_sorted, x_sorted, dy_tail, x_tail, M, K, N, E, seg);
 }
 
 }  // namespace bi

@@ -177,3 +177,40 @@ def test_grouped_m_zero_zeroes_dw(eng):
     assert torch.all(dw == 0)
     h = eng.handle
     assert bi.bi_grouped_forward(h, z, z, z, ids, 1, k, n, 0, "bf16", None, 1) == bi.BI_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+def test_grouped_tc_tile_edges_exact(eng, dtype):
+    """Expert row counts on the tensor-core tiling's edges (0, 1, 63/64/65 around
+    the 64-row contraction block, 255/256/257 around the 256-row tile, more than
+    two tiles), rows shuffled (id path) and grouped (segmented path), with
+    padding rows: small integers, so every pass must equal the oracle bit for bit."""
+    counts = np.array([0, 1, 63, 64, 65, 255, 256, 257, 577, 130])
+    e, npad, k, n = len(counts), 37, 136, 200
+    m = int(counts.sum()) + npad
+    rng = np.random.default_rng(71)
+    grouped_ids = np.concatenate([np.repeat(np.arange(e), counts), np.full(npad, e + 3)]).astype(np.uint32)
+    shuffled_ids = grouped_ids[rng.permutation(m)]
+    x = synth.small_ints((m, k), -8, 8, dtype, 72)
+    w = synth.small_ints((e, n, k), -8, 8, dtype, 73)
+    dy = synth.small_ints((m, n), -8, 8, dtype, 74)
+    xn, wn, dyn = (synth.to_np(t) for t in (x, w, dy))
+    tdt = synth.TORCH_DTYPES[dtype]
+    for idn in (shuffled_ids, grouped_ids):
+        y, dx, dw = run_grouped(eng, x, w, dy, torch.from_numpy(idn.astype(np.int64)), m, k, n, e, dtype, tc=1)
+        assert np.array_equal(y, oracle.grouped_forward(xn, wn, idn, m, k, n, e, dtype))
+        assert np.array_equal(dx, oracle.grouped_dinput(wn, dyn, idn, m, k, n, e, dtype))
+        assert np.array_equal(dw, oracle.grouped_dweights(xn, dyn, idn, m, k, n, e, dtype))
+        assert np.all(dw[0] == 0)
+    # the segmented entry points on the grouped rows
+    offs = torch.from_numpy(np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)).cuda()
+    X, W, DY = dev(x), dev(w), dev(dy)
+    Y = torch.empty(m, n, dtype=tdt, device="cuda")
+    DX = torch.empty(m, k, dtype=tdt, device="cuda")
+    DW = torch.empty(e, n, k, dtype=torch.float32, device="cuda")
+    eng.grouped_forward_segmented(Y, X, W, offs, m, k, n, e, dtype, None, bi.BI_STRATEGY_TENSOR_CORE)
+    eng.grouped_backward_segmented(DX, DW, X, W, DY, offs, m, k, n, e, dtype, None, bi.BI_STRATEGY_TENSOR_CORE)
+    eng.check()
+    assert np.array_equal(out_np(Y), oracle.grouped_forward(xn, wn, grouped_ids, m, k, n, e, dtype))
+    assert np.array_equal(out_np(DX), oracle.grouped_dinput(wn, dyn, grouped_ids, m, k, n, e, dtype))
+    assert np.array_equal(out_np(DW), oracle.grouped_dweights(xn, dyn, grouped_ids, m, k, n, e, dtype))
