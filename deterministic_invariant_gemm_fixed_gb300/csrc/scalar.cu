@@ -12,9 +12,13 @@
 //
 // Tiling: a 256-thread CTA computes a 128 x 128 output tile; each thread owns
 // 8 x 8 outputs (rows {4ty..4ty+3, 64+4ty..}, cols {4tx.., 64+4tx..}) and keeps
-// their accumulators in registers.  Operands are loaded with 16-byte vector
-// loads (when sizes and alignment allow), widened, and staged through a double
-// buffer in shared memory, 16 contraction steps at a time.
+// their accumulators in registers, as pairs of adjacent columns: the paired
+// FP32 FMA (fma.rn.f32x2) performs two independent round-to-nearest fmaf on
+// the two lanes, so each accumulator still follows its own chain while the
+// instruction count halves.  Operands are loaded with 16-byte vector loads
+// (when sizes and alignment allow), widened, and staged through a double
+// buffer in shared memory, 16 contraction steps at a time; every A value is
+// stored twice, so one 16-byte shared load gives two (a, a) lane pairs.
 //
 // dW reduction over rows (the weight gradient): rows are cut into chunks of
 // BI_DW_CHUNK rows from row 0 (per expert, from the expert's first row, for the
@@ -68,33 +72,93 @@ __device__ __forceinline__ void load8(const T* p, int avail, float (&v)[8]) {
     }
 }
 
-// Shared tile: s[l][i] with l the contraction step, i the row or column.
+// Shared tile: s[l][i] with l the contraction step, i the row or column; A
+// holds each value twice (a[l][2r] = a[l][2r+1] = A value of tile row r).
 template <int TMV>
 struct SmemT {
-    float a[2][TK][TMV + PAD];
+    float a[2][TK][2 * TMV + PAD];
     float b[2][TK][TN + PAD];
 };
 using Smem = SmemT<TM>;
 
-// 8x8 micro-tile product over one staged block: acc[i][j] chains over l ascending.
+// acc = (fmaf(a.lo, b.lo, acc.lo), fmaf(a.hi, b.hi, acc.hi)), each rounded to nearest.
+__device__ __forceinline__ void fma2(uint64_t& acc, uint64_t a, uint64_t b) {
+    asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc) : "l"(a), "l"(b));
+}
+// Accumulator (i, j) of a thread: lane j % 2 of pair acc[i][j / 2].
+__device__ __forceinline__ float acc_lane(const uint64_t (&acc)[8][4], int i, int j) {
+    const uint64_t v = acc[i][j >> 1];
+    return __uint_as_float(static_cast<uint32_t>((j & 1) ? (v >> 32) : v));
+}
+
+// ------------------------------------------------------------------ cp.async staging
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+// 16-byte global -> shared copy; src_bytes = 0 writes zeros (src is not read).
+__device__ __forceinline__ void cp_async16(void* dst, const void* src, uint32_t src_bytes) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_addr(dst)), "l"(src), "r"(src_bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
+// One block of the operands as they lie in global memory (raw element type),
+// filled by cp.async: A rows of TK elements, B as TK rows of TN columns, or
+// (BT) TN columns of TK elements; every row padded by 16 bytes, which keeps
+// the widening reads conflict-free.
+template <typename T, int TMV, bool BT>
+struct RawT {
+    static constexpr int PADE = 16 / sizeof(T);
+    T a[TMV][TK + PADE];
+    T b[BT ? TN : TK][(BT ? TK : TN) + PADE];
+};
+constexpr int RAW_STAGES = 3;
+// dW: both operands are [rows][out] with out contiguous: TK rows of TM / TN outs.
+template <typename T>
+struct RawDwT {
+    static constexpr int PADE = 16 / sizeof(T);
+    T a[TK][TM + PADE];
+    T b[TK][TN + PADE];
+};
+
+// 8 consecutive raw elements from shared memory, widened (p 16-byte aligned).
+template <typename T>
+__device__ __forceinline__ void smem_load8(const T* p, float (&v)[8]) {
+    if (sizeof(T) == 4) {
+        const float4 a = reinterpret_cast<const float4*>(p)[0];
+        const float4 b = reinterpret_cast<const float4*>(p)[1];
+        v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+        v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+    } else {
+        const uint4 a = *reinterpret_cast<const uint4*>(p);
+        const T* h = reinterpret_cast<const T*>(&a);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) v[i] = Elem<T>::up(h[i]);
+    }
+}
+
+// 8x8 micro-tile product over one staged block: each accumulator (i, j)
+// chains over l ascending; pair q of row i holds columns 2q and 2q+1.
 template <int TMV = TM>
-__device__ __forceinline__ void mma_block(const float (*as)[TMV + PAD], const float (*bs)[TN + PAD],
-                                          int ty, int tx, float (&acc)[8][8]) {
+__device__ __forceinline__ void mma_block(const float (*as)[2 * TMV + PAD], const float (*bs)[TN + PAD],
+                                          int ty, int tx, uint64_t (&acc)[8][4]) {
 #pragma unroll
     for (int l = 0; l < TK; ++l) {
-        float a[8], b[8];
-        const float4 a0 = *reinterpret_cast<const float4*>(&as[l][ty * 4]);
-        const float4 a1 = *reinterpret_cast<const float4*>(&as[l][TMV / 2 + ty * 4]);
-        const float4 b0 = *reinterpret_cast<const float4*>(&bs[l][tx * 4]);
-        const float4 b1 = *reinterpret_cast<const float4*>(&bs[l][64 + tx * 4]);
-        a[0] = a0.x; a[1] = a0.y; a[2] = a0.z; a[3] = a0.w;
-        a[4] = a1.x; a[5] = a1.y; a[6] = a1.z; a[7] = a1.w;
-        b[0] = b0.x; b[1] = b0.y; b[2] = b0.z; b[3] = b0.w;
-        b[4] = b1.x; b[5] = b1.y; b[6] = b1.z; b[7] = b1.w;
+        const ulonglong2 a0 = *reinterpret_cast<const ulonglong2*>(&as[l][ty * 8]);
+        const ulonglong2 a1 = *reinterpret_cast<const ulonglong2*>(&as[l][ty * 8 + 4]);
+        const ulonglong2 a2 = *reinterpret_cast<const ulonglong2*>(&as[l][TMV + ty * 8]);
+        const ulonglong2 a3 = *reinterpret_cast<const ulonglong2*>(&as[l][TMV + ty * 8 + 4]);
+        const ulonglong2 b0 = *reinterpret_cast<const ulonglong2*>(&bs[l][tx * 4]);
+        const ulonglong2 b1 = *reinterpret_cast<const ulonglong2*>(&bs[l][64 + tx * 4]);
+        const uint64_t a[8] = {a0.x, a0.y, a1.x, a1.y, a2.x, a2.y, a3.x, a3.y};
+        const uint64_t b[4] = {b0.x, b0.y, b1.x, b1.y};
 #pragma unroll
         for (int i = 0; i < 8; ++i)
 #pragma unroll
-            for (int j = 0; j < 8; ++j) acc[i][j] = __fmaf_rn(a[i], b[j], acc[i][j]);
+            for (int q = 0; q < 4; ++q) fma2(acc[i][q], a[i], b[q]);
     }
 }
 
@@ -118,10 +182,11 @@ struct RowsArgs {
 // out[r, c] = down( chain_l a[r, l] * b(l, c) (+ bias[c]) )
 // TMV = tile height (128 or 64); 2*TMV threads, each owning 8 x 8 outputs.
 template <typename T, bool BT, bool GROUPED, bool VEC, int TMV>
-__global__ void __launch_bounds__(2 * TMV, TMV == 128 ? 2 : 4) scalar_rows_kernel(const RowsArgs p) {
+__global__ void __launch_bounds__(2 * TMV, TMV == 128 ? 1 : (VEC ? 4 : 3)) scalar_rows_kernel(const RowsArgs p) {
     constexpr int NTV = 2 * TMV;
     constexpr int SL = (TK * TN) / (NTV * 8);  // 8-element B slots per thread
-    __shared__ __align__(16) SmemT<TMV> sm;
+    extern __shared__ __align__(16) uint8_t smem_rows[];
+    SmemT<TMV>& sm = *reinterpret_cast<SmemT<TMV>*>(smem_rows);
     const int tid = threadIdx.x, ty = tid / 16, tx = tid % 16;
     const T* A = static_cast<const T*>(p.a);
     const T* B = static_cast<const T*>(p.b);
@@ -181,7 +246,8 @@ __global__ void __launch_bounds__(2 * TMV, TMV == 128 ? 2 : 4) scalar_rows_kerne
     };
     auto store = [&](int buf) {
 #pragma unroll
-        for (int i = 0; i < 8; ++i) sm.a[buf][a_seg + i][a_row] = ra[i];
+        for (int i = 0; i < 8; ++i)
+            *reinterpret_cast<float2*>(&sm.a[buf][a_seg + i][2 * a_row]) = make_float2(ra[i], ra[i]);
 #pragma unroll
         for (int q = 0; q < SL; ++q) {
             const int e = tid + q * NTV;
@@ -197,23 +263,122 @@ __global__ void __launch_bounds__(2 * TMV, TMV == 128 ? 2 : 4) scalar_rows_kerne
         }
     };
 
-    float acc[8][8];
+    uint64_t acc[8][4];  // +0.0f in both lanes
 #pragma unroll
     for (int i = 0; i < 8; ++i)
 #pragma unroll
-        for (int j = 0; j < 8; ++j) acc[i][j] = 0.0f;
+        for (int q = 0; q < 4; ++q) acc[i][q] = 0;
 
     const int64_t nkb = (L + TK - 1) / TK;
-    load_a(0); load_b(0); store(0);
-    __syncthreads();
-    int buf = 0;
-    for (int64_t kb = 0; kb < nkb; ++kb) {
-        const bool more = kb + 1 < nkb;
-        if (more) { load_a((kb + 1) * TK); load_b((kb + 1) * TK); }
-        mma_block<TMV>(sm.a[buf], sm.b[buf], ty, tx, acc);
-        if (more) store(buf ^ 1);
+    if constexpr (VEC) {
+        // cp.async ring of RAW_STAGES raw blocks; block kb+1 is widened into the
+        // f32 tiles while block kb is multiplied (one barrier per block)
+        using Raw = RawT<T, TMV, BT>;
+        Raw* raw = reinterpret_cast<Raw*>(smem_rows + sizeof(SmemT<TMV>));
+        constexpr int EPC = 16 / static_cast<int>(sizeof(T));  // elements per 16-byte chunk
+        constexpr int ACPR = TK / EPC;                         // A chunks per row
+        constexpr int ACH = TMV * ACPR;
+        constexpr int AQ = (ACH + NTV - 1) / NTV;
+        constexpr int BCH = TK * TN / EPC;
+        constexpr int BQ = BCH / NTV;
+        int64_t a_src[AQ];  // source row of this thread's A chunks, or -1
+#pragma unroll
+        for (int q = 0; q < AQ; ++q) {
+            const int e = tid + q * NTV, row = e / ACPR;
+            a_src[q] = -1;
+            if (e < ACH && row < rvalid) a_src[q] = GROUPED ? static_cast<int64_t>(p.perm[sbase + row]) : r0 + row;
+        }
+        auto issue = [&](int64_t kb, int slot) {
+            if (kb < nkb) {
+                const int64_t l0 = kb * TK;
+                Raw& r = raw[slot];
+#pragma unroll
+                for (int q = 0; q < AQ; ++q) {
+                    const int e = tid + q * NTV;
+                    if (e < ACH) {
+                        const int row = e / ACPR, ch = e % ACPR;
+                        const int64_t l = l0 + ch * EPC;
+                        const bool ok = a_src[q] >= 0 && l < L;
+                        cp_async16(&r.a[row][ch * EPC], ok ? static_cast<const void*>(A + a_src[q] * L + l) : A,
+                                   ok ? 16u : 0u);
+                    }
+                }
+#pragma unroll
+                for (int q = 0; q < BQ; ++q) {
+                    const int e = tid + q * NTV;
+                    if (BT) {  // column c: TK elements of B[c * L + l]
+                        const int c = e / ACPR, ch = e % ACPR;
+                        const int64_t gc = c0 + c, l = l0 + ch * EPC;
+                        const bool ok = gc < C && l < L;
+                        cp_async16(&r.b[c][ch * EPC], ok ? static_cast<const void*>(B + gc * L + l) : B, ok ? 16u : 0u);
+                    } else {   // step l: TN elements of B[l * C + c]
+                        constexpr int CPR = TN / EPC;
+                        const int l = e / CPR, ch = e % CPR;
+                        const int64_t gl = l0 + l, gc = c0 + ch * EPC;
+                        const bool ok = gl < L && gc < C;
+                        cp_async16(&r.b[l][ch * EPC], ok ? static_cast<const void*>(B + gl * C + gc) : B, ok ? 16u : 0u);
+                    }
+                }
+            }
+            cp_async_commit();  // an empty group past the end keeps the count uniform
+        };
+        auto widen = [&](int slot, int buf) {
+            const Raw& r = raw[slot];
+            {   // A: row a_row, steps a_seg..a_seg+7, each value stored twice
+                float v[8];
+                smem_load8<T>(&r.a[a_row][a_seg], v);
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    *reinterpret_cast<float2*>(&sm.a[buf][a_seg + i][2 * a_row]) = make_float2(v[i], v[i]);
+            }
+            constexpr int EB = TK * TN / NTV;  // B elements per thread (8 or 16)
+            if (BT) {  // column c, steps lseg..lseg+EB-1, transposed into sm.b[l][c]
+                const int c = tid % TN, lseg = (tid / TN) * EB;
+#pragma unroll
+                for (int h = 0; h < EB; h += 8) {
+                    float v[8];
+                    smem_load8<T>(&r.b[c][lseg + h], v);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) sm.b[buf][lseg + h + i][c] = v[i];
+                }
+            } else {   // step l, columns cseg..cseg+EB-1
+                const int l = tid / (TN / EB), cseg = (tid % (TN / EB)) * EB;
+#pragma unroll
+                for (int h = 0; h < EB; h += 8) {
+                    float v[8];
+                    smem_load8<T>(&r.b[l][cseg + h], v);
+                    *reinterpret_cast<float4*>(&sm.b[buf][l][cseg + h]) = make_float4(v[0], v[1], v[2], v[3]);
+                    *reinterpret_cast<float4*>(&sm.b[buf][l][cseg + h + 4]) = make_float4(v[4], v[5], v[6], v[7]);
+                }
+            }
+        };
+        static_assert(RAW_STAGES == 3, "the waits below assume three raw stages");
+        issue(0, 0);
+        issue(1, 1);
+        cp_async_wait<1>();
         __syncthreads();
-        buf ^= 1;
+        widen(0, 0);
+        issue(2, 2);
+        for (int64_t kb = 0; kb < nkb; ++kb) {
+            cp_async_wait<1>();  // block kb+1 has landed (this thread's copies)
+            __syncthreads();     // ... everyone's; block kb widened; tiles of kb-1 no longer read
+            if (kb + 1 < nkb) widen(static_cast<int>((kb + 1) % RAW_STAGES), static_cast<int>((kb + 1) & 1));
+            issue(kb + RAW_STAGES, static_cast<int>(kb % RAW_STAGES));  // block kb's slot, already widened
+            mma_block<TMV>(sm.a[kb & 1], sm.b[kb & 1], ty, tx, acc);
+        }
+        cp_async_wait<0>();
+    } else {
+        load_a(0); load_b(0); store(0);
+        __syncthreads();
+        int buf = 0;
+        for (int64_t kb = 0; kb < nkb; ++kb) {
+            const bool more = kb + 1 < nkb;
+            if (more) { load_a((kb + 1) * TK); load_b((kb + 1) * TK); }
+            mma_block<TMV>(sm.a[buf], sm.b[buf], ty, tx, acc);
+            if (more) store(buf ^ 1);
+            __syncthreads();
+            buf ^= 1;
+        }
     }
 
     // epilogue: (+ bias), one rounding, store
@@ -228,7 +393,7 @@ __global__ void __launch_bounds__(2 * TMV, TMV == 128 ? 2 : 4) scalar_rows_kerne
         for (int j = 0; j < 8; ++j) {
             const int64_t c = c0 + mrow(tx, j);
             if (c >= C) continue;
-            float v = acc[i][j];
+            float v = acc_lane(acc, i, j);
             if (bias) v = v + Elem<T>::up(bias[c]);
             out[orow * C + c] = Elem<T>::down(v);
         }
@@ -252,7 +417,8 @@ struct DwArgs {
 // partial[z][r][c] = chain over the rows of chunk z of a[m, r] * b[m, c]
 template <typename T, bool GROUPED, bool VEC>
 __global__ void __launch_bounds__(NT, 2) scalar_dw_chunk_kernel(const DwArgs p) {
-    __shared__ __align__(16) Smem sm;
+    extern __shared__ __align__(16) uint8_t smem_dw[];
+    Smem& sm = *reinterpret_cast<Smem*>(smem_dw);
     const int tid = threadIdx.x, ty = tid / 16, tx = tid % 16;
     const T* A = static_cast<const T*>(p.a);
     const T* Bm = static_cast<const T*>(p.b);
@@ -294,21 +460,84 @@ __global__ void __launch_bounds__(NT, 2) scalar_dw_chunk_kernel(const DwArgs p) 
         load8<T, VEC>(A + (av_a ? row * R + r0 + s_ld : 0), av_a, ra);
         load8<T, VEC>(Bm + (av_b ? row * C + c0 + s_ld : 0), av_b, rb);
     };
+    // A doubled: this thread's 64 contiguous bytes as four 16-byte pieces,
+    // written in an order rotated by the thread index so the 16 threads of a
+    // row hit different banks in each store instruction
+    const int rot = tid & 3;
     auto store = [&](int buf) {
-        *reinterpret_cast<float4*>(&sm.a[buf][l_ld][s_ld]) = make_float4(ra[0], ra[1], ra[2], ra[3]);
-        *reinterpret_cast<float4*>(&sm.a[buf][l_ld][s_ld + 4]) = make_float4(ra[4], ra[5], ra[6], ra[7]);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const int c = (q + rot) & 3;
+            const float v0 = c == 0 ? ra[0] : c == 1 ? ra[2] : c == 2 ? ra[4] : ra[6];
+            const float v1 = c == 0 ? ra[1] : c == 1 ? ra[3] : c == 2 ? ra[5] : ra[7];
+            *reinterpret_cast<float4*>(&sm.a[buf][l_ld][2 * s_ld + 4 * c]) = make_float4(v0, v0, v1, v1);
+        }
         *reinterpret_cast<float4*>(&sm.b[buf][l_ld][s_ld]) = make_float4(rb[0], rb[1], rb[2], rb[3]);
         *reinterpret_cast<float4*>(&sm.b[buf][l_ld][s_ld + 4]) = make_float4(rb[4], rb[5], rb[6], rb[7]);
     };
 
-    float acc[8][8];
+    uint64_t acc[8][4];  // +0.0f in both lanes
 #pragma unroll
     for (int i = 0; i < 8; ++i)
 #pragma unroll
-        for (int j = 0; j < 8; ++j) acc[i][j] = 0.0f;
+        for (int q = 0; q < 4; ++q) acc[i][q] = 0;
 
     const int64_t nkb = (cnt + TK - 1) / TK;
-    if (nkb > 0) {
+    if (VEC && nkb > 0) {
+        // cp.async ring of RAW_STAGES raw blocks, as in the rows kernel
+        using Raw = RawDwT<T>;
+        Raw* raw = reinterpret_cast<Raw*>(smem_dw + sizeof(Smem));
+        constexpr int EPC = 16 / static_cast<int>(sizeof(T));
+        constexpr int CPR = TM / EPC;            // chunks per row (TM == TN)
+        constexpr int Q = TK * CPR / NT;         // chunks per thread and operand (1 or 2)
+        auto issue = [&](int64_t kb, int slot) {
+            if (kb < nkb) {
+                Raw& r = raw[slot];
+#pragma unroll
+                for (int q = 0; q < Q; ++q) {
+                    const int e = tid + q * NT, l = e / CPR, ch = e % CPR;
+                    const int64_t lr = kb * TK + l;
+                    int64_t row = -1;
+                    if (lr < cnt) row = GROUPED ? static_cast<int64_t>(p.perm[pos0 + lr]) : pos0 + lr;
+                    const int64_t ca = r0 + ch * EPC, cb = c0 + ch * EPC;
+                    const bool oka = row >= 0 && ca < R, okb = row >= 0 && cb < C;
+                    cp_async16(&r.a[l][ch * EPC], oka ? static_cast<const void*>(A + row * R + ca) : A, oka ? 16u : 0u);
+                    cp_async16(&r.b[l][ch * EPC], okb ? static_cast<const void*>(Bm + row * C + cb) : Bm, okb ? 16u : 0u);
+                }
+            }
+            cp_async_commit();
+        };
+        const int rot = tid & 3;  // rotated piece order of the doubled A stores (conflict-free)
+        auto widen = [&](int slot, int buf) {
+            const Raw& r = raw[slot];
+            float va[8], vb[8];
+            smem_load8<T>(&r.a[l_ld][s_ld], va);
+            smem_load8<T>(&r.b[l_ld][s_ld], vb);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int c = (q + rot) & 3;
+                const float v0 = c == 0 ? va[0] : c == 1 ? va[2] : c == 2 ? va[4] : va[6];
+                const float v1 = c == 0 ? va[1] : c == 1 ? va[3] : c == 2 ? va[5] : va[7];
+                *reinterpret_cast<float4*>(&sm.a[buf][l_ld][2 * s_ld + 4 * c]) = make_float4(v0, v0, v1, v1);
+            }
+            *reinterpret_cast<float4*>(&sm.b[buf][l_ld][s_ld]) = make_float4(vb[0], vb[1], vb[2], vb[3]);
+            *reinterpret_cast<float4*>(&sm.b[buf][l_ld][s_ld + 4]) = make_float4(vb[4], vb[5], vb[6], vb[7]);
+        };
+        issue(0, 0);
+        issue(1, 1);
+        cp_async_wait<1>();
+        __syncthreads();
+        widen(0, 0);
+        issue(2, 2);
+        for (int64_t kb = 0; kb < nkb; ++kb) {
+            cp_async_wait<1>();
+            __syncthreads();
+            if (kb + 1 < nkb) widen(static_cast<int>((kb + 1) % RAW_STAGES), static_cast<int>((kb + 1) & 1));
+            issue(kb + RAW_STAGES, static_cast<int>(kb % RAW_STAGES));
+            mma_block(sm.a[kb & 1], sm.b[kb & 1], ty, tx, acc);
+        }
+        cp_async_wait<0>();
+    } else if (nkb > 0) {
         load(0); store(0);
         __syncthreads();
         int buf = 0;
@@ -330,12 +559,13 @@ __global__ void __launch_bounds__(NT, 2) scalar_dw_chunk_kernel(const DwArgs p) 
         for (int j = 0; j < 8; ++j) {
             const int64_t c = c0 + mrow(tx, j);
             if (c >= C) continue;
+            const float v = acc_lane(acc, i, j);
             if (p.partials) {
-                p.partials[(z * R + r) * C + c] = acc[i][j];
+                p.partials[(z * R + r) * C + c] = v;
             } else if (p.out_f32) {
-                static_cast<float*>(p.out)[r * C + c] = acc[i][j];
+                static_cast<float*>(p.out)[r * C + c] = v;
             } else {
-                static_cast<T*>(p.out)[r * C + c] = Elem<T>::down(acc[i][j]);
+                static_cast<T*>(p.out)[r * C + c] = Elem<T>::down(v);
             }
         }
     }
@@ -425,6 +655,27 @@ int64_t row_tiles_for(int64_t R, int64_t E, bool grouped, int tm) {
     return (R + tm - 1) / tm + (grouped ? E : 0);
 }
 
+// Dynamic shared memory above the 48 KB default needs each kernel's opt-in,
+// once per kernel (the template argument is the kernel itself).
+template <auto KERN>
+cudaError_t allow_smem(size_t bytes) {
+    static std::once_flag once;
+    static cudaError_t err = cudaSuccess;
+    std::call_once(once, [&] {
+        err = cudaFuncSetAttribute(KERN, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes));
+    });
+    return err;
+}
+
+template <typename T, bool BT, bool G, bool V, int TMV>
+cudaError_t launch_rows(const LaunchCtx& c, dim3 grid, const RowsArgs& a) {
+    const size_t bytes = sizeof(SmemT<TMV>) + (V ? RAW_STAGES * sizeof(RawT<T, TMV, BT>) : 0);
+    const cudaError_t e = allow_smem<scalar_rows_kernel<T, BT, G, V, TMV>>(bytes);
+    if (e != cudaSuccess) return e;
+    scalar_rows_kernel<T, BT, G, V, TMV><<<grid, 2 * TMV, bytes, c.stream>>>(a);
+    return cudaSuccess;
+}
+
 template <typename T, bool BT, bool G>
 cudaError_t rows_t(const LaunchCtx& c, const RowsArgs& a) {
     // 8-element loads need rows of whole 16-byte units and aligned bases
@@ -435,15 +686,15 @@ cudaError_t rows_t(const LaunchCtx& c, const RowsArgs& a) {
     // shape: 64-row tiles when 128-row tiles would leave the SMs under-filled.
     const int64_t col_tiles = (a.C + TN - 1) / TN;
     const bool small = row_tiles_for(a.R, a.E, G, 128) * col_tiles < int64_t(c.sm_count) * 6;
+    cudaError_t e;
     if (small) {
         dim3 grid(static_cast<unsigned>(row_tiles_for(a.R, a.E, G, 64)), static_cast<unsigned>(col_tiles));
-        if (vec) scalar_rows_kernel<T, BT, G, true, 64><<<grid, 128, 0, c.stream>>>(a);
-        else scalar_rows_kernel<T, BT, G, false, 64><<<grid, 128, 0, c.stream>>>(a);
+        e = vec ? launch_rows<T, BT, G, true, 64>(c, grid, a) : launch_rows<T, BT, G, false, 64>(c, grid, a);
     } else {
         dim3 grid(static_cast<unsigned>(row_tiles_for(a.R, a.E, G, 128)), static_cast<unsigned>(col_tiles));
-        if (vec) scalar_rows_kernel<T, BT, G, true, 128><<<grid, 256, 0, c.stream>>>(a);
-        else scalar_rows_kernel<T, BT, G, false, 128><<<grid, 256, 0, c.stream>>>(a);
+        e = vec ? launch_rows<T, BT, G, true, 128>(c, grid, a) : launch_rows<T, BT, G, false, 128>(c, grid, a);
     }
+    if (e != cudaSuccess) return e;
     c.count();
     return cudaGetLastError();
 }
@@ -460,8 +711,12 @@ cudaError_t dw_chunks_t(const LaunchCtx& c, const DwArgs& a, int64_t chunks) {
     const bool vec = aligned16(a.a) && aligned16(a.b) && a.R % unit == 0 && a.C % unit == 0;
     dim3 grid(static_cast<unsigned>((a.C + TN - 1) / TN), static_cast<unsigned>((a.R + TM - 1) / TM),
               static_cast<unsigned>(chunks));
-    if (vec) scalar_dw_chunk_kernel<T, G, true><<<grid, NT, 0, c.stream>>>(a);
-    else scalar_dw_chunk_kernel<T, G, false><<<grid, NT, 0, c.stream>>>(a);
+    const size_t vbytes = sizeof(Smem) + RAW_STAGES * sizeof(RawDwT<T>);
+    const cudaError_t e = vec ? allow_smem<scalar_dw_chunk_kernel<T, G, true>>(vbytes)
+                              : allow_smem<scalar_dw_chunk_kernel<T, G, false>>(sizeof(Smem));
+    if (e != cudaSuccess) return e;
+    if (vec) scalar_dw_chunk_kernel<T, G, true><<<grid, NT, vbytes, c.stream>>>(a);
+    else scalar_dw_chunk_kernel<T, G, false><<<grid, NT, sizeof(Smem), c.stream>>>(a);
     c.count();
     return cudaGetLastError();
 }
