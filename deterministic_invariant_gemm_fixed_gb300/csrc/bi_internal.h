@@ -16,6 +16,7 @@ struct bi_engine_s {
     cudaMemPool_t pool = nullptr;
     int* d_status = nullptr;               // device status word (0 = fine)
     uint64_t wait_limit_ns = 2000000000ull; // bounded device-side waits
+    cudaStream_t side = nullptr;            // engine-owned stream for independent work within a call
     std::atomic<uint64_t> launches{0};
     std::mutex mu;                          // guards last_error
     std::string last_error;

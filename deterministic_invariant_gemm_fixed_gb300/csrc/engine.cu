@@ -166,6 +166,11 @@ bi_status bi_engine_create(int device, bi_engine* out) {
     }
     uint64_t keep = ~uint64_t(0);  // keep freed scratch cached in the pool
     cudaMemPoolSetAttribute(eng->pool, cudaMemPoolAttrReleaseThreshold, &keep);
+    if ((e = cudaStreamCreateWithFlags(&eng->side, cudaStreamNonBlocking)) != cudaSuccess) {
+        cudaMemPoolDestroy(eng->pool);
+        delete eng;
+        return cuda_fail(nullptr, e, "cudaStreamCreateWithFlags");
+    }
     if ((e = cudaMalloc(&eng->d_status, 16)) != cudaSuccess ||
         (e = cudaMemset(eng->d_status, 0, 16)) != cudaSuccess) {
         cudaMemPoolDestroy(eng->pool);
@@ -180,6 +185,7 @@ void bi_engine_destroy(bi_engine eng) {
     if (!eng) return;
     {
         DeviceGuard g(eng->device);
+        if (eng->side) cudaStreamDestroy(eng->side);
         cudaFree(eng->d_status);
         cudaMemPoolDestroy(eng->pool);
     }
@@ -506,7 +512,32 @@ bi_status grouped_backward_impl(bi_engine eng, void* dx, float* dw, const void* 
     float* part = reinterpret_cast<float*>(q);
     cudaError_t err = build_grouping(c, src, m, e, seg, perm, hist);
     const void* dy_sorted = dy;
-    const void* x_sorted = x;
+    const void* x_sorted = sorted_in_place ? x : xs;
+    // The dweights operands that dinput does not use (sorted X, both tail
+    // buffers) are prepared on the engine's side stream while dinput runs;
+    // the caller's stream waits for them before dweights (and before the
+    // scratch is released).  The arithmetic is the same either way.
+    const bool overlap = err == cudaSuccess && tier_dw && dx != nullptr;
+    cudaEvent_t fork = nullptr, join = nullptr;
+    if (overlap) {
+        err = cudaEventCreateWithFlags(&fork, cudaEventDisableTiming);
+        if (err == cudaSuccess) err = cudaEventCreateWithFlags(&join, cudaEventDisableTiming);
+        if (err == cudaSuccess) err = cudaEventRecord(fork, s);
+        if (err == cudaSuccess) err = cudaStreamWaitEvent(eng->side, fork, 0);
+    }
+    auto prepare_dw = [&](const bi::LaunchCtx& cc) {
+        cudaError_t r = cudaSuccess;
+        if (!sorted_in_place) r = bi::gather_sorted(cc, x, m, k, e, seg, perm, xs);
+        if (r == cudaSuccess) r = bi::build_tails(cc, dy, n, e, seg, perm, dyt);
+        if (r == cudaSuccess) r = bi::build_tails(cc, x, k, e, seg, perm, xt);
+        return r;
+    };
+    cudaError_t side_err = cudaSuccess;
+    if (overlap && err == cudaSuccess) {
+        side_err = prepare_dw(ctx(eng, eng->side));
+        const cudaError_t rj = cudaEventRecord(join, eng->side);  // recorded whatever happened above
+        if (side_err == cudaSuccess) side_err = rj;
+    }
     if (err == cudaSuccess && need_dys) {
         err = bi::gather_sorted(c, dy, m, n, e, seg, perm, dys);
         dy_sorted = dys;
@@ -517,14 +548,15 @@ bi_status grouped_backward_impl(bi_engine eng, void* dx, float* dw, const void* 
         if (err == cudaSuccess)
             err = bi::zero_padding_rows(c, dx, k, static_cast<int>(dsize(dtype)), e, seg, perm);
     }
+    if (join) {  // always joined before anything below and before the scratch is freed
+        const cudaError_t rw = cudaStreamWaitEvent(s, join, 0);
+        if (err == cudaSuccess) err = side_err != cudaSuccess ? side_err : rw;
+    }
+    if (fork) cudaEventDestroy(fork);
+    if (join) cudaEventDestroy(join);
     if (err == cudaSuccess) {
         if (tier_dw) {
-            if (!sorted_in_place) {
-                err = bi::gather_sorted(c, x, m, k, e, seg, perm, xs);
-                x_sorted = xs;
-            }
-            if (err == cudaSuccess) err = bi::build_tails(c, dy, n, e, seg, perm, dyt);
-            if (err == cudaSuccess) err = bi::build_tails(c, x, k, e, seg, perm, xt);
+            if (!overlap) err = prepare_dw(c);
             if (err == cudaSuccess)
                 err = bi::tc_grouped_dw(c, dtype, dw, dy_sorted, x_sorted, dyt, xt, m, k, n, e, seg);
         } else {
