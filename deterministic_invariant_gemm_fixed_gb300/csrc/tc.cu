@@ -367,7 +367,8 @@ __device__ __forceinline__ constexpr uint32_t instr_desc_pair() {
 // Accumulators: two 256-column TMEM buffers, so the epilogue of one tile
 // overlaps the MMAs of the next.  The 3xTF32 mode uses both halves of TMEM for
 // one tile instead: hi*hi accumulates in columns 0-255, lo*hi + hi*lo in
-// columns 256-511, and the epilogue adds the two (one rounding).  The tensor
+// columns 256-511, and the epilogue adds the two (one rounding) unless the
+// hi*hi sum is infinite, which then is the result.  The tensor
 // core's accumulation rounding then hits the large sum once per K step rather
 // than three times, and the small sum's rounding is 2^-11 smaller.
 template <int IN, int OUT, bool A_MN, bool B_MN, int MODE>
@@ -577,8 +578,11 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
                 for (int i = 0; i < 16; ++i) f[i] = __uint_as_float(v[i]);
                 if (IN == 3) {
+                    // an infinite hi*hi sum is the result: the cross terms of an
+                    // infinite operand (Inf * lo, with lo = 0 or NaN) carry no value
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) f[i] = __fadd_rn(f[i], __uint_as_float(v2[i]));
+                    for (int i = 0; i < 16; ++i)
+                        if (!isinf(f[i])) f[i] = __fadd_rn(f[i], __uint_as_float(v2[i]));
                     if (p.accum_out) {  // earlier pieces' sum, left by the previous launch
                         const float* prev = static_cast<const float*>(out) + orow * p.ldo + col0 + c0;
 #pragma unroll

@@ -5,7 +5,10 @@
 // subtraction is exact in f32).  Both parts are TF32 values stored as f32, so
 // the tensor core reads them without further loss, and x*y is taken as
 // hi_x*hi_y + hi_x*lo_y + lo_x*hi_y: the dropped lo*lo term and the rounding
-// of lo are each below 2^-21 of |x*y|.
+// of lo are each below 2^-21 of |x*y|.  For x = +-Inf, hi = x and lo = NaN
+// (Inf - Inf); the pair kernel's epilogue then keeps the infinite hi*hi sum
+// and drops the cross terms, so infinities and NaN come out as the plain f32
+// contraction gives them.
 //
 // The tensor cores read the parts K-major (the contraction index contiguous).
 // Operands whose contraction runs down the columns (w in the forward pass, x
