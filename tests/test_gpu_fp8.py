@@ -134,3 +134,30 @@ def test_fp8_argument_checks(eng):
     assert bi.bi_fp8_forward(h, y, z8, z8, None, None, s, 64, 64, 64, "bf16", None) == bi.BI_ERR_INVALID_ARG
     assert bi.bi_fp8_forward(h, y, z8, z8, None, s, s, 64, 64, 64, "bf16", None) == bi.BI_OK
     eng.check()
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16", "f32"])
+def test_quantize_special_values(eng, dtype):
+    """NaN quantizes to the e4m3 NaN code, infinities saturate to +-448, and
+    amax ignores NaN (an infinite input makes amax infinite)."""
+    x = synth.normal((2, 500), 1.0, dtype, 85)
+    flat = x.view(-1)
+    flat[3] = float("nan")
+    flat[10] = float("inf")
+    flat[20] = float("-inf")
+    flat[30] = float("nan")
+    q, amax = quantize(eng, x.cuda(), 1.0)
+    eng.check()
+    want_q, want_amax = oracle.fp8_quantize(synth.to_np(x), dtype, 1.0)
+    got = u8(q).reshape(-1)
+    assert np.array_equal(got, want_q.reshape(-1))
+    assert (got[3] & 0x7F) == 0x7F and (got[30] & 0x7F) == 0x7F
+    assert got[10] == 0x7E and got[20] == 0xFE
+    assert out_np(amax)[0] == want_amax and np.isinf(want_amax)
+    # without the infinities, the NaN inputs leave the maximum finite
+    flat[10] = 0.5
+    flat[20] = -0.5
+    q, amax = quantize(eng, x.cuda(), 1.0)
+    eng.check()
+    want_q, want_amax = oracle.fp8_quantize(synth.to_np(x), dtype, 1.0)
+    assert out_np(amax)[0] == want_amax and np.isfinite(want_amax)
