@@ -29,6 +29,22 @@ enum DeviceStatus : int { DEV_OK = 0, DEV_TIMEOUT_PRODUCER = 1, DEV_TIMEOUT_MMA 
                           DEV_TIMEOUT_EPILOGUE = 3, DEV_TIMEOUT_SELFTEST = 4,
                           DEV_BAD_OFFSETS = 5 };
 
+// One-time setup per device (kernel attributes and occupancy queries belong to
+// a device): value and status of the first call on each device, kept per
+// instantiation of the caller's static.
+constexpr int MAX_DEVICES = 64;
+struct PerDeviceOnce {
+    std::once_flag once[MAX_DEVICES];
+    cudaError_t err[MAX_DEVICES] = {};
+    int value[MAX_DEVICES] = {};
+    template <typename F>  // F(int& value) -> cudaError_t
+    cudaError_t run(int device, F&& f) {
+        if (device < 0 || device >= MAX_DEVICES) return cudaErrorInvalidDevice;
+        std::call_once(once[device], [&] { err[device] = f(value[device]); });
+        return err[device];
+    }
+};
+
 // Everything a kernel launcher needs from the engine.
 struct LaunchCtx {
     bi_engine eng;

@@ -84,6 +84,7 @@ extern "C" bi_status bi_grouped_forward_noalloc(void* y, const void* x, const vo
     DeviceSlot& slot = g_slots[dev];
     std::call_once(slot.once, [&slot, dev] {
         // the current device is `dev`: resolve the array's address on it
+        slot.counters.device = dev;  // per-device kernel set-up is keyed on it
         slot.err = cudaGetSymbolAddress(&slot.scratch, g_noalloc_scratch);
         if (slot.err == cudaSuccess)
             slot.err = cudaDeviceGetAttribute(&slot.sm_count, cudaDevAttrMultiProcessorCount, dev);

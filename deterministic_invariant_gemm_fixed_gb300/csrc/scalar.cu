@@ -656,21 +656,19 @@ int64_t row_tiles_for(int64_t R, int64_t E, bool grouped, int tm) {
 }
 
 // Dynamic shared memory above the 48 KB default needs each kernel's opt-in,
-// once per kernel (the template argument is the kernel itself).
+// once per kernel (the template argument is the kernel itself) and device.
 template <auto KERN>
-cudaError_t allow_smem(size_t bytes) {
-    static std::once_flag once;
-    static cudaError_t err = cudaSuccess;
-    std::call_once(once, [&] {
-        err = cudaFuncSetAttribute(KERN, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes));
+cudaError_t allow_smem(const LaunchCtx& c, size_t bytes) {
+    static PerDeviceOnce setup;
+    return setup.run(c.eng->device, [&](int&) {
+        return cudaFuncSetAttribute(KERN, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes));
     });
-    return err;
 }
 
 template <typename T, bool BT, bool G, bool V, int TMV>
 cudaError_t launch_rows(const LaunchCtx& c, dim3 grid, const RowsArgs& a) {
     const size_t bytes = sizeof(SmemT<TMV>) + (V ? RAW_STAGES * sizeof(RawT<T, TMV, BT>) : 0);
-    const cudaError_t e = allow_smem<scalar_rows_kernel<T, BT, G, V, TMV>>(bytes);
+    const cudaError_t e = allow_smem<scalar_rows_kernel<T, BT, G, V, TMV>>(c, bytes);
     if (e != cudaSuccess) return e;
     scalar_rows_kernel<T, BT, G, V, TMV><<<grid, 2 * TMV, bytes, c.stream>>>(a);
     return cudaSuccess;
@@ -712,8 +710,8 @@ cudaError_t dw_chunks_t(const LaunchCtx& c, const DwArgs& a, int64_t chunks) {
     dim3 grid(static_cast<unsigned>((a.C + TN - 1) / TN), static_cast<unsigned>((a.R + TM - 1) / TM),
               static_cast<unsigned>(chunks));
     const size_t vbytes = sizeof(Smem) + RAW_STAGES * sizeof(RawDwT<T>);
-    const cudaError_t e = vec ? allow_smem<scalar_dw_chunk_kernel<T, G, true>>(vbytes)
-                              : allow_smem<scalar_dw_chunk_kernel<T, G, false>>(sizeof(Smem));
+    const cudaError_t e = vec ? allow_smem<scalar_dw_chunk_kernel<T, G, true>>(c, vbytes)
+                              : allow_smem<scalar_dw_chunk_kernel<T, G, false>>(c, sizeof(Smem));
     if (e != cudaSuccess) return e;
     if (vec) scalar_dw_chunk_kernel<T, G, true><<<grid, NT, vbytes, c.stream>>>(a);
     else scalar_dw_chunk_kernel<T, G, false><<<grid, NT, sizeof(Smem), c.stream>>>(a);

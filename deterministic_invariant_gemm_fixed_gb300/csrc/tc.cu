@@ -698,28 +698,27 @@ cudaError_t launch_pair(const LaunchCtx& c, const CUtensorMap& a, const CUtensor
                         const CUtensorMap* a2 = nullptr, const CUtensorMap* b2 = nullptr, int64_t units = -1) {
     auto kern = tc_gemm_pair_kernel<IN, OUT, A_MN, B_MN, MODE>;
     constexpr int P_SMEM_BYTES = p_smem_bytes(IN);
-    static std::once_flag once;
-    static cudaError_t attr_err = cudaSuccess;
-    static int max_clusters = 0;
+    static PerDeviceOnce setup;  // per device: the shared-memory opt-in and the co-resident clusters
     cudaLaunchAttribute at[1];
     at[0].id = cudaLaunchAttributeClusterDimension;
     at[0].val.clusterDim.x = 2;
     at[0].val.clusterDim.y = 1;
     at[0].val.clusterDim.z = 1;
-    std::call_once(once, [&] {
-        attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, P_SMEM_BYTES);
-        if (attr_err == cudaSuccess) {
-            cudaLaunchConfig_t q = {};
-            q.gridDim = dim3(128);
-            q.blockDim = dim3(THREADS);
-            q.dynamicSmemBytes = P_SMEM_BYTES;
-            q.attrs = at;
-            q.numAttrs = 1;
-            attr_err = cudaOccupancyMaxActiveClusters(&max_clusters, kern, &q);
-            if (attr_err == cudaSuccess && max_clusters < 1) attr_err = cudaErrorInvalidConfiguration;
-        }
+    const cudaError_t attr_err = setup.run(c.eng->device, [&](int& max_clusters) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, P_SMEM_BYTES);
+        if (e != cudaSuccess) return e;
+        cudaLaunchConfig_t q = {};
+        q.gridDim = dim3(128);
+        q.blockDim = dim3(THREADS);
+        q.dynamicSmemBytes = P_SMEM_BYTES;
+        q.attrs = at;
+        q.numAttrs = 1;
+        e = cudaOccupancyMaxActiveClusters(&max_clusters, kern, &q);
+        if (e == cudaSuccess && max_clusters < 1) e = cudaErrorInvalidConfiguration;
+        return e;
     });
     if (attr_err != cudaSuccess) return attr_err;
+    const int max_clusters = setup.value[c.eng->device];
     if (units < 0) units = int64_t((p.num_m + 1) / 2) * p.num_n;
     if (units <= 0) return cudaSuccess;
     p.status = c.status;
