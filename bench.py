@@ -127,6 +127,21 @@ def projections():
     return projs, synth.SEVEN_B_M
 
 
+def max_over_ranks(seconds, dist, device):
+    """The slowest rank's time (all ranks get it); `dist` None on one process."""
+    if dist is None:
+        return seconds
+    import torch
+    t = torch.tensor([seconds], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_value(flops_per_step, steps, world, seconds):
+    """Whole-job TFLOP/s: every rank runs its own replica of the step."""
+    return world * flops_per_step * steps / seconds / 1e12
+
+
 def step_flops():
     projs, m = projections()
     return sum(3 * 2.0 * m * k * n for _, k, n in projs)
@@ -436,12 +451,8 @@ def our_arm(args, rank, world):
         barrier()
     launches = eng.launches() - launches0
     eng.check(stream)
-    elapsed = t0.elapsed_time(t1) / 1e3
-    if dist is not None:
-        tt = torch.tensor([elapsed], device="cuda", dtype=torch.float64)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        elapsed = float(tt.item())
-    value = world * fl_step * args.steps / elapsed / 1e12
+    elapsed = max_over_ranks(t0.elapsed_time(t1) / 1e3, dist, "cuda")
+    value = job_value(fl_step, args.steps, world, elapsed)
 
     # per-pass kernel times
     per = {}
@@ -518,12 +529,8 @@ def our_arm(args, rank, world):
     s1.synchronize()
     torch.cuda.synchronize()
     barrier()
-    e2e_t = s0.elapsed_time(s1) / 1e3
-    if dist is not None:
-        tt = torch.tensor([e2e_t], device="cuda", dtype=torch.float64)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        e2e_t = float(tt.item())
-    e2e_value = world * fl_step * e2e_steps / e2e_t / 1e12
+    e2e_t = max_over_ranks(s0.elapsed_time(s1) / 1e3, dist, "cuda")
+    e2e_value = job_value(fl_step, e2e_steps, world, e2e_t)
 
     sec = None
     if rank == 0 and not args.no_secondary:

@@ -1,0 +1,56 @@
+"""The bench's multi-rank path on CPU: gloo ranks for the max-over-ranks
+timing and the whole-job value, and the reference arm under torchrun with two
+ranks (rank 0 prints the only line, rank 1 exits without work)."""
+import json
+import os
+import socket
+import subprocess
+import sys
+
+import pytest
+import torch.multiprocessing as mp
+
+from conftest import ROOT
+
+
+def free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank(rank, world, port, out_dir):
+    import torch.distributed as dist
+    sys.path.insert(0, ROOT)
+    import bench
+    dist.init_process_group("gloo", init_method=f"tcp://127.0.0.1:{port}", rank=rank, world_size=world)
+    t = bench.max_over_ranks(0.5 + rank, dist, "cpu")  # rank 1 is the slow one
+    v = bench.job_value(7.7e12, 3, world, t)
+    dist.barrier()
+    dist.destroy_process_group()
+    with open(os.path.join(out_dir, f"r{rank}.json"), "w") as f:
+        json.dump({"t": t, "v": v}, f)
+
+
+def test_max_over_ranks_and_job_value_with_gloo(tmp_path):
+    world, port = 2, free_port()
+    mp.start_processes(_rank, args=(world, port, str(tmp_path)), nprocs=world, join=True, start_method="spawn")
+    res = [json.load(open(tmp_path / f"r{r}.json")) for r in range(world)]
+    for r in res:
+        assert r["t"] == 1.5
+        assert r["v"] == pytest.approx(world * 7.7e12 * 3 / 1.5 / 1e12)
+
+
+def test_reference_arm_under_torchrun_two_ranks():
+    port = free_port()
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node=2",
+           "--master-addr", "127.0.0.1", "--master-port", str(port),
+           os.path.join(ROOT, "bench.py"), "--impl", "reference", "--gpus", "2", "--steps", "1", "--warmup", "1"]
+    env = dict(os.environ, OMP_NUM_THREADS="4")
+    r = subprocess.run(cmd, capture_output=True, text=True, timeout=600, cwd=ROOT, env=env)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [l for l in r.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1
+    line = json.loads(lines[0])
+    assert line["impl"] == "reference" and line["n_gpus"] == 2 and line["value"] > 0
+    assert line["cpu_baseline"]["kind"] == "oracle"
