@@ -373,6 +373,26 @@ def secondary(eng, stream, reps=5):
     out["tf32x3_f32_o"] = {"workload": "f32 o-projection 8192x4096x4096 fwd+dX+dW, 3xTF32", "tflops": v32,
                            "ceiling_tflops": tf32_ceiling, "frac": v32 / tf32_ceiling}
     del X, W, DY, Yf, DXf, DWf
+    # f16 edge shapes: N = 48 (the scalar fallback: an output dimension < 64) and
+    # the ragged 1000^3 on the tensor-core tier; fwd + dX + dW (f32 dW) each
+    for name, m, k, n in synth.F16_EDGE[:2]:
+        x, w, dy, b = synth.dense_inputs(m, k, n, "f16", x=("uniform", 1.0), w=("uniform", 1.0),
+                                         dy=("uniform", 1.0), b=("uniform", 1.0))
+        X, W, DY, B = x.cuda(), w.cuda(), dy.cuda(), b.cuda()
+        Y = torch.empty(m, n, dtype=torch.float16, device="cuda")
+        DX = torch.empty(m, k, dtype=torch.float16, device="cuda")
+        DW = torch.empty(k, n, dtype=torch.float32, device="cuda")
+        tc = 0 if n < 64 else 1
+
+        def edge_step():
+            eng.forward(Y, X, W, B, m, k, n, "f16", stream, tc)
+            eng.backward_dx(DX, DY, W, m, k, n, "f16", stream, tc)
+            eng.backward_dw(DW, 1, X, DY, m, k, n, "f16", stream, tc)
+        te = timeit(edge_step)
+        moved = 2 * (X.nbytes + W.nbytes + DY.nbytes) + Y.nbytes + DX.nbytes + DW.nbytes  # each pass reads two operands
+        out["f16_" + name] = {"workload": f"f16 {m}x{k}x{n} fwd+dX+dW ({'scalar' if tc == 0 else 'tensor-core'} tier)",
+                              "tflops": 3 * 2.0 * m * k * n / te / 1e12, "gbs": moved / te / 1e9, "us": te * 1e6}
+        del X, W, DY, B, Y, DX, DW
     # GEMV f16 1x4096x4096, tensor-core tier (HBM-bound): W rotated over 8 copies > L2
     k = n = 4096
     ws = [synth.uniform((k, n), -1, 1, "f16", 100 + i).cuda() for i in range(8)]

@@ -400,6 +400,95 @@ __global__ void __launch_bounds__(2 * TMV, TMV == 128 ? 1 : (VEC ? 4 : 3)) scala
     }
 }
 
+// ------------------------------------------------------------------ narrow rows kernel
+
+// Outputs at most 64 columns wide (an output dimension below the tensor-core
+// threshold): 16 x 64 tiles on 256 threads, 2 x 2 outputs per thread, so a
+// narrow output still spreads over many CTAs.  Same chains as above: each
+// output is fmaf over l ascending from +0 (paired FMA lanes), then (+ bias)
+// and one rounding.  Dense only.
+constexpr int NW_TM = 16, NW_TN = 64, NW_TK = 32;
+
+template <typename T, bool BT>
+__global__ void __launch_bounds__(256) scalar_rows_narrow_kernel(const RowsArgs p) {
+    __shared__ __align__(16) float as[2][NW_TK][2 * NW_TM + 4];  // A doubled: [l][2r], [l][2r+1]
+    __shared__ __align__(16) float bs[2][NW_TK][NW_TN + 4];
+    const int tid = threadIdx.x, ty = tid >> 5, tx = tid & 31;  // rows 2ty, 2ty+1; cols 2tx, 2tx+1
+    const T* A = static_cast<const T*>(p.a);
+    const T* B = static_cast<const T*>(p.b);
+    const int64_t L = p.L, C = p.C;
+    const int64_t r0 = static_cast<int64_t>(blockIdx.x) * NW_TM;
+    const int64_t rvalid = lmin(NW_TM, p.R - r0);
+    // staging: A 16 rows x 32 steps (2 per thread), B 32 steps x 64 cols (8 per thread)
+    const int a_row = tid >> 4, a_l = (tid & 15) * 2;
+    const int b_i = BT ? (tid >> 2) : (tid >> 3);              // BT: column; else step
+    const int b_j = BT ? (tid & 3) * 8 : (tid & 7) * 8;        // BT: first step; else first column
+    float ra[2], rb[8];
+    auto load = [&](int64_t l0) {
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            const int64_t l = l0 + a_l + i;
+            ra[i] = (a_row < rvalid && l < L) ? Elem<T>::up(A[(r0 + a_row) * L + l]) : 0.0f;
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            if (BT) {  // b(l, c) = B[c * L + l]
+                const int64_t c = b_i, l = l0 + b_j + i;
+                rb[i] = (c < C && l < L) ? Elem<T>::up(B[c * L + l]) : 0.0f;
+            } else {   // b(l, c) = B[l * C + c]
+                const int64_t l = l0 + b_i, c = b_j + i;
+                rb[i] = (l < L && c < C) ? Elem<T>::up(B[l * C + c]) : 0.0f;
+            }
+        }
+    };
+    auto store = [&](int buf) {
+#pragma unroll
+        for (int i = 0; i < 2; ++i)
+            *reinterpret_cast<float2*>(&as[buf][a_l + i][2 * a_row]) = make_float2(ra[i], ra[i]);
+        if (BT) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) bs[buf][b_j + i][b_i] = rb[i];
+        } else {
+            *reinterpret_cast<float4*>(&bs[buf][b_i][b_j]) = make_float4(rb[0], rb[1], rb[2], rb[3]);
+            *reinterpret_cast<float4*>(&bs[buf][b_i][b_j + 4]) = make_float4(rb[4], rb[5], rb[6], rb[7]);
+        }
+    };
+    uint64_t acc[2] = {0, 0};  // rows 2ty, 2ty+1; lanes = cols 2tx, 2tx+1
+    const int64_t nkb = (L + NW_TK - 1) / NW_TK;
+    load(0);
+    store(0);
+    __syncthreads();
+    for (int64_t kb = 0; kb < nkb; ++kb) {
+        const int buf = static_cast<int>(kb & 1);
+        const bool more = kb + 1 < nkb;
+        if (more) load((kb + 1) * NW_TK);
+#pragma unroll
+        for (int l = 0; l < NW_TK; ++l) {
+            const ulonglong2 a = *reinterpret_cast<const ulonglong2*>(&as[buf][l][4 * ty]);
+            const uint64_t b = *reinterpret_cast<const uint64_t*>(&bs[buf][l][2 * tx]);
+            fma2(acc[0], a.x, b);
+            fma2(acc[1], a.y, b);
+        }
+        if (more) store(buf ^ 1);
+        __syncthreads();
+    }
+    T* out = static_cast<T*>(p.out);
+    const T* bias = static_cast<const T*>(p.bias);
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        const int lr = 2 * ty + i;
+        if (lr >= rvalid) continue;
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            const int64_t c = 2 * tx + j;
+            if (c >= C) continue;
+            float v = __uint_as_float(static_cast<uint32_t>(j ? (acc[i] >> 32) : acc[i]));
+            if (bias) v = v + Elem<T>::up(bias[c]);
+            out[(r0 + lr) * C + c] = Elem<T>::down(v);
+        }
+    }
+}
+
 // ------------------------------------------------------------------ dW kernels
 
 struct DwArgs {
@@ -571,6 +660,75 @@ __global__ void __launch_bounds__(NT, 2) scalar_dw_chunk_kernel(const DwArgs p) 
     }
 }
 
+// Chunk chains for outputs at most 64 columns wide: 16 x 64 tiles on 256
+// threads, 2 x 2 outputs per thread, one CTA per (tile, chunk).  Same chains as
+// scalar_dw_chunk_kernel (rows of the chunk ascending from +0).  Dense only.
+template <typename T>
+__global__ void __launch_bounds__(256) scalar_dw_narrow_kernel(const DwArgs p) {
+    __shared__ __align__(16) float as[2][NW_TK][2 * NW_TM + 4];  // A doubled: [l][2r], [l][2r+1]
+    __shared__ __align__(16) float bs[2][NW_TK][NW_TN + 4];
+    const int tid = threadIdx.x, ty = tid >> 5, tx = tid & 31;  // rows 2ty, 2ty+1; cols 2tx, 2tx+1
+    const T* A = static_cast<const T*>(p.a);
+    const T* Bm = static_cast<const T*>(p.b);
+    const int64_t R = p.R, C = p.C;
+    const int64_t r0 = static_cast<int64_t>(blockIdx.x) * NW_TM;
+    const int64_t z = blockIdx.y;
+    const int64_t pos0 = z * BI_DW_CHUNK;
+    const int64_t cnt = lmin(BI_DW_CHUNK, p.M - pos0);
+    // staging of a 32-row block: A [l][16 r] (2 per thread), B [l][64 c] (8 per thread)
+    const int sl = tid >> 3, sa = (tid & 7) * 2, sb = (tid & 7) * 8;
+    float ra[2], rb[8];
+    auto load = [&](int64_t l0) {
+        const bool ok = l0 + sl < cnt;
+        const int64_t row = pos0 + l0 + sl;
+#pragma unroll
+        for (int i = 0; i < 2; ++i)
+            ra[i] = (ok && r0 + sa + i < R) ? Elem<T>::up(A[row * R + r0 + sa + i]) : 0.0f;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) rb[i] = (ok && sb + i < C) ? Elem<T>::up(Bm[row * C + sb + i]) : 0.0f;
+    };
+    auto store = [&](int buf) {
+        *reinterpret_cast<float4*>(&as[buf][sl][2 * sa]) = make_float4(ra[0], ra[0], ra[1], ra[1]);
+        *reinterpret_cast<float4*>(&bs[buf][sl][sb]) = make_float4(rb[0], rb[1], rb[2], rb[3]);
+        *reinterpret_cast<float4*>(&bs[buf][sl][sb + 4]) = make_float4(rb[4], rb[5], rb[6], rb[7]);
+    };
+    uint64_t acc[2] = {0, 0};
+    const int64_t nkb = (cnt + NW_TK - 1) / NW_TK;
+    if (nkb > 0) {
+        load(0);
+        store(0);
+        __syncthreads();
+        for (int64_t kb = 0; kb < nkb; ++kb) {
+            const int buf = static_cast<int>(kb & 1);
+            const bool more = kb + 1 < nkb;
+            if (more) load((kb + 1) * NW_TK);
+#pragma unroll
+            for (int l = 0; l < NW_TK; ++l) {
+                const ulonglong2 a = *reinterpret_cast<const ulonglong2*>(&as[buf][l][4 * ty]);
+                const uint64_t b = *reinterpret_cast<const uint64_t*>(&bs[buf][l][2 * tx]);
+                fma2(acc[0], a.x, b);
+                fma2(acc[1], a.y, b);
+            }
+            if (more) store(buf ^ 1);
+            __syncthreads();
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        const int64_t r = r0 + 2 * ty + i;
+        if (r >= R) continue;
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            const int64_t c = 2 * tx + j;
+            if (c >= C) continue;
+            const float v = __uint_as_float(static_cast<uint32_t>(j ? (acc[i] >> 32) : acc[i]));
+            if (p.partials) p.partials[(z * R + r) * C + c] = v;
+            else if (p.out_f32) static_cast<float*>(p.out)[r * C + c] = v;
+            else static_cast<T*>(p.out)[r * C + c] = Elem<T>::down(v);
+        }
+    }
+}
+
 // The fixed tree over J chunk partials of one output, as a binary counter:
 // after chunk j the counter merges the two newest entries once per trailing
 // zero bit of j+1 (pairs of equal, aligned blocks), and at the end folds the
@@ -727,9 +885,25 @@ unsigned tree_grid(int64_t n, int sm) {
 
 }  // namespace
 
+template <typename T>
+cudaError_t rows_narrow_t(const LaunchCtx& c, const RowsArgs& a, int bt) {
+    const dim3 grid(static_cast<unsigned>((a.R + NW_TM - 1) / NW_TM));
+    if (bt) scalar_rows_narrow_kernel<T, true><<<grid, 256, 0, c.stream>>>(a);
+    else scalar_rows_narrow_kernel<T, false><<<grid, 256, 0, c.stream>>>(a);
+    c.count();
+    return cudaGetLastError();
+}
+
 cudaError_t scalar_rows(const LaunchCtx& c, bi_dtype dt, void* out, const void* a, const void* b,
                         const void* bias, int64_t R, int64_t L, int64_t C, int b_contr_contig) {
     RowsArgs args{out, a, b, bias, R, L, C, 0, nullptr, nullptr};
+    if (C <= NW_TN) {  // narrow output: the tile shape changes no chain
+        switch (dt) {
+            case BI_F32: return rows_narrow_t<float>(c, args, b_contr_contig);
+            case BI_BF16: return rows_narrow_t<__nv_bfloat16>(c, args, b_contr_contig);
+            default: return rows_narrow_t<__half>(c, args, b_contr_contig);
+        }
+    }
     switch (dt) {
         case BI_F32: return rows_dispatch<float>(c, args, b_contr_contig, false);
         case BI_BF16: return rows_dispatch<__nv_bfloat16>(c, args, b_contr_contig, false);
@@ -753,10 +927,21 @@ cudaError_t scalar_dw(const LaunchCtx& c, bi_dtype dt, void* out, int out_f32, c
     const int64_t J = (M + BI_DW_CHUNK - 1) / BI_DW_CHUNK;
     DwArgs args{out, out_f32, J > 1 ? partials : nullptr, a, b, M, R, C, 0, nullptr, nullptr};
     cudaError_t e;
-    switch (dt) {
-        case BI_F32: e = dw_chunks_t<float, false>(c, args, J); break;
-        case BI_BF16: e = dw_chunks_t<__nv_bfloat16, false>(c, args, J); break;
-        default: e = dw_chunks_t<__half, false>(c, args, J); break;
+    if (C <= NW_TN) {  // narrow output: the tile shape changes no chain
+        const dim3 grid(static_cast<unsigned>((R + NW_TM - 1) / NW_TM), static_cast<unsigned>(J));
+        switch (dt) {
+            case BI_F32: scalar_dw_narrow_kernel<float><<<grid, 256, 0, c.stream>>>(args); break;
+            case BI_BF16: scalar_dw_narrow_kernel<__nv_bfloat16><<<grid, 256, 0, c.stream>>>(args); break;
+            default: scalar_dw_narrow_kernel<__half><<<grid, 256, 0, c.stream>>>(args); break;
+        }
+        c.count();
+        e = cudaGetLastError();
+    } else {
+        switch (dt) {
+            case BI_F32: e = dw_chunks_t<float, false>(c, args, J); break;
+            case BI_BF16: e = dw_chunks_t<__nv_bfloat16, false>(c, args, J); break;
+            default: e = dw_chunks_t<__half, false>(c, args, J); break;
+        }
     }
     if (e != cudaSuccess || J <= 1) return e;
     const int64_t RC = R * C;

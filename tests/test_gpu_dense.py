@@ -58,6 +58,7 @@ SCALAR_CASES = [
     ("gemv_f16", "f16", 1, 4096, 4096, ("uniform", 1.0)),
     ("ragged_1000_f16", "f16", 1000, 1000, 1000, ("uniform", 1.0)),
     ("long_dw_chunks_bf16", "bf16", 1500, 64, 72, ("normal", 1.0)),  # 6 chunks, odd tree
+    ("narrow_both_bf16", "bf16", 333, 40, 48, ("normal", 1.0)),  # narrow-output kernel for Y and dX
 ]
 
 
