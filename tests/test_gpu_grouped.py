@@ -214,3 +214,43 @@ def test_grouped_tc_tile_edges_exact(eng, dtype):
     assert np.array_equal(out_np(Y), oracle.grouped_forward(xn, wn, grouped_ids, m, k, n, e, dtype))
     assert np.array_equal(out_np(DX), oracle.grouped_dinput(wn, dyn, grouped_ids, m, k, n, e, dtype))
     assert np.array_equal(out_np(DW), oracle.grouped_dweights(xn, dyn, grouped_ids, m, k, n, e, dtype))
+
+
+@pytest.mark.parametrize("e", [64, 300])
+@pytest.mark.parametrize("tc", [0, 1])
+def test_grouped_many_experts_exact(eng, e, tc):
+    """Many experts, most of them small and some empty (ids drawn from a skewed
+    distribution): exact small-integer problems, both tiers, ids and the
+    segmented entry points, equal to the oracle bit for bit."""
+    m, k, n, dtype = 3000, 128, 136, "bf16"
+    rng = np.random.default_rng(90 + e)
+    raw = np.minimum((rng.pareto(1.2, size=m) * e / 8).astype(np.int64), e + 5)  # skewed, some >= E
+    ids = raw.astype(np.uint32)
+    x = synth.small_ints((m, k), -8, 8, dtype, 91)
+    w = synth.small_ints((e, n, k), -8, 8, dtype, 92)
+    dy = synth.small_ints((m, n), -8, 8, dtype, 93)
+    xn, wn, dyn = (synth.to_np(t) for t in (x, w, dy))
+    want = (oracle.grouped_forward(xn, wn, ids, m, k, n, e, dtype),
+            oracle.grouped_dinput(wn, dyn, ids, m, k, n, e, dtype),
+            oracle.grouped_dweights(xn, dyn, ids, m, k, n, e, dtype))
+    assert (np.bincount(np.minimum(ids, e), minlength=e + 1)[:e] == 0).any()  # empty experts
+    got = run_grouped(eng, x, w, dy, torch.from_numpy(ids.astype(np.int64)), m, k, n, e, dtype, tc=tc)
+    for g_, w_ in zip(got, want):
+        assert np.array_equal(g_, w_)
+    # the same rows grouped by the caller
+    order = np.argsort(np.minimum(ids, e), kind="stable")
+    gids = ids[order]
+    xs, dys = x[torch.from_numpy(order)], dy[torch.from_numpy(order)]
+    counts = np.bincount(np.minimum(gids, e), minlength=e + 1)[:e]
+    offs = torch.from_numpy(np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)).cuda()
+    tdt = synth.TORCH_DTYPES[dtype]
+    Y = torch.empty(m, n, dtype=tdt, device="cuda")
+    DX = torch.empty(m, k, dtype=tdt, device="cuda")
+    DW = torch.empty(e, n, k, dtype=torch.float32, device="cuda")
+    strat = bi.BI_STRATEGY_TENSOR_CORE if tc else bi.BI_STRATEGY_SCALAR
+    eng.grouped_forward_segmented(Y, dev(xs), dev(w), offs, m, k, n, e, dtype, None, strat)
+    eng.grouped_backward_segmented(DX, DW, dev(xs), dev(w), dev(dys), offs, m, k, n, e, dtype, None, strat)
+    eng.check()
+    assert np.array_equal(out_np(Y), want[0][order])
+    assert np.array_equal(out_np(DX), want[1][order])
+    assert np.array_equal(out_np(DW), want[2])
