@@ -101,8 +101,11 @@ cudaError_t segment_from_offsets(const LaunchCtx& c, const uint32_t* offsets, in
 // for the sorted rows of experts 0..E-1 (s < offsets[E]).  build_tails: for each
 // expert g, rows [g*64, g*64+64) of dst hold its sorted rows from the last
 // multiple of 64 on, then zeros.
+// zero_out (nullable): an output [M, zero_C] (16-bit, zero_C a multiple of 8)
+// whose padding rows are zeroed in the same launch.
 cudaError_t gather_sorted(const LaunchCtx& c, const void* src, int64_t M, int64_t L, int64_t E,
-                          const uint32_t* seg, const uint32_t* perm, void* dst);
+                          const uint32_t* seg, const uint32_t* perm, void* dst, void* zero_out = nullptr,
+                          int64_t zero_C = 0);
 cudaError_t build_tails(const LaunchCtx& c, const void* src, int64_t L, int64_t E, const uint32_t* seg,
                         const uint32_t* perm, void* dst);
 // Zero the rows of out [M, C] (element size esize) whose ids are padding.

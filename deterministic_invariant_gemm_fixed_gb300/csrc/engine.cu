@@ -451,8 +451,8 @@ bi_status grouped_forward_impl(bi_engine eng, void* y, const void* x, const void
     if (err == cudaSuccess) {
         if (tier) {
             const void* a = x;
-            if (!sorted_in_place) {
-                err = bi::gather_sorted(c, x, m, k, e, seg, perm, xs);
+            if (!sorted_in_place) {  // the gather also zeroes the padding rows of y
+                err = bi::gather_sorted(c, x, m, k, e, seg, perm, xs, y, n);
                 a = xs;
             }
             if (err == cudaSuccess) err = bi::tc_grouped_rows(c, dtype, 0, y, a, w, m, k, n, e, seg, perm);
@@ -460,7 +460,8 @@ bi_status grouped_forward_impl(bi_engine eng, void* y, const void* x, const void
             err = bi::scalar_rows_grouped(c, dtype, y, x, w, m, k, n, e, 1, seg, perm);
         }
     }
-    if (err == cudaSuccess) err = bi::zero_padding_rows(c, y, n, static_cast<int>(dsize(dtype)), e, seg, perm);
+    if (err == cudaSuccess && !(tier && !sorted_in_place))
+        err = bi::zero_padding_rows(c, y, n, static_cast<int>(dsize(dtype)), e, seg, perm);
     return err == cudaSuccess ? BI_OK : cuda_fail(eng, err, name);
 }
 
@@ -538,14 +539,16 @@ bi_status grouped_backward_impl(bi_engine eng, void* dx, float* dw, const void* 
         const cudaError_t rj = cudaEventRecord(join, eng->side);  // recorded whatever happened above
         if (side_err == cudaSuccess) side_err = rj;
     }
+    // the dY gather also zeroes the padding rows of dx when the tensor cores write dx
+    const bool fused_zero = need_dys && dx && tier_dx;
     if (err == cudaSuccess && need_dys) {
-        err = bi::gather_sorted(c, dy, m, n, e, seg, perm, dys);
+        err = bi::gather_sorted(c, dy, m, n, e, seg, perm, dys, fused_zero ? dx : nullptr, k);
         dy_sorted = dys;
     }
     if (err == cudaSuccess && dx) {
         err = tier_dx ? bi::tc_grouped_rows(c, dtype, 1, dx, dy_sorted, w, m, k, n, e, seg, perm)
                       : bi::scalar_rows_grouped(c, dtype, dx, dy, w, m, n, k, e, 0, seg, perm);
-        if (err == cudaSuccess)
+        if (err == cudaSuccess && !fused_zero)
             err = bi::zero_padding_rows(c, dx, k, static_cast<int>(dsize(dtype)), e, seg, perm);
     }
     if (join) {  // always joined before anything below and before the scratch is freed

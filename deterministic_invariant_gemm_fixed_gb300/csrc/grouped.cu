@@ -169,14 +169,23 @@ __global__ void seg_from_offsets_kernel(const uint32_t* offsets, int64_t M, uint
         perm[r] = static_cast<uint32_t>(r);
 }
 
-// dst row s (s < offsets[E]) = src row perm[s]; one row per block step.
+// dst row s (s < offsets[E]) = src row perm[s]; one row per block step.  With
+// zout, the padding rows (sorted positions offsets[E] .. M) of that output are
+// zeroed too: the grouped GEMM never writes them.
 __global__ void gather_sorted_kernel(const uint4* src, int64_t L16, uint32_t E, const uint32_t* seg,
-                                     const uint32_t* perm, uint4* dst) {
+                                     const uint32_t* perm, uint4* dst, uint4* zout, int64_t Z16) {
     const int64_t rows = seg[E];
-    for (int64_t r = blockIdx.x; r < rows; r += gridDim.x) {
-        const uint4* sp = src + static_cast<int64_t>(perm[r]) * L16;
-        uint4* d = dst + r * L16;
-        for (int64_t i = threadIdx.x; i < L16; i += blockDim.x) d[i] = __ldg(sp + i);
+    const int64_t all = zout ? static_cast<int64_t>(seg[E + 1]) : rows;
+    for (int64_t r = blockIdx.x; r < all; r += gridDim.x) {
+        if (r < rows) {
+            const uint4* sp = src + static_cast<int64_t>(perm[r]) * L16;
+            uint4* d = dst + r * L16;
+            for (int64_t i = threadIdx.x; i < L16; i += blockDim.x) d[i] = __ldg(sp + i);
+        } else {
+            uint4* d = zout + static_cast<int64_t>(perm[r]) * Z16;
+            const uint4 z = make_uint4(0, 0, 0, 0);
+            for (int64_t i = threadIdx.x; i < Z16; i += blockDim.x) d[i] = z;
+        }
     }
 }
 
@@ -281,13 +290,15 @@ cudaError_t segment_from_offsets(const LaunchCtx& c, const uint32_t* offsets, in
 }
 
 cudaError_t gather_sorted(const LaunchCtx& c, const void* src, int64_t M, int64_t L, int64_t E,
-                          const uint32_t* seg, const uint32_t* perm, void* dst) {
+                          const uint32_t* seg, const uint32_t* perm, void* dst, void* zero_out, int64_t zero_C) {
     if (M == 0) return cudaSuccess;
     const int64_t L16 = L * 2 / 16;  // 16-bit data, L a multiple of 8
+    const int64_t Z16 = zero_C * 2 / 16;  // 16-bit output rows, zero_C a multiple of 8
     const int64_t cap = static_cast<int64_t>(c.sm_count) * 16;
     const int64_t blocks = M < cap ? M : cap;
     gather_sorted_kernel<<<static_cast<unsigned>(blocks), 256, 0, c.stream>>>(
-        static_cast<const uint4*>(src), L16, static_cast<uint32_t>(E), seg, perm, static_cast<uint4*>(dst));
+        static_cast<const uint4*>(src), L16, static_cast<uint32_t>(E), seg, perm, static_cast<uint4*>(dst),
+        static_cast<uint4*>(zero_out), Z16);
     c.count();
     return cudaGetLastError();
 }
