@@ -45,6 +45,32 @@ struct PerDeviceOnce {
     }
 };
 
+// Programmatic dependent launch: a kernel launched with launch_pdl may be
+// scheduled while the previous kernel in its stream is still finishing.  It
+// must call grid_dep_wait() before touching global memory (that waits for the
+// previous kernel to complete and its writes to be visible); grid_dep_launch()
+// lets the kernel after it be scheduled early in turn.  Both are no-ops for a
+// kernel launched the ordinary way.
+#ifdef __CUDACC__
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+#endif
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                       Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+}
+
 // Everything a kernel launcher needs from the engine.
 struct LaunchCtx {
     bi_engine eng;

@@ -44,6 +44,8 @@ __device__ __forceinline__ void rank_in_step(const uint32_t* sb, int tid, uint32
 
 __global__ void __launch_bounds__(SEG_THREADS)
     seg_count_kernel(const uint32_t* ids, int64_t M, uint32_t E, uint32_t* hist, int64_t NB) {
+    grid_dep_wait();
+    grid_dep_launch();
     __shared__ uint32_t sb[SEG_THREADS];
     const int64_t b = blockIdx.x;
     const int64_t begin = b * SEG_ROWS_PER_BLOCK;
@@ -81,6 +83,8 @@ __device__ void write_tile_starts(uint32_t* seg, uint32_t E) {
 // prefix sum; seg receives offsets[0..E+1] and the tile starts.
 __global__ void __launch_bounds__(1024)
     seg_scan_kernel(uint32_t* hist, int64_t NB, uint32_t E, int64_t M, uint32_t* seg) {
+    grid_dep_wait();
+    grid_dep_launch();
     __shared__ uint32_t warp_sums[32];
     __shared__ uint32_t carry;
     const int64_t total = (static_cast<int64_t>(E) + 1) * NB;
@@ -122,6 +126,8 @@ __global__ void __launch_bounds__(1024)
 __global__ void __launch_bounds__(SEG_THREADS)
     seg_scatter_kernel(const uint32_t* ids, int64_t M, uint32_t E, uint32_t* base_pos, int64_t NB,
                        uint32_t* perm) {
+    grid_dep_wait();
+    grid_dep_launch();
     __shared__ uint32_t sb[SEG_THREADS];
     const int64_t b = blockIdx.x;
     const int64_t begin = b * SEG_ROWS_PER_BLOCK;
@@ -148,6 +154,8 @@ __global__ void __launch_bounds__(SEG_THREADS)
 // whatever the caller passed.
 __global__ void seg_from_offsets_kernel(const uint32_t* offsets, int64_t M, uint32_t E, uint32_t* seg,
                                         uint32_t* perm, int* status) {
+    grid_dep_wait();
+    grid_dep_launch();
     if (blockIdx.x == 0 && threadIdx.x == 0) {
         const uint32_t m = static_cast<uint32_t>(M);
         bool bad = offsets[0] != 0;
@@ -174,6 +182,8 @@ __global__ void seg_from_offsets_kernel(const uint32_t* offsets, int64_t M, uint
 // zeroed too: the grouped GEMM never writes them.
 __global__ void gather_sorted_kernel(const uint4* src, int64_t L16, uint32_t E, const uint32_t* seg,
                                      const uint32_t* perm, uint4* dst, uint4* zout, int64_t Z16) {
+    grid_dep_wait();
+    grid_dep_launch();
     const int64_t rows = seg[E];
     const int64_t all = zout ? static_cast<int64_t>(seg[E + 1]) : rows;
     for (int64_t r = blockIdx.x; r < all; r += gridDim.x) {
@@ -193,6 +203,8 @@ __global__ void gather_sorted_kernel(const uint4* src, int64_t L16, uint32_t E, 
 // the expert has it, else zeros.
 __global__ void build_tails_kernel(const uint4* src, int64_t L16, uint32_t E, const uint32_t* seg,
                                    const uint32_t* perm, uint4* dst) {
+    grid_dep_wait();
+    grid_dep_launch();
     const int64_t rows = static_cast<int64_t>(E) * GROUPED_TAIL_ROWS;
     for (int64_t q = blockIdx.x; q < rows; q += gridDim.x) {
         const uint32_t g = static_cast<uint32_t>(q / GROUPED_TAIL_ROWS);
@@ -212,6 +224,8 @@ __global__ void build_tails_kernel(const uint4* src, int64_t L16, uint32_t E, co
 
 __global__ void zero_rows_kernel(uint8_t* out, int64_t row_bytes, uint32_t E, const uint32_t* seg,
                                  const uint32_t* perm) {
+    grid_dep_wait();
+    grid_dep_launch();
     const int64_t first = seg[E], end = seg[E + 1];
     for (int64_t s = first + blockIdx.x; s < end; s += gridDim.x) {
         uint8_t* d = out + static_cast<int64_t>(perm[s]) * row_bytes;
@@ -263,16 +277,22 @@ cudaError_t segment(const LaunchCtx& c, const uint32_t* ids, int64_t M, int64_t 
     const int64_t NB = num_seg_blocks(M) > 0 ? num_seg_blocks(M) : 1;
     uint32_t* hist = static_cast<uint32_t*>(scratch);
     if (M > 0) {
-        seg_count_kernel<<<static_cast<unsigned>(NB), SEG_THREADS, 0, c.stream>>>(ids, M, static_cast<uint32_t>(E), hist, NB);
+        const cudaError_t e = launch_pdl(seg_count_kernel, dim3(static_cast<unsigned>(NB)), dim3(SEG_THREADS), 0,
+                                         c.stream, ids, M, static_cast<uint32_t>(E), hist, NB);
+        if (e != cudaSuccess) return e;
         c.count();
     } else {
         cudaError_t e = cudaMemsetAsync(hist, 0, (E + 1) * NB * 4, c.stream);
         if (e != cudaSuccess) return e;
     }
-    seg_scan_kernel<<<1, 1024, 0, c.stream>>>(hist, NB, static_cast<uint32_t>(E), M, seg);
+    cudaError_t e = launch_pdl(seg_scan_kernel, dim3(1), dim3(1024), 0, c.stream, hist, NB, static_cast<uint32_t>(E),
+                               M, seg);
+    if (e != cudaSuccess) return e;
     c.count();
     if (M > 0) {
-        seg_scatter_kernel<<<static_cast<unsigned>(NB), SEG_THREADS, 0, c.stream>>>(ids, M, static_cast<uint32_t>(E), hist, NB, perm);
+        e = launch_pdl(seg_scatter_kernel, dim3(static_cast<unsigned>(NB)), dim3(SEG_THREADS), 0, c.stream, ids, M,
+                       static_cast<uint32_t>(E), hist, NB, perm);
+        if (e != cudaSuccess) return e;
         c.count();
     }
     return cudaGetLastError();
@@ -283,8 +303,9 @@ cudaError_t segment_from_offsets(const LaunchCtx& c, const uint32_t* offsets, in
     int64_t blocks = (M + 255) / 256;
     if (blocks > static_cast<int64_t>(c.sm_count) * 8) blocks = static_cast<int64_t>(c.sm_count) * 8;
     if (blocks < 1) blocks = 1;
-    seg_from_offsets_kernel<<<static_cast<unsigned>(blocks), 256, 0, c.stream>>>(
-        offsets, M, static_cast<uint32_t>(E), seg, perm, c.status);
+    const cudaError_t e = launch_pdl(seg_from_offsets_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0,
+                                     c.stream, offsets, M, static_cast<uint32_t>(E), seg, perm, c.status);
+    if (e != cudaSuccess) return e;
     c.count();
     return cudaGetLastError();
 }
@@ -296,9 +317,10 @@ cudaError_t gather_sorted(const LaunchCtx& c, const void* src, int64_t M, int64_
     const int64_t Z16 = zero_C * 2 / 16;  // 16-bit output rows, zero_C a multiple of 8
     const int64_t cap = static_cast<int64_t>(c.sm_count) * 16;
     const int64_t blocks = M < cap ? M : cap;
-    gather_sorted_kernel<<<static_cast<unsigned>(blocks), 256, 0, c.stream>>>(
-        static_cast<const uint4*>(src), L16, static_cast<uint32_t>(E), seg, perm, static_cast<uint4*>(dst),
-        static_cast<uint4*>(zero_out), Z16);
+    const cudaError_t e = launch_pdl(gather_sorted_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, c.stream,
+                                     static_cast<const uint4*>(src), L16, static_cast<uint32_t>(E), seg, perm,
+                                     static_cast<uint4*>(dst), static_cast<uint4*>(zero_out), Z16);
+    if (e != cudaSuccess) return e;
     c.count();
     return cudaGetLastError();
 }
@@ -309,8 +331,10 @@ cudaError_t build_tails(const LaunchCtx& c, const void* src, int64_t L, int64_t 
     const int64_t rows = E * GROUPED_TAIL_ROWS;
     const int64_t cap = static_cast<int64_t>(c.sm_count) * 16;
     const int64_t blocks = rows < cap ? rows : cap;
-    build_tails_kernel<<<static_cast<unsigned>(blocks), 256, 0, c.stream>>>(
-        static_cast<const uint4*>(src), L16, static_cast<uint32_t>(E), seg, perm, static_cast<uint4*>(dst));
+    const cudaError_t e = launch_pdl(build_tails_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, c.stream,
+                                     static_cast<const uint4*>(src), L16, static_cast<uint32_t>(E), seg, perm,
+                                     static_cast<uint4*>(dst));
+    if (e != cudaSuccess) return e;
     c.count();
     return cudaGetLastError();
 }
@@ -318,8 +342,9 @@ cudaError_t build_tails(const LaunchCtx& c, const void* src, int64_t L, int64_t 
 cudaError_t zero_padding_rows(const LaunchCtx& c, void* out, int64_t C, int esize, int64_t E,
                               const uint32_t* seg, const uint32_t* perm) {
     const unsigned blocks = static_cast<unsigned>(c.sm_count * 4);
-    zero_rows_kernel<<<blocks, 256, 0, c.stream>>>(static_cast<uint8_t*>(out), C * esize,
-                                                  static_cast<uint32_t>(E), seg, perm);
+    const cudaError_t e = launch_pdl(zero_rows_kernel, dim3(blocks), dim3(256), 0, c.stream, static_cast<uint8_t*>(out),
+                                     C * esize, static_cast<uint32_t>(E), seg, perm);
+    if (e != cudaSuccess) return e;
     c.count();
     return cudaGetLastError();
 }

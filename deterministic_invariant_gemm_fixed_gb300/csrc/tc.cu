@@ -431,6 +431,10 @@ __global__ void __launch_bounds__(THREADS, 1)
     cluster_sync();
     tc_fence_after();
     const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
+    // set-up above touches no global memory; everything below may read what
+    // the previous kernel in the stream wrote
+    grid_dep_wait();
+    grid_dep_launch();
 
     if (warp == 0 && lane == 0) {
         // ------------------------------------------------------------ producer (both CTAs)
@@ -729,8 +733,11 @@ cudaError_t launch_pair(const LaunchCtx& c, const CUtensorMap& a, const CUtensor
     cfg.blockDim = dim3(THREADS);
     cfg.dynamicSmemBytes = P_SMEM_BYTES;
     cfg.stream = c.stream;
-    cfg.attrs = at;
-    cfg.numAttrs = 1;
+    cudaLaunchAttribute la[2] = {at[0], {}};
+    la[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // see grid_dep_wait
+    la[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = la;
+    cfg.numAttrs = 2;
     cudaError_t e = cudaLaunchKernelEx(&cfg, kern, a, b, a2 ? *a2 : a, b2 ? *b2 : b, p);
     if (e != cudaSuccess) return e;
     c.count();
