@@ -14,7 +14,9 @@
 // Operands whose contraction runs down the columns (w in the forward pass, x
 // and dy in dW) are transposed by the split itself: it reads every element
 // once and writes both parts once either way, so the transpose costs no extra
-// HBM traffic.
+// HBM traffic.  The transposing split needs rows of x whose length is a
+// multiple of 4 floats and 16-byte aligned buffers (the tensor-core tier's
+// shapes and pointers always are).
 #include "bi_internal.h"
 
 namespace bi {
@@ -36,9 +38,24 @@ __global__ void tf32_split_kernel(const float* x, float* hi, float* lo, int64_t 
     }
 }
 
-// 32 x 32 tiles through shared memory (one padding column: the column-wise
-// reads hit 32 different banks); 32 x 8 threads, each moving 4 elements.
-constexpr int TT = 32;
+// The same, four elements per step with 16-byte loads and stores (all three
+// pointers 16-byte aligned, count a multiple of 4).
+__global__ void tf32_split4_kernel(const float4* x, float4* hi, float4* lo, int64_t count4) {
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < count4; i += stride) {
+        const float4 v = x[i];
+        const float4 h = make_float4(to_tf32(v.x), to_tf32(v.y), to_tf32(v.z), to_tf32(v.w));
+        hi[i] = h;
+        lo[i] = make_float4(to_tf32(__fsub_rn(v.x, h.x)), to_tf32(__fsub_rn(v.y, h.y)), to_tf32(__fsub_rn(v.z, h.z)),
+                            to_tf32(__fsub_rn(v.w, h.w)));
+    }
+}
+
+// Transposing split: 64 x 64 tiles through shared memory (one padding column),
+// 256 threads, each reading four float4 along rows of x and writing four
+// float4 of the parts (four consecutive rows of x for one column).  cols is a
+// multiple of 4; ld (>= rows) a multiple of 4; the bases 16-byte aligned.
+constexpr int TT = 64;
 
 __global__ void __launch_bounds__(256) tf32_split_t_kernel(const float* __restrict__ x, float* __restrict__ hi,
                                                            float* __restrict__ lo, int64_t rows, int64_t cols,
@@ -47,24 +64,40 @@ __global__ void __launch_bounds__(256) tf32_split_t_kernel(const float* __restri
     __shared__ float tl[TT][TT + 1];
     const int64_t tiles_c = (cols + TT - 1) / TT;
     const int64_t tiles = ((rows + TT - 1) / TT) * tiles_c;
-    const int tx = threadIdx.x, ty = threadIdx.y;
+    const int t16 = threadIdx.x & 15, t_hi = threadIdx.x >> 4;  // 16 float4 per 64-element row
     for (int64_t t = blockIdx.x; t < tiles; t += gridDim.x) {
         const int64_t r0 = (t / tiles_c) * TT, c0 = (t % tiles_c) * TT;
-        for (int i = ty; i < TT; i += 8) {
-            const int64_t r = r0 + i, col = c0 + tx;
-            if (r < rows && col < cols) {
-                const float v = x[r * cols + col];
-                const float h = to_tf32(v);
-                th[i][tx] = h;
-                tl[i][tx] = to_tf32(__fsub_rn(v, h));
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {  // x rows r0 + t_hi + 16i, columns c0 + 4 t16 .. +3
+            const int r = t_hi + 16 * i, c = 4 * t16;
+            float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (r0 + r < rows && c0 + c < cols) v = *reinterpret_cast<const float4*>(x + (r0 + r) * cols + c0 + c);
+            const float e[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const float h = to_tf32(e[j]);
+                th[r][c + j] = h;
+                tl[r][c + j] = to_tf32(__fsub_rn(e[j], h));
             }
         }
         __syncthreads();
-        for (int i = ty; i < TT; i += 8) {
-            const int64_t col = c0 + i, r = r0 + tx;  // output row col, column r
-            if (r < rows && col < cols) {
-                hi[col * ld + r] = th[tx][i];
-                lo[col * ld + r] = tl[tx][i];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {  // output row = x column c0 + oc; x rows r0 + 4 t16 .. +3
+            const int oc = t_hi + 16 * i, r = 4 * t16;
+            const int64_t col = c0 + oc, row = r0 + r;
+            if (col < cols && row < rows) {
+                const float4 h = make_float4(th[r][oc], th[r + 1][oc], th[r + 2][oc], th[r + 3][oc]);
+                const float4 l = make_float4(tl[r][oc], tl[r + 1][oc], tl[r + 2][oc], tl[r + 3][oc]);
+                if (row + 4 <= rows) {
+                    *reinterpret_cast<float4*>(hi + col * ld + row) = h;
+                    *reinterpret_cast<float4*>(lo + col * ld + row) = l;
+                } else {  // the last rows of x: the rest of the padded row is never read
+                    const float hv[4] = {h.x, h.y, h.z, h.w}, lv[4] = {l.x, l.y, l.z, l.w};
+                    for (int j = 0; j < 4 && row + j < rows; ++j) {
+                        hi[col * ld + row + j] = hv[j];
+                        lo[col * ld + row + j] = lv[j];
+                    }
+                }
             }
         }
         __syncthreads();
@@ -78,15 +111,25 @@ cudaError_t tf32_split(const LaunchCtx& c, const float* x, float* hi, float* lo,
     const int64_t count = rows * cols;
     if (count == 0) return cudaSuccess;
     const int64_t cap = static_cast<int64_t>(c.sm_count) * 16;
+    const bool a16 = ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(hi) |
+                       reinterpret_cast<uintptr_t>(lo)) & 15u) == 0;
     if (!transpose) {
-        int64_t blocks = (count + 255) / 256;
-        if (blocks > cap) blocks = cap;
-        tf32_split_kernel<<<static_cast<unsigned>(blocks), 256, 0, c.stream>>>(x, hi, lo, count);
+        if (a16 && count % 4 == 0) {
+            int64_t blocks = (count / 4 + 255) / 256;
+            if (blocks > cap) blocks = cap;
+            tf32_split4_kernel<<<static_cast<unsigned>(blocks), 256, 0, c.stream>>>(
+                reinterpret_cast<const float4*>(x), reinterpret_cast<float4*>(hi), reinterpret_cast<float4*>(lo),
+                count / 4);
+        } else {
+            int64_t blocks = (count + 255) / 256;
+            if (blocks > cap) blocks = cap;
+            tf32_split_kernel<<<static_cast<unsigned>(blocks), 256, 0, c.stream>>>(x, hi, lo, count);
+        }
     } else {
-        if (ld < rows) return cudaErrorInvalidValue;
+        if (ld < rows || ld % 4 != 0 || cols % 4 != 0 || !a16) return cudaErrorInvalidValue;
         int64_t blocks = ((rows + TT - 1) / TT) * ((cols + TT - 1) / TT);
         if (blocks > cap) blocks = cap;
-        tf32_split_t_kernel<<<static_cast<unsigned>(blocks), dim3(TT, 8), 0, c.stream>>>(x, hi, lo, rows, cols, ld);
+        tf32_split_t_kernel<<<static_cast<unsigned>(blocks), 256, 0, c.stream>>>(x, hi, lo, rows, cols, ld);
     }
     c.count();
     return cudaGetLastError();
