@@ -734,7 +734,7 @@ __global__ void __launch_bounds__(256) scalar_dw_narrow_kernel(const DwArgs p) {
 // zero bit of j+1 (pairs of equal, aligned blocks), and at the end folds the
 // remaining entries from the newest down.  Same pairs, same operands as the
 // level-by-level pairwise tree with the odd last entry carried.
-__device__ __forceinline__ float tree_from(const float* part, int64_t stride, int64_t J) {
+__device__ __forceinline__ float tree_counter(const float* part, int64_t stride, int64_t J) {
     float st[32];
     int sp = 0;
     for (int64_t j = 0; j < J; ++j) {
@@ -747,6 +747,27 @@ __device__ __forceinline__ float tree_from(const float* part, int64_t stride, in
     float v = sp ? st[sp - 1] : 0.0f;
     for (int i = sp - 2; i >= 0; --i) v = st[i] + v;
     return v;
+}
+
+// The same tree for J <= 32, level by level as defined (adjacent pairs, an odd
+// last entry carried up), with all J partials loaded first and every index
+// fixed at compile time, so the partials stay in registers.
+__device__ __forceinline__ float tree_levels32(const float* part, int64_t stride, int J) {
+    float v[32];
+#pragma unroll
+    for (int j = 0; j < 32; ++j) v[j] = j < J ? part[j * stride] : 0.0f;
+    int n = J;
+#pragma unroll
+    for (int lvl = 0; lvl < 5; ++lvl) {
+#pragma unroll
+        for (int i = 0; i < (16 >> lvl); ++i) v[i] = (2 * i + 1 < n) ? v[2 * i] + v[2 * i + 1] : v[2 * i];
+        n = (n + 1) / 2;
+    }
+    return v[0];
+}
+
+__device__ __forceinline__ float tree_from(const float* part, int64_t stride, int64_t J) {
+    return J <= 32 ? tree_levels32(part, stride, static_cast<int>(J)) : tree_counter(part, stride, J);
 }
 
 template <typename T>

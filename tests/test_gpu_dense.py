@@ -59,6 +59,8 @@ SCALAR_CASES = [
     ("ragged_1000_f16", "f16", 1000, 1000, 1000, ("uniform", 1.0)),
     ("long_dw_chunks_bf16", "bf16", 1500, 64, 72, ("normal", 1.0)),  # 6 chunks, odd tree
     ("narrow_both_bf16", "bf16", 333, 40, 48, ("normal", 1.0)),  # narrow-output kernel for Y and dX
+    ("tree32_f16", "f16", 8192, 64, 72, ("uniform", 1.0)),   # 32 dW chunks: the register tree
+    ("tree33_bf16", "bf16", 8200, 64, 72, ("normal", 1.0)),  # 33 dW chunks: the counter form
 ]
 
 
