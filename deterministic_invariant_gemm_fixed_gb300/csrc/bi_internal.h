@@ -171,6 +171,10 @@ cudaError_t tf32_split(const LaunchCtx& c, const float* x, float* hi, float* lo,
 // piece order: the tensor core's accumulation error grows with the contraction
 // length, and a fixed piece length (independent of the batch) bounds it.
 constexpr int64_t TF32X3_PIECE = 4096;
+// The same for the 16-bit and FP8 tensor-core passes whose result stays f32
+// (dW with dw_f32, the FP8 dW in f32, the grouped dweights): contractions over
+// more rows than this run in pieces of this many rows, summed in order in dW.
+constexpr int64_t TC_PIECE_ROWS = 8192;
 // out[r][c] = sum over pieces (in order) of the piece's sum over d of
 // a[r][d] * b[c][d], + bias[c]; both operands K-major (a: rows x depth, leading
 // dim lda; b: cols x depth, ldb); f32 out, leading dim ldo.

@@ -55,7 +55,8 @@ struct Params {
     int E;
     const float* scale_a;    // FP8: per-tensor scales applied to the f32 product
     const float* scale_b;
-    int accum_out;           // 3xTF32 contraction piece after the first: out += result
+    int accum_out;           // f32 out, a contraction piece after the first: out += result
+    int piece_kb0, piece_kbn;  // grouped dweights: contraction blocks [kb0, kb0 + kbn) of each expert
     int* status;
     unsigned long long wait_limit;
 };
@@ -250,6 +251,7 @@ struct PairTile {
     int row0;     // grouped: first sorted row of the unit (rows) / of the expert (dweights)
     int row_end;  // grouped: end of the expert's sorted rows
     int full_kb;  // dweights: blocks read in place; block full_kb is the tail block
+    int kb0;      // dweights: first contraction block of this piece (others: 0)
 };
 
 template <int MODE>
@@ -269,6 +271,7 @@ __device__ __forceinline__ bool pair_tile(const Params& p, int t, PairTile& u) {
         u.row0 = 0;
         u.row_end = 0;
         u.full_kb = p.num_kb;
+        u.kb0 = 0;
         return true;
     }
     const uint32_t* off = p.seg;            // sorted offsets of buckets 0..E, then m
@@ -288,6 +291,7 @@ __device__ __forceinline__ bool pair_tile(const Params& p, int t, PairTile& u) {
         u.row_end = static_cast<int>(off[lo + 1]);
         u.nkb = p.num_kb;
         u.full_kb = p.num_kb;
+        u.kb0 = 0;
         return true;
     }
     const int per = units_m * p.num_n;
@@ -301,7 +305,9 @@ __device__ __forceinline__ bool pair_tile(const Params& p, int t, PairTile& u) {
     u.row0 = static_cast<int>(off[g]);
     u.row_end = u.row0 + cnt;
     u.full_kb = cnt / BK;
-    u.nkb = (cnt + BK - 1) / BK;
+    const int all_kb = (cnt + BK - 1) / BK;  // this piece: blocks [kb0, kb0 + nkb) of the expert
+    u.kb0 = min(p.piece_kb0, all_kb);
+    u.nkb = min(all_kb, p.piece_kb0 + p.piece_kbn) - u.kb0;
     return true;
 }
 
@@ -452,8 +458,9 @@ __global__ void __launch_bounds__(THREADS, 1)
                 int kofs = kb * BKE;  // contraction coordinate
                 bool tail = false;
                 if (MODE == GROUPED_DW) {  // the expert's rows in place, or its tail block
-                    tail = kb == u.full_kb;
-                    kofs = tail ? u.g * BKE : u.row0 + kofs;
+                    const int kba = u.kb0 + kb;
+                    tail = kba == u.full_kb;
+                    kofs = tail ? u.g * BKE : u.row0 + kba * BKE;
                 }
 #pragma unroll
                 for (int part = 0; part < p_tiles(IN); ++part) {
@@ -559,8 +566,8 @@ __global__ void __launch_bounds__(THREADS, 1)
                 if (MODE == GROUPED_DW) out = static_cast<float*>(p.out) + static_cast<int64_t>(u.g) * p.rows * p.ldo;
             }
             const int64_t col0 = static_cast<int64_t>(u.nb) * BN;
-            if (u.nkb == 0) {  // empty expert (dweights): +0, no accumulator involved
-                if (orow >= 0)
+            if (u.nkb == 0) {  // no rows of the expert in this piece: +0 from the first piece only
+                if (orow >= 0 && !p.accum_out)
                     for (int64_t c = col0; c < col0 + BN && c < p.cols; ++c)
                         static_cast<float*>(out)[orow * p.ldo + c] = 0.0f;
                 continue;
@@ -587,16 +594,16 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
                     for (int i = 0; i < 16; ++i)
                         if (!isinf(f[i])) f[i] = __fadd_rn(f[i], __uint_as_float(v2[i]));
-                    if (p.accum_out) {  // earlier pieces' sum, left by the previous launch
-                        const float* prev = static_cast<const float*>(out) + orow * p.ldo + col0 + c0;
-#pragma unroll
-                        for (int i = 0; i < 16; ++i)
-                            if (col0 + c0 + i < p.cols) f[i] = __fadd_rn(prev[i], f[i]);
-                    }
                 }
                 if (IN == 2) {
 #pragma unroll
                     for (int i = 0; i < 16; ++i) f[i] = __fmul_rn(f[i], scale);
+                }
+                if (OUT == 2 && p.accum_out) {  // the earlier pieces' sum, left by the previous launch
+                    const float* prev = static_cast<const float*>(out) + orow * p.ldo + col0 + c0;
+#pragma unroll
+                    for (int i = 0; i < 16; ++i)
+                        if (col0 + c0 + i < p.cols) f[i] = __fadd_rn(prev[i], f[i]);
                 }
                 const int64_t cb = col0 + c0;
                 if (p.bias != nullptr) {  // the bias has the output's type
@@ -777,16 +784,26 @@ cudaError_t dx_t(const LaunchCtx& c, bi_dtype dt, void* dx, const void* dy, cons
 template <int FMT, bool F32>
 cudaError_t dw_t(const LaunchCtx& c, bi_dtype dt, void* dw, const void* x, const void* dy,
                  int64_t M, int64_t K, int64_t N) {
-    CUtensorMap a, b;
-    cudaError_t e;
-    if ((e = make_map(&a, dt, x, K, M, 1, BK)) != cudaSuccess) return e;   // X [M,K]: out k, contraction m
-    if ((e = make_map(&b, dt, dy, N, M, 1, BK)) != cudaSuccess) return e;  // dY [M,N]: out n, contraction m
-    Params p{};
-    p.out = dw; p.ldo = N; p.rows = K; p.cols = N;
-    p.num_m = static_cast<int>((K + BM - 1) / BM);
-    p.num_n = static_cast<int>((N + BN - 1) / BN);
-    p.num_kb = static_cast<int>((M + BK - 1) / BK);
-    return launch_pair<FMT, F32 ? 2 : FMT, true, true>(c, a, b, p);
+    // an f32 result over more than TC_PIECE_ROWS rows: pieces of that many rows,
+    // each launch after the first adding its result to dW (a rounded dW takes
+    // the whole contraction in one launch)
+    const int64_t piece = F32 ? TC_PIECE_ROWS : M;  // M > 0 (the engine writes +0 for M = 0)
+    for (int64_t d0 = 0; d0 < M; d0 += piece) {
+        const int64_t len = lmin(piece, M - d0);
+        CUtensorMap a, b;
+        cudaError_t e;
+        // X [M,K]: out k, contraction m; dY [M,N]: out n, contraction m (rows d0 .. d0 + len)
+        if ((e = make_map(&a, dt, static_cast<const uint16_t*>(x) + d0 * K, K, len, 1, BK)) != cudaSuccess) return e;
+        if ((e = make_map(&b, dt, static_cast<const uint16_t*>(dy) + d0 * N, N, len, 1, BK)) != cudaSuccess) return e;
+        Params p{};
+        p.out = dw; p.ldo = N; p.rows = K; p.cols = N;
+        p.accum_out = d0 > 0 ? 1 : 0;
+        p.num_m = static_cast<int>((K + BM - 1) / BM);
+        p.num_n = static_cast<int>((N + BN - 1) / BN);
+        p.num_kb = static_cast<int>((len + BK - 1) / BK);
+        if ((e = launch_pair<FMT, F32 ? 2 : FMT, true, true>(c, a, b, p)) != cudaSuccess) return e;
+    }
+    return cudaSuccess;
 }
 
 template <int FMT>
@@ -832,7 +849,16 @@ cudaError_t grouped_dw_t(const LaunchCtx& c, bi_dtype dt, float* dw, const void*
     p.num_n = static_cast<int>((K + BN - 1) / BN);
     p.num_kb = 0;
     const int64_t units = E * int64_t((p.num_m + 1) / 2) * p.num_n;
-    return launch_pair<FMT, 2, true, true, GROUPED_DW>(c, a, b, p, &a2, &b2, units);
+    // each expert's rows in pieces of TC_PIECE_ROWS (no expert has more than M
+    // rows); a unit with no rows in a later piece leaves dweights untouched
+    const int piece_kb = static_cast<int>(TC_PIECE_ROWS / BK);
+    for (int64_t j = 0; j * TC_PIECE_ROWS < M || j == 0; ++j) {
+        p.piece_kb0 = static_cast<int>(j) * piece_kb;
+        p.piece_kbn = piece_kb;
+        p.accum_out = j > 0 ? 1 : 0;
+        if ((e = launch_pair<FMT, 2, true, true, GROUPED_DW>(c, a, b, p, &a2, &b2, units)) != cudaSuccess) return e;
+    }
+    return cudaSuccess;
 }
 
 // 8-bit row-major tensor [outer][inner], box {128, box_outer}, 128-byte swizzle.
@@ -874,14 +900,21 @@ cudaError_t fp8_pass_t(const LaunchCtx& c, int pass, void* out, const uint8_t* a
         p.num_kb = static_cast<int>((N + 127) / 128);
         return launch_pair<2, OUT, false, false>(c, ma, mb, p);
     }
-    // dw = xq^T gq: A = xq [M,K] (out k, contraction m), B = gq [M,N] (out n, contraction m)
-    if ((e = make_map8(&ma, a, K, M, 128)) != cudaSuccess) return e;
-    if ((e = make_map8(&mb, b, N, M, 128)) != cudaSuccess) return e;
-    p.out = out; p.ldo = N; p.rows = K; p.cols = N; p.bias = nullptr;
-    p.num_m = static_cast<int>((K + BM - 1) / BM);
-    p.num_n = static_cast<int>((N + BN - 1) / BN);
-    p.num_kb = static_cast<int>((M + 127) / 128);
-    return launch_pair<2, OUT, true, true>(c, ma, mb, p);
+    // dw = xq^T gq: A = xq [M,K] (out k, contraction m), B = gq [M,N] (out n, contraction m);
+    // an f32 result in pieces of TC_PIECE_ROWS rows, as for the 16-bit dW
+    const int64_t piece = OUT == 2 ? TC_PIECE_ROWS : M;
+    for (int64_t d0 = 0; d0 < M; d0 += piece) {
+        const int64_t len = lmin(piece, M - d0);
+        if ((e = make_map8(&ma, a + d0 * K, K, len, 128)) != cudaSuccess) return e;
+        if ((e = make_map8(&mb, b + d0 * N, N, len, 128)) != cudaSuccess) return e;
+        p.out = out; p.ldo = N; p.rows = K; p.cols = N; p.bias = nullptr;
+        p.accum_out = d0 > 0 ? 1 : 0;
+        p.num_m = static_cast<int>((K + BM - 1) / BM);
+        p.num_n = static_cast<int>((N + BN - 1) / BN);
+        p.num_kb = static_cast<int>((len + 127) / 128);
+        if ((e = launch_pair<2, OUT, true, true>(c, ma, mb, p)) != cudaSuccess) return e;
+    }
+    return cudaSuccess;
 }
 
 // 32-bit K-major tensor [outer][inner] with row stride ld elements (ld >= inner,

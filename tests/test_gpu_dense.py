@@ -348,3 +348,26 @@ def test_launch_count_counts_kernels(eng):
     before = eng.launches()
     run_dense(eng, x, w, dy, b, m, k, n, "bf16", tc=0, passes=("y", "dx"))
     assert eng.launches() - before == 2
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+def test_tc_dw_f32_in_pieces(eng, dtype):
+    """dW kept in f32 over more rows than one 8192-row piece (8192 + 8192 + 3616):
+    exact on small integers, within the tolerance on random data, and the rounded
+    dW (one launch over all rows) within 1 ulp."""
+    m, k, n = 20000, 64, 136
+    hi = 16 if dtype == "f16" else 8
+    xi = synth.small_ints((m, k), -hi, hi, dtype, 95)
+    gi = synth.small_ints((m, n), -2, 2, dtype, 96)  # keeps every partial sum exact in f32
+    got = run_dense(eng, xi, None, gi, None, m, k, n, dtype, tc=1, passes=("dw",))
+    assert np.array_equal(got["dw"], oracle.backward_dw(synth.to_np(xi), synth.to_np(gi), m, k, n, dtype, dw_f32=True))
+    x, _, dy, _ = synth.dense_inputs(m, k, n, dtype, b=None)
+    got = run_dense(eng, x, None, dy, None, m, k, n, dtype, tc=1, passes=("dw",))
+    xn, dyn = synth.to_np(x), synth.to_np(dy)
+    x64, dy64 = f64(xn, dtype), f64(dyn, dtype)
+    r = oracle.backward_dw(xn, dyn, m, k, n, dtype, dw_f32=True)
+    ok, st = check_tc(got["dw"], r, abs_sum(x64.T, dy64), "f32")
+    assert ok, st
+    got_r = run_dense(eng, x, None, dy, None, m, k, n, dtype, tc=1, dw_f32=False, passes=("dw",))
+    ok, st = check_tc(got_r["dw"], r, abs_sum(x64.T, dy64), dtype)
+    assert ok, st

@@ -161,3 +161,15 @@ def test_quantize_special_values(eng, dtype):
     eng.check()
     want_q, want_amax = oracle.fp8_quantize(synth.to_np(x), dtype, 1.0)
     assert out_np(amax)[0] == want_amax and np.isfinite(want_amax)
+
+
+def test_fp8_dw_f32_in_pieces(eng):
+    """The FP8 dW kept in f32 over 20000 rows (pieces of 8192): exact on small integers."""
+    m, k, n = 20000, 128, 144
+    rng = np.random.default_rng(86)
+    xq = e4m3(rng.integers(-8, 9, size=(m, k)))
+    gq = e4m3(rng.integers(-2, 3, size=(m, n)))
+    dw = torch.empty(k, n, dtype=torch.float32, device="cuda")
+    eng.fp8_backward_dw(dw, xq.cuda(), gq.cuda(), scal(0.5), scal(0.25), m, k, n, "f32")
+    eng.check()
+    assert np.array_equal(out_np(dw), oracle.fp8_backward_dw(xq.numpy(), gq.numpy(), 0.5, 0.25, m, k, n, "f32"))

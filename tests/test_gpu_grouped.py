@@ -254,3 +254,32 @@ def test_grouped_many_experts_exact(eng, e, tc):
     assert np.array_equal(out_np(Y), want[0][order])
     assert np.array_equal(out_np(DX), want[1][order])
     assert np.array_equal(out_np(DW), want[2])
+
+
+@pytest.mark.parametrize("tc", [0, 1])
+def test_grouped_long_expert_in_pieces(eng, tc):
+    """One expert with more rows than an 8192-row piece (17000), one small, one
+    empty, plus padding: dweights bit-exact on small integers (the tensor-core
+    tier sums the expert's pieces in order), ids and caller-grouped rows."""
+    counts = np.array([17000, 2000, 0])
+    e, npad, k, n = 3, 1000, 64, 72
+    m = int(counts.sum()) + npad
+    rng = np.random.default_rng(97)
+    grouped_ids = np.concatenate([np.repeat(np.arange(e), counts), np.full(npad, e)]).astype(np.uint32)
+    ids = grouped_ids[rng.permutation(m)]
+    x = synth.small_ints((m, k), -4, 4, "bf16", 98)
+    w = synth.small_ints((e, n, k), -4, 4, "bf16", 99)
+    dy = synth.small_ints((m, n), -2, 2, "bf16", 100)
+    xn, wn, dyn = (synth.to_np(t) for t in (x, w, dy))
+    want = oracle.grouped_dweights(xn, dyn, ids, m, k, n, e, "bf16")
+    _, _, dw = run_grouped(eng, x, w, dy, torch.from_numpy(ids.astype(np.int64)), m, k, n, e, "bf16", tc=tc,
+                           with_dx=False)
+    assert np.array_equal(dw, want) and np.all(dw[2] == 0)
+    order = np.argsort(np.minimum(ids, e), kind="stable")
+    offs = torch.from_numpy(np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)).cuda()
+    DW = torch.empty(e, n, k, dtype=torch.float32, device="cuda")
+    strat = bi.BI_STRATEGY_TENSOR_CORE if tc else bi.BI_STRATEGY_SCALAR
+    eng.grouped_backward_segmented(None, DW, dev(x[torch.from_numpy(order)]), dev(w),
+                                   dev(dy[torch.from_numpy(order)]), offs, m, k, n, e, "bf16", None, strat)
+    eng.check()
+    assert np.array_equal(out_np(DW), want)
