@@ -110,11 +110,17 @@ def dtype_code(dtype) -> int:
 
 
 def _ptr(t):
-    """Device address of a tensor (or an int / None passed through)."""
+    """Device address of a tensor (or an int / None passed through).  The C ABI
+    reads dense row-major device memory, so a tensor on the host or a strided
+    view is refused here rather than handed to the kernels."""
     if t is None:
         return None
     if isinstance(t, int):
         return t
+    if not t.is_cuda:
+        raise ValueError("bi: tensors must be on a CUDA device")
+    if not t.is_contiguous():
+        raise ValueError("bi: tensors must be contiguous (dense, row-major)")
     return t.data_ptr()
 
 

@@ -90,3 +90,13 @@ def test_binding_rejects_unknown_dtypes(bi):
     with pytest.raises(ValueError):
         bi.dtype_code("int8")
     assert bi.dtype_code("bf16") == bi.BI_BF16
+
+
+def test_binding_refuses_host_and_strided_tensors(bi):
+    import torch
+    with pytest.raises(ValueError):
+        bi._ptr(torch.zeros(4, 4))  # a host tensor never reaches the kernels
+    if torch.cuda.is_available():
+        with pytest.raises(ValueError):
+            bi._ptr(torch.zeros(4, 4, device="cuda").t())
+    assert bi._ptr(None) is None and bi._ptr(1234) == 1234
