@@ -254,9 +254,10 @@ def test_tc_f32_long_contractions(eng, m, k, n):
     assert np.array_equal(part["y"], got["y"][:mp]) and np.array_equal(part["dx"], got["dx"][:mp])
 
 
+@pytest.mark.parametrize("dtype", ["bf16", "f16", "f32"])
 @pytest.mark.parametrize("tc", [0, 1])
-def test_ten_runs_bit_identical(eng, tc):
-    m, k, n, dtype = 1024, 768, 1536, "bf16"
+def test_ten_runs_bit_identical(eng, tc, dtype):
+    m, k, n = 1024, 768, 1536
     x, w, dy, b = synth.dense_inputs(m, k, n, dtype)
     first = run_dense(eng, x, w, dy, b, m, k, n, dtype, tc=tc)
     for _ in range(9):
