@@ -3,9 +3,11 @@
 // Contract (sgemm-bi 0.1.1.post2, "Determinism contracts", row "tensor cores"):
 // f32 accumulation, bit-identical across runs, each output row independent of M.
 // Every arithmetic choice is fixed by (pass, dtype, K, N):
-//   - one MMA shape per operand type: every pass, dense and grouped, runs
-//     tcgen05.mma.cta_group::2 M256 x N256 on a CTA pair (tc_gemm_pair_kernel;
-//     K16 per instruction for bf16/f16); f32 accumulators live in tensor memory;
+//   - every pass, dense and grouped, runs tcgen05.mma.cta_group::2 M256 x N256
+//     on a CTA pair (tc_gemm_pair_kernel; K16 per instruction for bf16/f16),
+//     except a 16-bit dW whose K x N output has few 256 x 256 tiles, which runs
+//     M256 x N128 (chosen from K and N alone); f32 accumulators live in tensor
+//     memory;
 //   - the contracted index is walked in 64-wide blocks in ascending order, four
 //     K16 instructions per block, accumulating into the same TMEM tile;
 //   - no split of the contraction, no atomics, no stream-K;
@@ -16,7 +18,7 @@
 //   warp 0 lane 0  TMA producer: cp.async.bulk.tensor loads into a ring of stages
 //   warp 1 lane 0  MMA issuer (warp 1 also owns the TMEM allocation)
 //   warps 2..5     epilogue: tcgen05.ld -> (+bias) -> one rounding -> st.global
-// The accumulator is double-buffered (2 x 256 TMEM columns) so the epilogue of
+// The accumulator is double-buffered (2 x N TMEM columns) so the epilogue of
 // one tile overlaps the main loop of the next.  Every mbarrier wait is bounded
 // by a %globaltimer limit; on expiry the kernel records a status code, stops all
 // roles, drains its own copies and MMAs, frees TMEM and returns.
@@ -32,11 +34,9 @@ namespace bi {
 namespace {
 
 constexpr int BM = 128;        // tile rows = MMA M
-constexpr int BN = 256;        // tile cols = MMA N
+constexpr int BN = 256;        // tile cols = MMA N (the 16-bit passes also have a 128-column tile)
 constexpr int BK = 64;         // contraction block = one 128-byte swizzle row of 16-bit data
-constexpr int UK = 16;         // contraction per MMA instruction
 constexpr int THREADS = 192;
-constexpr int TMEM_COLS = 2 * BN;
 constexpr int BAR_BYTES = 256;
 constexpr int GROUP_M = 16;    // raster: 16 row-tiles share the column sweep (L2 reuse)
 static_assert(GROUPED_TILE_ROWS == 256 && GROUPED_TAIL_ROWS == BK,
@@ -80,10 +80,6 @@ __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
 __device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
                  : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
@@ -186,16 +182,17 @@ template <> struct OutT<1> {
 // ---------------------------------------------------------------- CTA-pair kernel
 //
 // Every pass runs on a pair of CTAs (a 2-CTA cluster) that run one
-// tcgen05.mma.cta_group::2 of shape M256 x N256 x K16: CTA r of the pair holds
-// rows [128r, 128r+128) of the A tile and columns [128r, 128r+128) of the B
-// tile in its own shared memory, and receives rows [128r, 128r+128) of the
-// 256 x 256 accumulator in its own tensor memory.  Only CTA 0 issues MMAs.
-// Per CTA a 64-wide contraction block is 32 KB (A 16 KB + B 16 KB), so a
-// 7-stage ring fits.  Each output element is one ascending chain of K16 blocks
+// tcgen05.mma.cta_group::2 of shape M256 x BN x K16 (BN = 256, or 128 for the
+// few-tile dW): CTA r of the pair holds rows [128r, 128r+128) of the A tile and
+// columns [r BN/2, (r+1) BN/2) of the B tile in its own shared memory, and
+// receives rows [128r, 128r+128) of the 256 x BN accumulator in its own tensor
+// memory.  Only CTA 0 issues MMAs.  Per CTA a 64-wide contraction block is
+// 32 KB (A 16 KB + B 16 KB), so a 7-stage ring fits (24 KB and 9 stages at
+// BN = 128).  Each output element is one ascending chain of K16 blocks
 // in its accumulator; the instruction shape and the CTA mapping are fixed by
 // the pass, never by M.
 //
-// Work units (256 x 256 output tiles), by mode:
+// Work units (256 x BN output tiles), by mode:
 //   DENSE         a grouped raster over (row pair-tile, column tile);
 //   GROUPED_ROWS  forward / dinput: 256 consecutive rows of one expert in the
 //                 row-sorted operand, starting at any row (rows past the
@@ -210,13 +207,18 @@ template <> struct OutT<1> {
 // (each CTA, commit multicast), tempty[b] (CTA 0, 8 arrivals: the 4 epilogue
 // warps of each CTA).
 constexpr int P_A_BYTES = 128 * BK * 2;  // one 128 x 128-byte tile
-constexpr int P_B_BYTES = 128 * BK * 2;
+// B holds bnt / 2 rows of 128 bytes per CTA (bnt = the tile's columns).
+__host__ __device__ constexpr int p_b_bytes(int bnt) { return (bnt / 2) * BK * 2; }
 // Stage layout per operand type: one A and one B tile, or for the 3xTF32 mode
 // (IN = 3) the high and low parts of both (A_hi, B_hi, A_lo, B_lo).
 __host__ __device__ constexpr int p_tiles(int in) { return in == 3 ? 2 : 1; }
-__host__ __device__ constexpr int p_stage_bytes(int in) { return p_tiles(in) * (P_A_BYTES + P_B_BYTES); }
-__host__ __device__ constexpr int p_stages(int in) { return in == 3 ? 3 : 7; }
-__host__ __device__ constexpr int p_smem_bytes(int in) { return 1024 + p_stages(in) * p_stage_bytes(in) + BAR_BYTES; }
+__host__ __device__ constexpr int p_stage_bytes(int in, int bnt) { return p_tiles(in) * (P_A_BYTES + p_b_bytes(bnt)); }
+__host__ __device__ constexpr int p_stages(int in, int bnt) { return in == 3 ? 3 : (bnt == 256 ? 7 : 9); }
+__host__ __device__ constexpr int p_smem_bytes(int in, int bnt) {
+    return 1024 + p_stages(in, bnt) * p_stage_bytes(in, bnt) + BAR_BYTES;
+}
+static_assert(p_smem_bytes(0, 256) <= 227 * 1024 && p_smem_bytes(0, 128) <= 227 * 1024 &&
+              p_smem_bytes(3, 256) <= 227 * 1024, "stages fit the shared memory of one CTA");
 
 __device__ __forceinline__ uint32_t mapa_rank(uint32_t saddr, uint32_t rank) {
     uint32_t r;
@@ -246,7 +248,7 @@ __device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const CUtensorMap
 struct PairTile {
     int g;        // expert (grouped modes)
     int mpair;    // 256-row output tile (dense, dweights); tile within the expert (rows)
-    int nb;       // 256-column output tile
+    int nb;       // BN-column output tile
     int nkb;      // contraction blocks
     int row0;     // grouped: first sorted row of the unit (rows) / of the expert (dweights)
     int row_end;  // grouped: end of the expert's sorted rows
@@ -356,12 +358,12 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar_cluster) {
 }
 
 // kind::f16: format 0 = f16, 1 = bf16; kind::f8f6f4: 0 = e4m3; kind::tf32: 2 = tf32.
-template <int IN, bool A_MN, bool B_MN>
+template <int IN, bool A_MN, bool B_MN, int BNT>
 __device__ __forceinline__ constexpr uint32_t instr_desc_pair() {
     constexpr uint32_t FMT = IN == 1 ? 1u : (IN == 3 ? 2u : 0u);
     return (1u << 4) | (FMT << 7) | (FMT << 10) |
            (static_cast<uint32_t>(A_MN) << 15) | (static_cast<uint32_t>(B_MN) << 16) |
-           (static_cast<uint32_t>(256 >> 3) << 17) | (static_cast<uint32_t>(256 >> 4) << 24);
+           (static_cast<uint32_t>(BNT >> 3) << 17) | (static_cast<uint32_t>(256 >> 4) << 24);
 }
 
 // IN: 0 f16, 1 bf16, 2 e4m3 (scaled by *scale_a * *scale_b), 3 f32 as a
@@ -370,14 +372,14 @@ __device__ __forceinline__ constexpr uint32_t instr_desc_pair() {
 // tile row (64, 128 or 32 elements); four MMAs of K = 16 / 32 / 8 cover it
 // (three per K step in the 3xTF32 mode).
 //
-// Accumulators: two 256-column TMEM buffers, so the epilogue of one tile
+// Accumulators: two BN-column TMEM buffers, so the epilogue of one tile
 // overlaps the MMAs of the next.  The 3xTF32 mode uses both halves of TMEM for
 // one tile instead: hi*hi accumulates in columns 0-255, lo*hi + hi*lo in
 // columns 256-511, and the epilogue adds the two (one rounding) unless the
 // hi*hi sum is infinite, which then is the result.  The tensor
 // core's accumulation rounding then hits the large sum once per K step rather
 // than three times, and the small sum's rounding is 2^-11 smaller.
-template <int IN, int OUT, bool A_MN, bool B_MN, int MODE>
+template <int IN, int OUT, bool A_MN, bool B_MN, int MODE, int BNT>
 __global__ void __launch_bounds__(THREADS, 1)
     tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ CUtensorMap tmA2, const __grid_constant__ CUtensorMap tmB2,
@@ -386,11 +388,16 @@ __global__ void __launch_bounds__(THREADS, 1)
     // the tf32 operands are always staged K-major (the split kernel transposes)
     static_assert(IN != 3 || (!A_MN && !B_MN), "3xTF32 takes K-major operands only");
     static_assert(MODE == DENSE || IN <= 1, "grouped passes take bf16 / f16 operands");
-    constexpr int P_STAGES = p_stages(IN);
-    constexpr int P_STAGE_BYTES = p_stage_bytes(IN);
+    static_assert(BNT == 256 || (BNT == 128 && IN <= 1 && MODE == DENSE), "the 128-column tile: 16-bit dense");
+    constexpr int BN = BNT;                 // tile columns = MMA N
+    constexpr int TMEM_COLS = 2 * BN;
+    constexpr int P_B_BYTES = p_b_bytes(BN);
+    constexpr int P_STAGES = p_stages(IN, BN);
+    constexpr int P_STAGE_BYTES = p_stage_bytes(IN, BN);
     constexpr int BKE = 128 / ES;           // contraction elements per block
     constexpr int NACC = IN == 3 ? 1 : 2;   // accumulator buffers in flight
     constexpr int MN_ATOMS = ES;            // 128-byte atoms across a 128-wide MN-major tile
+    constexpr int B_ATOMS = (BN / 2) * ES / 128;  // the same across this CTA's B columns
     constexpr uint32_t MN_STEP = (32 / ES) * 128;  // one MMA's rows of an MN-major tile, bytes
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
@@ -450,7 +457,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         for (int t = cidx; pair_tile<MODE>(p, t, u); t += ncl) {
             // A rows (MN-major: A columns) and B columns of this CTA
             const int arow = (MODE == GROUPED_ROWS ? u.row0 : u.mpair * 256) + static_cast<int>(crank) * 128;
-            const int bcol = u.nb * BN + static_cast<int>(crank) * 128;
+            const int bcol = u.nb * BN + static_cast<int>(crank) * (BN / 2);
             for (int kb = 0; kb < u.nkb; ++kb) {
                 if (!mbar_wait(empty_bar(s), ph ^ 1u, abort_flag, p, DEV_TIMEOUT_PRODUCER)) goto done_p;
                 const uint32_t fb_leader = mapa_rank(full_bar(s), 0);
@@ -476,14 +483,14 @@ __global__ void __launch_bounds__(THREADS, 1)
                     }
                     if (MODE == GROUPED_ROWS) {  // W[g] through a 3-D map
                         if (B_MN) {
-                            for (int b = 0; b < MN_ATOMS; ++b)
+                            for (int b = 0; b < B_ATOMS; ++b)
                                 tma_load_3d_pair(b_dst + b * (BKE * 128), mb, bcol + b * (128 / ES), kofs, u.g,
                                                  fb_leader);
                         } else {
                             tma_load_3d_pair(b_dst, mb, kofs, bcol, u.g, fb_leader);
                         }
                     } else if (B_MN) {
-                        for (int b = 0; b < MN_ATOMS; ++b)
+                        for (int b = 0; b < B_ATOMS; ++b)
                             tma_load_2d_pair(b_dst + b * (BKE * 128), mb, bcol + b * (128 / ES), kofs, fb_leader);
                     } else {
                         tma_load_2d_pair(b_dst, mb, kofs, bcol, fb_leader);
@@ -498,7 +505,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         // barrier below before either CTA releases its shared memory.
     } else if (warp == 1 && lane == 0 && crank == 0) {
         // ------------------------------------------------------------ MMA issuer (CTA 0)
-        constexpr uint32_t idesc = instr_desc_pair<IN, A_MN, B_MN>();
+        constexpr uint32_t idesc = instr_desc_pair<IN, A_MN, B_MN, BN>();
         int s = 0;
         uint32_t ph = 0;
         int ab = 0;
@@ -566,6 +573,17 @@ __global__ void __launch_bounds__(THREADS, 1)
                 if (MODE == GROUPED_DW) out = static_cast<float*>(p.out) + static_cast<int64_t>(u.g) * p.rows * p.ldo;
             }
             const int64_t col0 = static_cast<int64_t>(u.nb) * BN;
+            // the tile's bias, read before its accumulator is ready: lane l holds
+            // columns col0 + 8l .. col0 + 8l + 7, handed out by shuffles below
+            float bv[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int64_t c = col0 + 8 * lane + i;
+                bv[i] = (p.bias != nullptr && c < p.cols)
+                            ? (OUT == 2 ? static_cast<const float*>(p.bias)[c] : OutT<OUT == 1 ? 1 : 0>::load(p.bias, c))
+                            : 0.0f;
+            }
+            static_assert(BN <= 8 * 32, "one 8-column bias slice per lane");
             if (u.nkb == 0) {  // no rows of the expert in this piece: +0 from the first piece only
                 if (orow >= 0 && !p.accum_out)
                     for (int64_t c = col0; c < col0 + BN && c < p.cols; ++c)
@@ -580,10 +598,16 @@ __global__ void __launch_bounds__(THREADS, 1)
                                    static_cast<uint32_t>(ab * BN);
             for (int c0 = 0; c0 < BN; c0 += 16) {
                 if (col0 + c0 >= p.cols) break;
+                __syncwarp();  // lanes past the output rows rejoin before the aligned load
                 uint32_t v[16];
                 tmem_ld16(tbase + c0, v);
                 uint32_t v2[16];
                 if (IN == 3) tmem_ld16(tbase + BN + c0, v2);
+                float bias16[16];  // every lane takes part in the shuffles
+                if (p.bias != nullptr) {
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) bias16[i] = __shfl_sync(0xffffffffu, bv[i & 7], (c0 >> 3) + (i >> 3));
+                }
                 if (orow < 0) continue;
                 float f[16];
 #pragma unroll
@@ -609,9 +633,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 if (p.bias != nullptr) {  // the bias has the output's type
 #pragma unroll
                     for (int i = 0; i < 16; ++i)
-                        if (cb + i < p.cols)
-                            f[i] = __fadd_rn(f[i], OUT == 2 ? static_cast<const float*>(p.bias)[cb + i]
-                                                            : OutT<OUT == 1 ? 1 : 0>::load(p.bias, cb + i));
+                        if (cb + i < p.cols) f[i] = __fadd_rn(f[i], bias16[i]);
                 }
                 const bool full = cb + 16 <= p.cols;
                 if (OUT == 2) {
@@ -704,11 +726,11 @@ cudaError_t make_map(CUtensorMap* m, bi_dtype dt, const void* ptr, uint64_t inne
 
 // units: work units (or an upper bound, for the grouped modes, whose count is
 // known only on the device); -1 = the dense count.
-template <int IN, int OUT, bool A_MN, bool B_MN, int MODE = DENSE>
+template <int IN, int OUT, bool A_MN, bool B_MN, int MODE = DENSE, int BNT = BN>
 cudaError_t launch_pair(const LaunchCtx& c, const CUtensorMap& a, const CUtensorMap& b, Params p,
                         const CUtensorMap* a2 = nullptr, const CUtensorMap* b2 = nullptr, int64_t units = -1) {
-    auto kern = tc_gemm_pair_kernel<IN, OUT, A_MN, B_MN, MODE>;
-    constexpr int P_SMEM_BYTES = p_smem_bytes(IN);
+    auto kern = tc_gemm_pair_kernel<IN, OUT, A_MN, B_MN, MODE, BNT>;
+    constexpr int P_SMEM_BYTES = p_smem_bytes(IN, BNT);
     static PerDeviceOnce setup;  // per device: the shared-memory opt-in and the co-resident clusters
     cudaLaunchAttribute at[1];
     at[0].id = cudaLaunchAttributeClusterDimension;
@@ -781,7 +803,7 @@ cudaError_t dx_t(const LaunchCtx& c, bi_dtype dt, void* dx, const void* dy, cons
     return launch_pair<FMT, FMT, false, false>(c, a, b, p);
 }
 
-template <int FMT, bool F32>
+template <int FMT, bool F32, int BNT>
 cudaError_t dw_t(const LaunchCtx& c, bi_dtype dt, void* dw, const void* x, const void* dy,
                  int64_t M, int64_t K, int64_t N) {
     // an f32 result over more than TC_PIECE_ROWS rows: pieces of that many rows,
@@ -799,9 +821,9 @@ cudaError_t dw_t(const LaunchCtx& c, bi_dtype dt, void* dw, const void* x, const
         p.out = dw; p.ldo = N; p.rows = K; p.cols = N;
         p.accum_out = d0 > 0 ? 1 : 0;
         p.num_m = static_cast<int>((K + BM - 1) / BM);
-        p.num_n = static_cast<int>((N + BN - 1) / BN);
+        p.num_n = static_cast<int>((N + BNT - 1) / BNT);
         p.num_kb = static_cast<int>((len + BK - 1) / BK);
-        if ((e = launch_pair<FMT, F32 ? 2 : FMT, true, true>(c, a, b, p)) != cudaSuccess) return e;
+        if ((e = launch_pair<FMT, F32 ? 2 : FMT, true, true, DENSE, BNT>(c, a, b, p)) != cudaSuccess) return e;
     }
     return cudaSuccess;
 }
@@ -932,6 +954,17 @@ cudaError_t make_map32(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+// Tile width of the 16-bit dW, a function of K and N only: 128 columns when
+// the K x N output has fewer 256 x 256 tiles than a 152-SM GPU has CTA pairs,
+// so that more pairs share a small weight gradient.  (A 128-column stage is
+// consumed in half the time of a 256-column one, and the deepest ring that
+// fits does not cover the load latency; with work for every pair the wider
+// tile is faster, so Y and dX, whose tile counts grow with M, keep it.)  The
+// tile width does not enter the accumulation order: every output element is
+// the same ascending chain of 64-wide contraction blocks.
+constexpr int64_t DW_FEW_TILES = 76;
+bool narrow_dw(int64_t K, int64_t N) { return ((K + 255) / 256) * ((N + 255) / 256) < DW_FEW_TILES; }
+
 }  // namespace
 
 cudaError_t tc_forward(const LaunchCtx& c, bi_dtype dt, void* y, const void* x, const void* w,
@@ -947,9 +980,13 @@ cudaError_t tc_dx(const LaunchCtx& c, bi_dtype dt, void* dx, const void* dy, con
 
 cudaError_t tc_dw(const LaunchCtx& c, bi_dtype dt, void* dw, int dw_f32, const void* x,
                   const void* dy, int64_t M, int64_t K, int64_t N) {
-    if (dt == BI_BF16)
-        return dw_f32 ? dw_t<1, true>(c, dt, dw, x, dy, M, K, N) : dw_t<1, false>(c, dt, dw, x, dy, M, K, N);
-    return dw_f32 ? dw_t<0, true>(c, dt, dw, x, dy, M, K, N) : dw_t<0, false>(c, dt, dw, x, dy, M, K, N);
+    const bool nw = narrow_dw(K, N);
+    if (dt == BI_BF16) {
+        if (dw_f32) return nw ? dw_t<1, true, 128>(c, dt, dw, x, dy, M, K, N) : dw_t<1, true, 256>(c, dt, dw, x, dy, M, K, N);
+        return nw ? dw_t<1, false, 128>(c, dt, dw, x, dy, M, K, N) : dw_t<1, false, 256>(c, dt, dw, x, dy, M, K, N);
+    }
+    if (dw_f32) return nw ? dw_t<0, true, 128>(c, dt, dw, x, dy, M, K, N) : dw_t<0, true, 256>(c, dt, dw, x, dy, M, K, N);
+    return nw ? dw_t<0, false, 128>(c, dt, dw, x, dy, M, K, N) : dw_t<0, false, 256>(c, dt, dw, x, dy, M, K, N);
 }
 
 cudaError_t tc_grouped_rows(const LaunchCtx& c, bi_dtype dt, int pass_dinput, void* out, const void* a_sorted,

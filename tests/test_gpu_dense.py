@@ -114,6 +114,8 @@ TC_CASES = [
     ("ragged_1000_f16", "f16", 1000, 1000, 1000),
     ("gemv_f16", "f16", 1, 4096, 4096),
     ("small_k_f16", "f16", 130, 8, 72),
+    ("ragged_tiles_bf16", "bf16", 700, 384, 1408),  # 5.5 and 1.5 column tiles; dW on 128-column tiles
+    ("ragged_tiles_f16", "f16", 520, 640, 384),
 ]
 
 
@@ -289,6 +291,21 @@ def test_batch_invariance_prefixes(eng, dtype, tc):
                          passes=("y", "dx"))
         assert np.array_equal(part["y"], full["y"][:mp])
         assert np.array_equal(part["dx"], full["dx"][:mp])
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+def test_batch_invariance_ragged_tiles(eng, dtype):
+    """Rows of Y and dX do not depend on M where N and K end half-way through
+    a column tile (N = 5.5 tiles, K = 1.5 tiles) and M is not a multiple of the
+    256-row pair tile."""
+    m, k, n = 700, 384, 1408
+    x, w, dy, b = synth.dense_inputs(m, k, n, dtype)
+    full = run_dense(eng, x, w, dy, b, m, k, n, dtype, tc=1, passes=("y", "dx"))
+    for mp in (1, 7, 256, 300):
+        part = run_dense(eng, x[:mp].contiguous(), w, dy[:mp].contiguous(), b, mp, k, n, dtype, tc=1,
+                         passes=("y", "dx"))
+        assert np.array_equal(part["y"], full["y"][:mp]), mp
+        assert np.array_equal(part["dx"], full["dx"][:mp]), mp
 
 
 # ------------------------------------------------------------------- edge cases and errors

@@ -57,10 +57,11 @@ def test_grouped_scalar_bit_exact(eng, dtype):
     assert np.all(dw[2] == 0)
 
 
+@pytest.mark.parametrize("k,n", [(96, 136), (384, 640)])  # (384, 640): half-used last column tiles
 @pytest.mark.parametrize("dtype", ["bf16", "f16"])
-def test_grouped_tc_within_tolerance(eng, dtype):
-    m, k, n, e = 700, 96, 136, 5
-    x, w, dy, ids = small_case(dtype)
+def test_grouped_tc_within_tolerance(eng, dtype, k, n):
+    m, e = 700, 5
+    x, w, dy, ids = small_case(dtype, k=k, n=n)
     y, dx, dw = run_grouped(eng, x, w, dy, ids, m, k, n, e, dtype, tc=1)
     xn, wn, dyn, idn = (synth.to_np(t) for t in (x, w, dy, ids))
     x64, w64, dy64 = f64(xn, dtype), f64(wn, dtype).reshape(e, n, k), f64(dyn, dtype)
