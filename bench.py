@@ -3,7 +3,8 @@
 One step = the four projections of a 7B-class transformer layer at M = 8192
 tokens (qkv 4096->12288, o 4096->4096, up 4096->11008, down 11008->4096), each
 run through bi_forward, bi_backward_dx and bi_backward_dw (f32 dW) on the
-tensor-core tier: 12 kernel launches, 7.73 TFLOP of algorithmic work.
+tensor-core tier: 12 GEMM launches (plus one chunk-sum launch per dW whose
+last wave of tiles is split), 7.73 TFLOP of algorithmic work.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
 
@@ -165,7 +166,7 @@ def make_inputs(device):
 
 
 def run_step(eng, bufs, m, stream, events=None):
-    """Enqueue one step (12 launches).  events: list to append (pass, start, end)."""
+    """Enqueue one step (12 calls).  events: list to append (pass, start, end)."""
     import torch
     for b in bufs:
         k, n = b["k"], b["n"]

@@ -144,8 +144,12 @@ cudaError_t tc_forward(const LaunchCtx& c, bi_dtype dt, void* y, const void* x, 
                        const void* bias, int64_t M, int64_t K, int64_t N);
 cudaError_t tc_dx(const LaunchCtx& c, bi_dtype dt, void* dx, const void* dy, const void* w,
                   int64_t M, int64_t K, int64_t N);
+// dW: the output tiles of the last, partial wave run their contraction in
+// chunks, summed in order; ws holds their f32 results (tc_dw_workspace_bytes,
+// 0 = no split for this shape, ws may be null).
+int64_t tc_dw_workspace_bytes(int dw_f32, int64_t M, int64_t K, int64_t N);
 cudaError_t tc_dw(const LaunchCtx& c, bi_dtype dt, void* dw, int dw_f32, const void* x,
-                  const void* dy, int64_t M, int64_t K, int64_t N);
+                  const void* dy, int64_t M, int64_t K, int64_t N, float* ws);
 // Grouped forward / dinput on a row-sorted operand a_sorted [M, K or N] (row
 // s = original row perm[s]); output row perm[s] for every sorted row of an expert.
 cudaError_t tc_grouped_rows(const LaunchCtx& c, bi_dtype dt, int pass_dinput, void* out, const void* a_sorted,

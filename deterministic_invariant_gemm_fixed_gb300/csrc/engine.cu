@@ -294,7 +294,9 @@ bi_status bi_backward_dw(bi_engine eng, void* dw, int dw_f32, const void* x, con
     if (tier && dtype == BI_F32)  // dw = x^T dy: both transposed (contraction over m)
         return tf32x3(eng, c, {x, m, k, true}, {dy, m, n, true}, dw, n, nullptr, k, n, m, "bi_backward_dw");
     if (tier) {
-        cudaError_t e = bi::tc_dw(c, dtype, dw, out_f32, x, dy, m, k, n);
+        Scratch ws(eng, s, static_cast<size_t>(bi::tc_dw_workspace_bytes(out_f32, m, k, n)));
+        if (ws.err != cudaSuccess) return cuda_fail(eng, ws.err, "dW chunk scratch");
+        cudaError_t e = bi::tc_dw(c, dtype, dw, out_f32, x, dy, m, k, n, static_cast<float*>(ws.ptr));
         return e == cudaSuccess ? BI_OK : cuda_fail(eng, e, "bi_backward_dw");
     }
     Scratch part(eng, s, J > 1 ? static_cast<size_t>(J * k * n * 4) : 0);

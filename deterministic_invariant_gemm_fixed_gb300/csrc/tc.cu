@@ -57,6 +57,8 @@ struct Params {
     const float* scale_b;
     int accum_out;           // f32 out, a contraction piece after the first: out += result
     int piece_kb0, piece_kbn;  // grouped dweights: contraction blocks [kb0, kb0 + kbn) of each expert
+    int split_from, split_s; // dense: tiles from split_from on run their contraction as split_s chunks
+    float* partials;         // ... whose f32 results go here, 256 x BN per (tile, chunk)
     int* status;
     unsigned long long wait_limit;
 };
@@ -244,6 +246,18 @@ __device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const CUtensorMap
         : "memory");
 }
 
+// Raster of the dense tiles: GROUP_M row pairs share a sweep over the column
+// tiles (L2 reuse of the B columns).
+__host__ __device__ __forceinline__ void dense_raster(int t, int units_m, int num_n, int& mpair, int& nb) {
+    const int span = GROUP_M * num_n;
+    const int grp = t / span;
+    const int first = grp * GROUP_M;
+    const int gsize = min(units_m - first, GROUP_M);
+    const int r = t - grp * span;
+    mpair = first + r % gsize;
+    nb = r / gsize;
+}
+
 // One work unit of the pair kernel.
 struct PairTile {
     int g;        // expert (grouped modes)
@@ -253,27 +267,37 @@ struct PairTile {
     int row0;     // grouped: first sorted row of the unit (rows) / of the expert (dweights)
     int row_end;  // grouped: end of the expert's sorted rows
     int full_kb;  // dweights: blocks read in place; block full_kb is the tail block
-    int kb0;      // dweights: first contraction block of this piece (others: 0)
+    int kb0;      // first contraction block of this unit (dweights pieces, dense chunks)
+    int part;     // dense chunk: its slot in p.partials; -1 = the unit writes the output
 };
 
 template <int MODE>
 __device__ __forceinline__ bool pair_tile(const Params& p, int t, PairTile& u) {
     const int units_m = (p.num_m + 1) / 2;
+    u.part = -1;
     if (MODE == DENSE) {
-        if (t >= units_m * p.num_n) return false;
-        const int span = GROUP_M * p.num_n;
-        const int grp = t / span;
-        const int first = grp * GROUP_M;
-        const int gsize = min(units_m - first, GROUP_M);
-        const int r = t - grp * span;
+        // tiles [0, split_from) whole; each later tile as split_s consecutive
+        // units, chunk j contracting blocks [j nkb / s, (j + 1) nkb / s)
+        int tile = t, chunk = -1;
+        if (p.split_s > 1 && t >= p.split_from) {
+            const int q = t - p.split_from;
+            tile = p.split_from + q / p.split_s;
+            chunk = q - (q / p.split_s) * p.split_s;
+            u.part = q;
+        }
+        if (tile >= units_m * p.num_n) return false;
+        dense_raster(tile, units_m, p.num_n, u.mpair, u.nb);
         u.g = 0;
-        u.mpair = first + r % gsize;
-        u.nb = r / gsize;
-        u.nkb = p.num_kb;
         u.row0 = 0;
         u.row_end = 0;
         u.full_kb = p.num_kb;
-        u.kb0 = 0;
+        if (chunk < 0) {
+            u.kb0 = 0;
+            u.nkb = p.num_kb;
+        } else {
+            u.kb0 = chunk * p.num_kb / p.split_s;
+            u.nkb = (chunk + 1) * p.num_kb / p.split_s - u.kb0;
+        }
         return true;
     }
     const uint32_t* off = p.seg;            // sorted offsets of buckets 0..E, then m
@@ -462,7 +486,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 if (!mbar_wait(empty_bar(s), ph ^ 1u, abort_flag, p, DEV_TIMEOUT_PRODUCER)) goto done_p;
                 const uint32_t fb_leader = mapa_rank(full_bar(s), 0);
                 if (crank == 0) mbar_expect_tx(full_bar(s), 2 * P_STAGE_BYTES);
-                int kofs = kb * BKE;  // contraction coordinate
+                int kofs = (u.kb0 + kb) * BKE;  // contraction coordinate
                 bool tail = false;
                 if (MODE == GROUPED_DW) {  // the expert's rows in place, or its tail block
                     const int kba = u.kb0 + kb;
@@ -608,6 +632,16 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
                     for (int i = 0; i < 16; ++i) bias16[i] = __shfl_sync(0xffffffffu, bv[i & 7], (c0 >> 3) + (i >> 3));
                 }
+                if (IN <= 1 && MODE == DENSE && u.part >= 0) {  // a chunk's raw f32 sum
+                    float* dst = p.partials + static_cast<int64_t>(u.part) * (256 * BN) +
+                                 static_cast<int64_t>(crank * 128 + r) * BN + c0;
+#pragma unroll
+                    for (int i = 0; i < 16; i += 4)
+                        *reinterpret_cast<float4*>(dst + i) =
+                            make_float4(__uint_as_float(v[i]), __uint_as_float(v[i + 1]), __uint_as_float(v[i + 2]),
+                                        __uint_as_float(v[i + 3]));
+                    continue;
+                }
                 if (orow < 0) continue;
                 float f[16];
 #pragma unroll
@@ -686,6 +720,57 @@ __global__ void __launch_bounds__(THREADS, 1)
         asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
                      "r"(TMEM_COLS)
                      : "memory");
+    }
+}
+
+// dW tiles whose contraction ran as chunks: out = (((c_0 + c_1) + c_2) + ...)
+// in chunk order (then, for a contraction piece after the first, the earlier
+// pieces' sum in out plus that), rounded once to the output type.  One thread
+// per 4 consecutive columns of a tile row.
+template <int OUT>
+__global__ void __launch_bounds__(256) dw_chunk_sum_kernel(const float* __restrict__ partials, int split_from,
+                                                           int split_s, int split_tiles, int units_m, int num_n,
+                                                           int bn, void* out, int64_t ldo, int64_t rows,
+                                                           int64_t cols, int accum_out) {
+    grid_dep_wait();
+    grid_dep_launch();
+    const int64_t per_tile = 256 * static_cast<int64_t>(bn) / 4;
+    const int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (idx >= split_tiles * per_tile) return;
+    const int ti = static_cast<int>(idx / per_tile);
+    const int64_t rem = idx - ti * per_tile;
+    const int row = static_cast<int>(rem / (bn / 4));
+    const int c4 = static_cast<int>(rem - static_cast<int64_t>(row) * (bn / 4)) * 4;
+    int mpair, nb;
+    dense_raster(split_from + ti, units_m, num_n, mpair, nb);
+    const int64_t gr = static_cast<int64_t>(mpair) * 256 + row, gc = static_cast<int64_t>(nb) * bn + c4;
+    if (gr >= rows || gc >= cols) return;  // cols is a multiple of 8: the 4 columns are inside
+    const int64_t slot = 256 * static_cast<int64_t>(bn);
+    const float* src = partials + static_cast<int64_t>(ti) * split_s * slot + static_cast<int64_t>(row) * bn + c4;
+    float4 v = *reinterpret_cast<const float4*>(src);
+    for (int j = 1; j < split_s; ++j) {
+        const float4 w = *reinterpret_cast<const float4*>(src + j * slot);
+        v.x = __fadd_rn(v.x, w.x);
+        v.y = __fadd_rn(v.y, w.y);
+        v.z = __fadd_rn(v.z, w.z);
+        v.w = __fadd_rn(v.w, w.w);
+    }
+    if (OUT == 2) {
+        float4* dst = reinterpret_cast<float4*>(static_cast<float*>(out) + gr * ldo + gc);
+        if (accum_out) {
+            const float4 prev = *dst;
+            v.x = __fadd_rn(prev.x, v.x);
+            v.y = __fadd_rn(prev.y, v.y);
+            v.z = __fadd_rn(prev.z, v.z);
+            v.w = __fadd_rn(prev.w, v.w);
+        }
+        *dst = v;
+    } else {
+        using O = OutT<OUT == 1 ? 1 : 0>;
+        uint2 w;
+        w.x = O::pack(v.x, v.y);
+        w.y = O::pack(v.z, v.w);
+        *reinterpret_cast<uint2*>(static_cast<typename O::T*>(out) + gr * ldo + gc) = w;
     }
 }
 
@@ -803,9 +888,42 @@ cudaError_t dx_t(const LaunchCtx& c, bi_dtype dt, void* dx, const void* dy, cons
     return launch_pair<FMT, FMT, false, false>(c, a, b, p);
 }
 
+// Tile width of the 16-bit dW, a function of K and N only: 128 columns when
+// the K x N output has fewer 256 x 256 tiles than a 152-SM GPU has CTA pairs,
+// so that more pairs share a small weight gradient.  (A 128-column stage is
+// consumed in half the time of a 256-column one, and the deepest ring that
+// fits does not cover the load latency; with work for every pair the wider
+// tile is faster, so Y and dX, whose tile counts grow with M, keep it.)  The
+// tile width does not enter the accumulation order: every output element is
+// the same ascending chain of 64-wide contraction blocks.
+constexpr int64_t DW_FEW_TILES = 76;
+bool narrow_dw(int64_t K, int64_t N) { return ((K + 255) / 256) * ((N + 255) / 256) < DW_FEW_TILES; }
+// dW's output tiles do not depend on M, and its contraction is the batch: the
+// tiles of the last, partial wave (on a 152-SM GPU's 76 CTA pairs) run their
+// contraction as s chunks of consecutive 64-row blocks, s pairs per tile, and
+// dw_chunk_sum_kernel adds the chunks in order.  s = min(76 / tail tiles,
+// blocks / 8), a function of M, K and N only; 1 = no split.  Y and dX are
+// never split: their rows must not depend on M.
+constexpr int64_t DW_WAVE = 76;
+constexpr int64_t DW_MIN_CHUNK_KB = 8;
+int dw_split(int64_t tiles, int64_t nkb) {
+    const int64_t tail = tiles % DW_WAVE;
+    if (tail == 0) return 1;
+    const int64_t sp = lmin(DW_WAVE / tail, nkb / DW_MIN_CHUNK_KB);
+    return sp >= 2 ? static_cast<int>(sp) : 1;
+}
+struct DwShape {
+    int bnt;        // tile columns
+    int64_t tiles;  // output tiles of K x N
+};
+DwShape dw_shape(int64_t K, int64_t N) {
+    const int bnt = narrow_dw(K, N) ? 128 : 256;
+    return {bnt, ((K + BM - 1) / BM + 1) / 2 * ((N + bnt - 1) / bnt)};
+}
+
 template <int FMT, bool F32, int BNT>
 cudaError_t dw_t(const LaunchCtx& c, bi_dtype dt, void* dw, const void* x, const void* dy,
-                 int64_t M, int64_t K, int64_t N) {
+                 int64_t M, int64_t K, int64_t N, float* ws) {
     // an f32 result over more than TC_PIECE_ROWS rows: pieces of that many rows,
     // each launch after the first adding its result to dW (a rounded dW takes
     // the whole contraction in one launch)
@@ -823,7 +941,26 @@ cudaError_t dw_t(const LaunchCtx& c, bi_dtype dt, void* dw, const void* x, const
         p.num_m = static_cast<int>((K + BM - 1) / BM);
         p.num_n = static_cast<int>((N + BNT - 1) / BNT);
         p.num_kb = static_cast<int>((len + BK - 1) / BK);
-        if ((e = launch_pair<FMT, F32 ? 2 : FMT, true, true, DENSE, BNT>(c, a, b, p)) != cudaSuccess) return e;
+        const int units_m = (p.num_m + 1) / 2;
+        const int64_t tiles = static_cast<int64_t>(units_m) * p.num_n;
+        const int sp = dw_split(tiles, p.num_kb);
+        if (sp > 1 && ws == nullptr) return cudaErrorInvalidValue;
+        p.split_s = sp;
+        p.split_from = static_cast<int>(sp > 1 ? tiles - tiles % DW_WAVE : tiles);
+        p.partials = ws;
+        const int64_t split_tiles = tiles - p.split_from;
+        if ((e = launch_pair<FMT, F32 ? 2 : FMT, true, true, DENSE, BNT>(c, a, b, p, nullptr, nullptr,
+                                                                          p.split_from + split_tiles * sp)) !=
+            cudaSuccess)
+            return e;
+        if (sp > 1) {
+            const int64_t threads = split_tiles * 256 * BNT / 4;
+            e = launch_pdl(dw_chunk_sum_kernel<F32 ? 2 : FMT>, dim3(static_cast<unsigned>((threads + 255) / 256)),
+                           dim3(256), 0, c.stream, ws, p.split_from, sp, static_cast<int>(split_tiles), units_m,
+                           p.num_n, BNT, dw, p.ldo, p.rows, p.cols, p.accum_out);
+            if (e != cudaSuccess) return e;
+            c.count();
+        }
     }
     return cudaSuccess;
 }
@@ -954,17 +1091,6 @@ cudaError_t make_map32(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-// Tile width of the 16-bit dW, a function of K and N only: 128 columns when
-// the K x N output has fewer 256 x 256 tiles than a 152-SM GPU has CTA pairs,
-// so that more pairs share a small weight gradient.  (A 128-column stage is
-// consumed in half the time of a 256-column one, and the deepest ring that
-// fits does not cover the load latency; with work for every pair the wider
-// tile is faster, so Y and dX, whose tile counts grow with M, keep it.)  The
-// tile width does not enter the accumulation order: every output element is
-// the same ascending chain of 64-wide contraction blocks.
-constexpr int64_t DW_FEW_TILES = 76;
-bool narrow_dw(int64_t K, int64_t N) { return ((K + 255) / 256) * ((N + 255) / 256) < DW_FEW_TILES; }
-
 }  // namespace
 
 cudaError_t tc_forward(const LaunchCtx& c, bi_dtype dt, void* y, const void* x, const void* w,
@@ -978,15 +1104,22 @@ cudaError_t tc_dx(const LaunchCtx& c, bi_dtype dt, void* dx, const void* dy, con
     return dt == BI_BF16 ? dx_t<1>(c, dt, dx, dy, w, M, K, N) : dx_t<0>(c, dt, dx, dy, w, M, K, N);
 }
 
+int64_t tc_dw_workspace_bytes(int dw_f32, int64_t M, int64_t K, int64_t N) {
+    const DwShape d = dw_shape(K, N);
+    const int64_t len = dw_f32 ? lmin(M, TC_PIECE_ROWS) : M;  // the first (longest) contraction piece
+    const int sp = dw_split(d.tiles, (len + BK - 1) / BK);
+    return sp > 1 ? (d.tiles % DW_WAVE) * sp * 256 * d.bnt * 4 : 0;
+}
+
 cudaError_t tc_dw(const LaunchCtx& c, bi_dtype dt, void* dw, int dw_f32, const void* x,
-                  const void* dy, int64_t M, int64_t K, int64_t N) {
-    const bool nw = narrow_dw(K, N);
+                  const void* dy, int64_t M, int64_t K, int64_t N, float* ws) {
+    const bool nw = dw_shape(K, N).bnt == 128;
     if (dt == BI_BF16) {
-        if (dw_f32) return nw ? dw_t<1, true, 128>(c, dt, dw, x, dy, M, K, N) : dw_t<1, true, 256>(c, dt, dw, x, dy, M, K, N);
-        return nw ? dw_t<1, false, 128>(c, dt, dw, x, dy, M, K, N) : dw_t<1, false, 256>(c, dt, dw, x, dy, M, K, N);
+        if (dw_f32) return nw ? dw_t<1, true, 128>(c, dt, dw, x, dy, M, K, N, ws) : dw_t<1, true, 256>(c, dt, dw, x, dy, M, K, N, ws);
+        return nw ? dw_t<1, false, 128>(c, dt, dw, x, dy, M, K, N, ws) : dw_t<1, false, 256>(c, dt, dw, x, dy, M, K, N, ws);
     }
-    if (dw_f32) return nw ? dw_t<0, true, 128>(c, dt, dw, x, dy, M, K, N) : dw_t<0, true, 256>(c, dt, dw, x, dy, M, K, N);
-    return nw ? dw_t<0, false, 128>(c, dt, dw, x, dy, M, K, N) : dw_t<0, false, 256>(c, dt, dw, x, dy, M, K, N);
+    if (dw_f32) return nw ? dw_t<0, true, 128>(c, dt, dw, x, dy, M, K, N, ws) : dw_t<0, true, 256>(c, dt, dw, x, dy, M, K, N, ws);
+    return nw ? dw_t<0, false, 128>(c, dt, dw, x, dy, M, K, N, ws) : dw_t<0, false, 256>(c, dt, dw, x, dy, M, K, N, ws);
 }
 
 cudaError_t tc_grouped_rows(const LaunchCtx& c, bi_dtype dt, int pass_dinput, void* out, const void* a_sorted,

@@ -369,6 +369,36 @@ def test_launch_count_counts_kernels(eng):
 
 
 @pytest.mark.parametrize("dtype", ["bf16", "f16"])
+def test_tc_dw_tail_tiles_in_chunks(eng, dtype):
+    """dW tiles of the last, partial wave run their contraction as chunks summed
+    in order.  1024 x 2048 x 2560: 80 tiles of 256 x 256, the last 4 (rows
+    1024-2047, columns 2304-2559) in 2 chunks of 512 rows; checked there and on
+    whole tiles, f32 and rounded, and run to run.  2048 x 256 x 2048: 16 tiles of
+    256 x 128, each in 4 chunks, exact on small integers."""
+    m, k, n = 1024, 2048, 2560
+    x, _, dy, _ = synth.dense_inputs(m, k, n, dtype, b=None)
+    got = run_dense(eng, x, None, dy, None, m, k, n, dtype, tc=1, passes=("dw",))
+    got_r = run_dense(eng, x, None, dy, None, m, k, n, dtype, tc=1, dw_f32=False, passes=("dw",))
+    xn, dyn = synth.to_np(x), synth.to_np(dy)
+    x64, dy64 = f64(xn, dtype), f64(dyn, dtype)
+    cols = np.concatenate([np.arange(2304, 2560), sample_rows(2304, 24, seed=4)])
+    r = oracle.backward_dw(xn, dyn, m, k, n, dtype, dw_f32=True, cols=cols)
+    S = abs_sum(x64.T, dy64[:, cols])
+    ok, st = check_tc(got["dw"][:, cols], r, S, "f32")
+    assert ok, st
+    ok, st = check_tc(got_r["dw"][:, cols], r, S, dtype)
+    assert ok, st
+    again = run_dense(eng, x, None, dy, None, m, k, n, dtype, tc=1, passes=("dw",))
+    assert np.array_equal(again["dw"], got["dw"])
+    m, k, n = 2048, 256, 2048
+    hi = 16 if dtype == "f16" else 8
+    xi = synth.small_ints((m, k), -hi, hi, dtype, 97)
+    gi = synth.small_ints((m, n), -2, 2, dtype, 98)  # every partial sum exact in f32
+    got = run_dense(eng, xi, None, gi, None, m, k, n, dtype, tc=1, passes=("dw",))
+    assert np.array_equal(got["dw"], oracle.backward_dw(synth.to_np(xi), synth.to_np(gi), m, k, n, dtype, dw_f32=True))
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
 def test_tc_dw_f32_in_pieces(eng, dtype):
     """dW kept in f32 over more rows than one 8192-row piece (8192 + 8192 + 3616):
     exact on small integers, within the tolerance on random data, and the rounded
