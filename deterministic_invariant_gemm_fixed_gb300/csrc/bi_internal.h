@@ -161,9 +161,11 @@ cudaError_t tc_grouped_dw(const LaunchCtx& c, bi_dtype dt, float* dw, const void
                           const uint32_t* seg);
 // FP8 e4m3 scaled matmuls on the CTA pair (pass 0 forward, 1 dX, 2 dW): the
 // f32 product is multiplied by *sa * *sb, then (+ bias), then rounded to out_dt.
+// The dW splits its last wave of tiles as tc_dw does (ws: tc_fp8_dw_workspace_bytes).
+int64_t tc_fp8_dw_workspace_bytes(int out_f32, int64_t M, int64_t K, int64_t N);
 cudaError_t tc_fp8_pass(const LaunchCtx& c, int pass, bi_dtype out_dt, void* out, const uint8_t* a,
                         const uint8_t* b, const void* bias, const float* sa, const float* sb, int64_t M,
-                        int64_t K, int64_t N);
+                        int64_t K, int64_t N, float* ws);
 // 3xTF32 (f32 operands on the tensor cores, tf32.cu and tc.cu).
 // tf32_split: x [rows][cols] row-major into TF32 parts hi, lo.  Without transpose
 // they keep x's layout; with transpose they are [cols][ld] (ld >= rows, a

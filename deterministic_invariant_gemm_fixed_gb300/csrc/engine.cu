@@ -364,7 +364,11 @@ bi_status fp8_pass(bi_engine eng, int pass, void* out, const uint8_t* a, const u
                                         static_cast<cudaStream_t>(stream));
         return e == cudaSuccess ? BI_OK : cuda_fail(eng, e, name);
     }
-    cudaError_t e = bi::tc_fp8_pass(ctx(eng, stream), pass, out_dtype, out, a, b, bias, sa, sb, m, k, n);
+    Scratch ws(eng, static_cast<cudaStream_t>(stream),
+               pass == 2 ? static_cast<size_t>(bi::tc_fp8_dw_workspace_bytes(out_dtype == BI_F32, m, k, n)) : 0);
+    if (ws.err != cudaSuccess) return cuda_fail(eng, ws.err, "FP8 dW chunk scratch");
+    cudaError_t e = bi::tc_fp8_pass(ctx(eng, stream), pass, out_dtype, out, a, b, bias, sa, sb, m, k, n,
+                                    static_cast<float*>(ws.ptr));
     return e == cudaSuccess ? BI_OK : cuda_fail(eng, e, name);
 }
 

@@ -632,7 +632,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
                     for (int i = 0; i < 16; ++i) bias16[i] = __shfl_sync(0xffffffffu, bv[i & 7], (c0 >> 3) + (i >> 3));
                 }
-                if (IN <= 1 && MODE == DENSE && u.part >= 0) {  // a chunk's raw f32 sum
+                if (IN <= 2 && MODE == DENSE && u.part >= 0) {  // a chunk's raw f32 sum (unscaled)
                     float* dst = p.partials + static_cast<int64_t>(u.part) * (256 * BN) +
                                  static_cast<int64_t>(crank * 128 + r) * BN + c0;
 #pragma unroll
@@ -724,14 +724,16 @@ __global__ void __launch_bounds__(THREADS, 1)
 }
 
 // dW tiles whose contraction ran as chunks: out = (((c_0 + c_1) + c_2) + ...)
-// in chunk order (then, for a contraction piece after the first, the earlier
-// pieces' sum in out plus that), rounded once to the output type.  One thread
-// per 4 consecutive columns of a tile row.
+// in chunk order, times *scale_a * *scale_b for FP8 (scales non-null), then for
+// a contraction piece after the first the earlier pieces' sum in out plus
+// that, rounded once to the output type.  One thread per 4 consecutive columns
+// of a tile row.
 template <int OUT>
 __global__ void __launch_bounds__(256) dw_chunk_sum_kernel(const float* __restrict__ partials, int split_from,
                                                            int split_s, int split_tiles, int units_m, int num_n,
                                                            int bn, void* out, int64_t ldo, int64_t rows,
-                                                           int64_t cols, int accum_out) {
+                                                           int64_t cols, int accum_out, const float* scale_a,
+                                                           const float* scale_b) {
     grid_dep_wait();
     grid_dep_launch();
     const int64_t per_tile = 256 * static_cast<int64_t>(bn) / 4;
@@ -754,6 +756,13 @@ __global__ void __launch_bounds__(256) dw_chunk_sum_kernel(const float* __restri
         v.y = __fadd_rn(v.y, w.y);
         v.z = __fadd_rn(v.z, w.z);
         v.w = __fadd_rn(v.w, w.w);
+    }
+    if (scale_a != nullptr) {
+        const float sc = __fmul_rn(__ldg(scale_a), __ldg(scale_b));
+        v.x = __fmul_rn(v.x, sc);
+        v.y = __fmul_rn(v.y, sc);
+        v.z = __fmul_rn(v.z, sc);
+        v.w = __fmul_rn(v.w, sc);
     }
     if (OUT == 2) {
         float4* dst = reinterpret_cast<float4*>(static_cast<float*>(out) + gr * ldo + gc);
@@ -957,7 +966,7 @@ cudaError_t dw_t(const LaunchCtx& c, bi_dtype dt, void* dw, const void* x, const
             const int64_t threads = split_tiles * 256 * BNT / 4;
             e = launch_pdl(dw_chunk_sum_kernel<F32 ? 2 : FMT>, dim3(static_cast<unsigned>((threads + 255) / 256)),
                            dim3(256), 0, c.stream, ws, p.split_from, sp, static_cast<int>(split_tiles), units_m,
-                           p.num_n, BNT, dw, p.ldo, p.rows, p.cols, p.accum_out);
+                           p.num_n, BNT, dw, p.ldo, p.rows, p.cols, p.accum_out, nullptr, nullptr);
             if (e != cudaSuccess) return e;
             c.count();
         }
@@ -1036,7 +1045,8 @@ cudaError_t make_map8(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t 
 
 template <int OUT>
 cudaError_t fp8_pass_t(const LaunchCtx& c, int pass, void* out, const uint8_t* a, const uint8_t* b,
-                       const void* bias, const float* sa, const float* sb, int64_t M, int64_t K, int64_t N) {
+                       const void* bias, const float* sa, const float* sb, int64_t M, int64_t K, int64_t N,
+                       float* ws) {
     CUtensorMap ma, mb;
     cudaError_t e;
     Params p{};
@@ -1071,7 +1081,26 @@ cudaError_t fp8_pass_t(const LaunchCtx& c, int pass, void* out, const uint8_t* a
         p.num_m = static_cast<int>((K + BM - 1) / BM);
         p.num_n = static_cast<int>((N + BN - 1) / BN);
         p.num_kb = static_cast<int>((len + 127) / 128);
-        if ((e = launch_pair<2, OUT, true, true>(c, ma, mb, p)) != cudaSuccess) return e;
+        // the last wave's tiles in chunks, as for the 16-bit dW
+        const int units_m = (p.num_m + 1) / 2;
+        const int64_t tiles = static_cast<int64_t>(units_m) * p.num_n;
+        const int sp = dw_split(tiles, p.num_kb);
+        if (sp > 1 && ws == nullptr) return cudaErrorInvalidValue;
+        p.split_s = sp;
+        p.split_from = static_cast<int>(sp > 1 ? tiles - tiles % DW_WAVE : tiles);
+        p.partials = ws;
+        const int64_t split_tiles = tiles - p.split_from;
+        if ((e = launch_pair<2, OUT, true, true>(c, ma, mb, p, nullptr, nullptr, p.split_from + split_tiles * sp)) !=
+            cudaSuccess)
+            return e;
+        if (sp > 1) {
+            const int64_t threads = split_tiles * 256 * BN / 4;
+            e = launch_pdl(dw_chunk_sum_kernel<OUT>, dim3(static_cast<unsigned>((threads + 255) / 256)), dim3(256),
+                           0, c.stream, ws, p.split_from, sp, static_cast<int>(split_tiles), units_m, p.num_n, BN,
+                           out, p.ldo, p.rows, p.cols, p.accum_out, sa, sb);
+            if (e != cudaSuccess) return e;
+            c.count();
+        }
     }
     return cudaSuccess;
 }
@@ -1154,13 +1183,20 @@ cudaError_t tc_tf32x3_pass(const LaunchCtx& c, const float* a_hi, const float* a
     return cudaSuccess;
 }
 
+int64_t tc_fp8_dw_workspace_bytes(int out_f32, int64_t M, int64_t K, int64_t N) {
+    const int64_t tiles = ((K + BM - 1) / BM + 1) / 2 * ((N + BN - 1) / BN);
+    const int64_t len = out_f32 ? lmin(M, TC_PIECE_ROWS) : M;  // the first (longest) contraction piece
+    const int sp = dw_split(tiles, (len + 127) / 128);
+    return sp > 1 ? (tiles % DW_WAVE) * sp * 256 * BN * 4 : 0;
+}
+
 cudaError_t tc_fp8_pass(const LaunchCtx& c, int pass, bi_dtype out_dt, void* out, const uint8_t* a,
                        const uint8_t* b, const void* bias, const float* sa, const float* sb, int64_t M,
-                       int64_t K, int64_t N) {
+                       int64_t K, int64_t N, float* ws) {
     switch (out_dt) {
-        case BI_BF16: return fp8_pass_t<1>(c, pass, out, a, b, bias, sa, sb, M, K, N);
-        case BI_F16: return fp8_pass_t<0>(c, pass, out, a, b, bias, sa, sb, M, K, N);
-        default: return fp8_pass_t<2>(c, pass, out, a, b, bias, sa, sb, M, K, N);
+        case BI_BF16: return fp8_pass_t<1>(c, pass, out, a, b, bias, sa, sb, M, K, N, ws);
+        case BI_F16: return fp8_pass_t<0>(c, pass, out, a, b, bias, sa, sb, M, K, N, ws);
+        default: return fp8_pass_t<2>(c, pass, out, a, b, bias, sa, sb, M, K, N, ws);
     }
 }
 

@@ -173,3 +173,27 @@ def test_fp8_dw_f32_in_pieces(eng):
     eng.fp8_backward_dw(dw, xq.cuda(), gq.cuda(), scal(0.5), scal(0.25), m, k, n, "f32")
     eng.check()
     assert np.array_equal(out_np(dw), oracle.fp8_backward_dw(xq.numpy(), gq.numpy(), 0.5, 0.25, m, k, n, "f32"))
+
+
+@pytest.mark.parametrize("out", ["bf16", "f32"])
+def test_fp8_dw_tail_chunks(eng, out):
+    """2048 x 256 x 1024: 4 dW tiles, each contracting as 2 chunks of 1024 rows
+    summed in order, then scaled: within the tolerance, and run to run."""
+    m, k, n = 2048, 256, 1024
+    x = synth.normal((m, k), 1.0, "bf16", 87).cuda()
+    g = synth.normal((m, n), 1.0, "bf16", 88).cuda()
+    xq, _ = quantize(eng, x, 64.0)
+    gq, _ = quantize(eng, g, 64.0)
+    sx = sg = 1 / 64.0
+    dw = torch.empty(k, n, dtype=TD[out], device="cuda")
+    eng.fp8_backward_dw(dw, xq, gq, scal(sx), scal(sg), m, k, n, out)
+    eng.check()
+    got = out_np(dw)
+    xqn, gqn = u8(xq), u8(gq)
+    xv, gv = (oracle.up_e4m3(a).astype(np.float64) for a in (xqn, gqn))
+    r = oracle.fp8_backward_dw(xqn, gqn, sx, sg, m, k, n, "f32")
+    ok, st = check_tc(got, r, (np.abs(xv).T @ np.abs(gv)) * (np.float32(sx) * np.float32(sg)), out)
+    assert ok, st
+    eng.fp8_backward_dw(dw, xq, gq, scal(sx), scal(sg), m, k, n, out)
+    assert np.array_equal(out_np(dw), got)
+
