@@ -225,7 +225,7 @@ def oracle_sample(rows=512, cols=128, seed=0):
 
 
 PAIR_BEGIN = "// ---------------------------------------------------------------- CTA-pair kernel"
-PAIR_END = "// ---------------------------------------------------------------- host side"
+PAIR_END = "// ---------------------------------------------------------------- dW chunk sum"
 
 
 def pair_kernel_sha():

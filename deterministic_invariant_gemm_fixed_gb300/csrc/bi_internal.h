@@ -145,7 +145,7 @@ cudaError_t tc_forward(const LaunchCtx& c, bi_dtype dt, void* y, const void* x, 
 cudaError_t tc_dx(const LaunchCtx& c, bi_dtype dt, void* dx, const void* dy, const void* w,
                   int64_t M, int64_t K, int64_t N);
 // dW: the output tiles of the last, partial wave run their contraction in
-// chunks, summed in order; ws holds their f32 results (tc_dw_workspace_bytes,
+// chunks added by the dW tree; ws holds their f32 results (tc_dw_workspace_bytes,
 // 0 = no split for this shape, ws may be null).
 int64_t tc_dw_workspace_bytes(int dw_f32, int64_t M, int64_t K, int64_t N);
 cudaError_t tc_dw(const LaunchCtx& c, bi_dtype dt, void* dw, int dw_f32, const void* x,

@@ -723,12 +723,22 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
 }
 
-// dW tiles whose contraction ran as chunks: out = (((c_0 + c_1) + c_2) + ...)
-// in chunk order, times *scale_a * *scale_b for FP8 (scales non-null), then for
-// a contraction piece after the first the earlier pieces' sum in out plus
-// that, rounded once to the output type.  One thread per 4 consecutive columns
-// of a tile row.
-template <int OUT>
+// ---------------------------------------------------------------- dW chunk sum
+
+__device__ __forceinline__ float4 add4(const float4 a, const float4 b) {
+    return make_float4(__fadd_rn(a.x, b.x), __fadd_rn(a.y, b.y), __fadd_rn(a.z, b.z), __fadd_rn(a.w, b.w));
+}
+
+// dW tiles whose contraction ran as chunks: the chunks' f32 results c_0 ..
+// c_{s-1} (s <= SMAX, a power of two at most 16) are added by the dW
+// reduction's fixed pairwise tree (adjacent pairs level by level, an odd last
+// entry carried up), all loaded first so the loads overlap and the tree runs
+// in registers; then times *scale_a * *scale_b for FP8 (scales non-null), then
+// for a contraction piece after the first the earlier pieces' sum in out plus
+// that, rounded once to the output type.  One thread per 4 consecutive
+// columns of a tile row.
+constexpr int DW_MAX_CHUNKS = 16;
+template <int OUT, int SMAX>
 __global__ void __launch_bounds__(256) dw_chunk_sum_kernel(const float* __restrict__ partials, int split_from,
                                                            int split_s, int split_tiles, int units_m, int num_n,
                                                            int bn, void* out, int64_t ldo, int64_t rows,
@@ -736,51 +746,59 @@ __global__ void __launch_bounds__(256) dw_chunk_sum_kernel(const float* __restri
                                                            const float* scale_b) {
     grid_dep_wait();
     grid_dep_launch();
-    const int64_t per_tile = 256 * static_cast<int64_t>(bn) / 4;
+    const int64_t slot = 256 * static_cast<int64_t>(bn);
+    const int64_t per_tile = slot / 4;
     const int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
     if (idx >= split_tiles * per_tile) return;
     const int ti = static_cast<int>(idx / per_tile);
-    const int64_t rem = idx - ti * per_tile;
-    const int row = static_cast<int>(rem / (bn / 4));
-    const int c4 = static_cast<int>(rem - static_cast<int64_t>(row) * (bn / 4)) * 4;
+    const int64_t e = (idx - ti * per_tile) * 4;  // row * bn + first column within the tile
+    const int row = static_cast<int>(e / bn), col = static_cast<int>(e - static_cast<int64_t>(row) * bn);
     int mpair, nb;
     dense_raster(split_from + ti, units_m, num_n, mpair, nb);
-    const int64_t gr = static_cast<int64_t>(mpair) * 256 + row, gc = static_cast<int64_t>(nb) * bn + c4;
+    const int64_t gr = static_cast<int64_t>(mpair) * 256 + row, gc = static_cast<int64_t>(nb) * bn + col;
     if (gr >= rows || gc >= cols) return;  // cols is a multiple of 8: the 4 columns are inside
-    const int64_t slot = 256 * static_cast<int64_t>(bn);
-    const float* src = partials + static_cast<int64_t>(ti) * split_s * slot + static_cast<int64_t>(row) * bn + c4;
-    float4 v = *reinterpret_cast<const float4*>(src);
-    for (int j = 1; j < split_s; ++j) {
-        const float4 w = *reinterpret_cast<const float4*>(src + j * slot);
-        v.x = __fadd_rn(v.x, w.x);
-        v.y = __fadd_rn(v.y, w.y);
-        v.z = __fadd_rn(v.z, w.z);
-        v.w = __fadd_rn(v.w, w.w);
+    const float* src = partials + static_cast<int64_t>(ti) * split_s * slot + e;
+    float4 v[SMAX];
+#pragma unroll
+    for (int j = 0; j < SMAX; ++j)
+        v[j] = j < split_s ? *reinterpret_cast<const float4*>(src + j * slot) : make_float4(0.f, 0.f, 0.f, 0.f);
+    int n = split_s;
+#pragma unroll
+    for (int w = SMAX; w > 1; w >>= 1) {
+#pragma unroll
+        for (int i = 0; i < w / 2; ++i) v[i] = (2 * i + 1 < n) ? add4(v[2 * i], v[2 * i + 1]) : v[2 * i];
+        n = (n + 1) / 2;
     }
+    float4 r = v[0];
     if (scale_a != nullptr) {
         const float sc = __fmul_rn(__ldg(scale_a), __ldg(scale_b));
-        v.x = __fmul_rn(v.x, sc);
-        v.y = __fmul_rn(v.y, sc);
-        v.z = __fmul_rn(v.z, sc);
-        v.w = __fmul_rn(v.w, sc);
+        r = make_float4(__fmul_rn(r.x, sc), __fmul_rn(r.y, sc), __fmul_rn(r.z, sc), __fmul_rn(r.w, sc));
     }
     if (OUT == 2) {
         float4* dst = reinterpret_cast<float4*>(static_cast<float*>(out) + gr * ldo + gc);
-        if (accum_out) {
-            const float4 prev = *dst;
-            v.x = __fadd_rn(prev.x, v.x);
-            v.y = __fadd_rn(prev.y, v.y);
-            v.z = __fadd_rn(prev.z, v.z);
-            v.w = __fadd_rn(prev.w, v.w);
-        }
-        *dst = v;
+        *dst = accum_out ? add4(*dst, r) : r;
     } else {
         using O = OutT<OUT == 1 ? 1 : 0>;
         uint2 w;
-        w.x = O::pack(v.x, v.y);
-        w.y = O::pack(v.z, v.w);
+        w.x = O::pack(r.x, r.y);
+        w.y = O::pack(r.z, r.w);
         *reinterpret_cast<uint2*>(static_cast<typename O::T*>(out) + gr * ldo + gc) = w;
     }
+}
+
+template <int OUT>
+cudaError_t launch_chunk_sum(const LaunchCtx& c, const float* ws, int split_from, int sp, int64_t split_tiles,
+                             int units_m, int num_n, int bn, void* out, int64_t ldo, int64_t rows, int64_t cols,
+                             int accum_out, const float* sa, const float* sb) {
+    auto kern = sp <= 2 ? dw_chunk_sum_kernel<OUT, 2>
+              : sp <= 4 ? dw_chunk_sum_kernel<OUT, 4>
+              : sp <= 8 ? dw_chunk_sum_kernel<OUT, 8> : dw_chunk_sum_kernel<OUT, 16>;
+    const int64_t threads = split_tiles * 256 * bn / 4;
+    cudaError_t e = launch_pdl(kern, dim3(static_cast<unsigned>((threads + 255) / 256)), dim3(256), 0, c.stream, ws,
+                               split_from, sp, static_cast<int>(split_tiles), units_m, num_n, bn, out, ldo, rows,
+                               cols, accum_out, sa, sb);
+    if (e == cudaSuccess) c.count();
+    return e;
 }
 
 // ---------------------------------------------------------------- host side
@@ -910,15 +928,15 @@ bool narrow_dw(int64_t K, int64_t N) { return ((K + 255) / 256) * ((N + 255) / 2
 // dW's output tiles do not depend on M, and its contraction is the batch: the
 // tiles of the last, partial wave (on a 152-SM GPU's 76 CTA pairs) run their
 // contraction as s chunks of consecutive 64-row blocks, s pairs per tile, and
-// dw_chunk_sum_kernel adds the chunks in order.  s = min(76 / tail tiles,
-// blocks / 8), a function of M, K and N only; 1 = no split.  Y and dX are
+// dw_chunk_sum_kernel adds the chunks by the dW tree.  s = min(76 / tail tiles,
+// 16, blocks / 8), a function of M, K and N only; 1 = no split.  Y and dX are
 // never split: their rows must not depend on M.
 constexpr int64_t DW_WAVE = 76;
 constexpr int64_t DW_MIN_CHUNK_KB = 8;
 int dw_split(int64_t tiles, int64_t nkb) {
     const int64_t tail = tiles % DW_WAVE;
     if (tail == 0) return 1;
-    const int64_t sp = lmin(DW_WAVE / tail, nkb / DW_MIN_CHUNK_KB);
+    const int64_t sp = lmin(lmin(DW_WAVE / tail, DW_MAX_CHUNKS), nkb / DW_MIN_CHUNK_KB);
     return sp >= 2 ? static_cast<int>(sp) : 1;
 }
 struct DwShape {
@@ -962,14 +980,10 @@ cudaError_t dw_t(const LaunchCtx& c, bi_dtype dt, void* dw, const void* x, const
                                                                           p.split_from + split_tiles * sp)) !=
             cudaSuccess)
             return e;
-        if (sp > 1) {
-            const int64_t threads = split_tiles * 256 * BNT / 4;
-            e = launch_pdl(dw_chunk_sum_kernel<F32 ? 2 : FMT>, dim3(static_cast<unsigned>((threads + 255) / 256)),
-                           dim3(256), 0, c.stream, ws, p.split_from, sp, static_cast<int>(split_tiles), units_m,
-                           p.num_n, BNT, dw, p.ldo, p.rows, p.cols, p.accum_out, nullptr, nullptr);
-            if (e != cudaSuccess) return e;
-            c.count();
-        }
+        if (sp > 1 && (e = launch_chunk_sum<F32 ? 2 : FMT>(c, ws, p.split_from, sp, split_tiles, units_m, p.num_n, BNT,
+                                                           dw, p.ldo, p.rows, p.cols, p.accum_out, nullptr,
+                                                           nullptr)) != cudaSuccess)
+            return e;
     }
     return cudaSuccess;
 }
@@ -1093,14 +1107,9 @@ cudaError_t fp8_pass_t(const LaunchCtx& c, int pass, void* out, const uint8_t* a
         if ((e = launch_pair<2, OUT, true, true>(c, ma, mb, p, nullptr, nullptr, p.split_from + split_tiles * sp)) !=
             cudaSuccess)
             return e;
-        if (sp > 1) {
-            const int64_t threads = split_tiles * 256 * BN / 4;
-            e = launch_pdl(dw_chunk_sum_kernel<OUT>, dim3(static_cast<unsigned>((threads + 255) / 256)), dim3(256),
-                           0, c.stream, ws, p.split_from, sp, static_cast<int>(split_tiles), units_m, p.num_n, BN,
-                           out, p.ldo, p.rows, p.cols, p.accum_out, sa, sb);
-            if (e != cudaSuccess) return e;
-            c.count();
-        }
+        if (sp > 1 && (e = launch_chunk_sum<OUT>(c, ws, p.split_from, sp, split_tiles, units_m, p.num_n, BN, out,
+                                                 p.ldo, p.rows, p.cols, p.accum_out, sa, sb)) != cudaSuccess)
+            return e;
     }
     return cudaSuccess;
 }

@@ -370,11 +370,14 @@ def test_launch_count_counts_kernels(eng):
 
 @pytest.mark.parametrize("dtype", ["bf16", "f16"])
 def test_tc_dw_tail_tiles_in_chunks(eng, dtype):
-    """dW tiles of the last, partial wave run their contraction as chunks summed
-    in order.  1024 x 2048 x 2560: 80 tiles of 256 x 256, the last 4 (rows
+    """dW tiles of the last, partial wave run their contraction as chunks added
+    by the dW tree.  1024 x 2048 x 2560: 80 tiles of 256 x 256, the last 4 (rows
     1024-2047, columns 2304-2559) in 2 chunks of 512 rows; checked there and on
     whole tiles, f32 and rounded, and run to run.  2048 x 256 x 2048: 16 tiles of
-    256 x 128, each in 4 chunks, exact on small integers."""
+    256 x 128, each in 4 chunks of 512 rows, exact on small integers, and the
+    chunk order: chunk results 2^24, 1, 1, -2^24 give (c0 + c1) + (c2 + c3) = 1
+    by the pairwise tree (2^24 + 1 rounds to 2^24), where adding them one by
+    one would give 0."""
     m, k, n = 1024, 2048, 2560
     x, _, dy, _ = synth.dense_inputs(m, k, n, dtype, b=None)
     got = run_dense(eng, x, None, dy, None, m, k, n, dtype, tc=1, passes=("dw",))
@@ -396,6 +399,17 @@ def test_tc_dw_tail_tiles_in_chunks(eng, dtype):
     gi = synth.small_ints((m, n), -2, 2, dtype, 98)  # every partial sum exact in f32
     got = run_dense(eng, xi, None, gi, None, m, k, n, dtype, tc=1, passes=("dw",))
     assert np.array_equal(got["dw"], oracle.backward_dw(synth.to_np(xi), synth.to_np(gi), m, k, n, dtype, dw_f32=True))
+    k0, n0 = 5, 700
+    xa, ga = np.zeros((m, k)), np.zeros((m, n))
+    xa[:512, k0], ga[:512, n0] = 64.0, 512.0          # chunk 0: 512 * 2^15 = 2^24, every partial sum exact
+    xa[600, k0], ga[600, n0] = 1.0, 1.0                # chunk 1: 1
+    xa[1100, k0], ga[1100, n0] = 1.0, 1.0              # chunk 2: 1
+    xa[1536:, k0], ga[1536:, n0] = 64.0, -512.0        # chunk 3: -2^24
+    xt, gt = (torch.from_numpy(a).to(synth.TORCH_DTYPES[dtype]) for a in (xa, ga))  # all values exact
+    got = run_dense(eng, xt, None, gt, None, m, k, n, dtype, tc=1, passes=("dw",))
+    want = np.zeros((k, n), dtype=np.float32)
+    want[k0, n0] = 1.0
+    assert np.array_equal(got["dw"], want)
 
 
 @pytest.mark.parametrize("dtype", ["bf16", "f16"])

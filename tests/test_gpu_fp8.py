@@ -178,7 +178,7 @@ def test_fp8_dw_f32_in_pieces(eng):
 @pytest.mark.parametrize("out", ["bf16", "f32"])
 def test_fp8_dw_tail_chunks(eng, out):
     """2048 x 256 x 1024: 4 dW tiles, each contracting as 2 chunks of 1024 rows
-    summed in order, then scaled: within the tolerance, and run to run."""
+    added by the dW tree, then scaled: within the tolerance, and run to run."""
     m, k, n = 2048, 256, 1024
     x = synth.normal((m, k), 1.0, "bf16", 87).cuda()
     g = synth.normal((m, n), 1.0, "bf16", 88).cuda()
