@@ -407,6 +407,15 @@ def secondary(eng, stream, reps=5):
     t_g = timeit(gemv)
     out["gemv_tc_f16"] = {"workload": "f16 1x4096x4096", "gbs": (k * n * 2 + k * 2 + n * 2) / t_g / 1e9,
                           "us": t_g * 1e6}
+
+    # the same GEMV on the scalar tier (one lane per output column, bit-exact chains)
+    def gemv_scalar():
+        eng.forward(yv, xv, ws[state["i"] % 8], None, 1, k, n, "f16", stream, 0)
+        state["i"] += 1
+    t_gs = timeit(gemv_scalar)
+    out["gemv_scalar_f16"] = {"workload": "f16 1x4096x4096 (scalar tier)",
+                              "gbs": (k * n * 2 + k * 2 + n * 2) / t_gs / 1e9, "us": t_gs * 1e6,
+                              "chain_bound_us": k * 4 / 2.07e3}
     return out
 
 

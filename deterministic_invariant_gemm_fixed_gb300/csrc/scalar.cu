@@ -38,14 +38,17 @@ constexpr int TM = 128, TN = 128, TK = 16, NT = 256, PAD = 4;
 
 template <typename T> struct Elem;
 template <> struct Elem<float> {
+    static constexpr bool is_bf16 = false;
     static __device__ __forceinline__ float up(float v) { return v; }
     static __device__ __forceinline__ float down(float v) { return v; }
 };
 template <> struct Elem<__nv_bfloat16> {
+    static constexpr bool is_bf16 = true;
     static __device__ __forceinline__ float up(__nv_bfloat16 v) { return __bfloat162float(v); }
     static __device__ __forceinline__ __nv_bfloat16 down(float v) { return __float2bfloat16_rn(v); }
 };
 template <> struct Elem<__half> {
+    static constexpr bool is_bf16 = false;
     static __device__ __forceinline__ float up(__half v) { return __half2float(v); }
     static __device__ __forceinline__ __half down(float v) { return __float2half_rn(v); }
 };
@@ -660,6 +663,158 @@ __global__ void __launch_bounds__(NT, 2) scalar_dw_chunk_kernel(const DwArgs p) 
     }
 }
 
+// Outputs of at most SK_R rows (a matrix-vector product, or a few rows): one
+// warp per 64 output columns, two columns per lane advanced together by the
+// paired FMA, one accumulator per row and column, each the same chain as
+// above (fmaf over l ascending from +0, then (+ bias) and one rounding).  The
+// parallelism is one chain per output, so the chain's per-step latency and
+// the instructions one warp issues per step bound the kernel.  Operands stream
+// through a deep cp.async ring of raw 64-step blocks (each lane copies fixed
+// 16-byte units whose addresses advance by a fixed stride), and the A steps of
+// a block are widened once into shared memory, each stored twice so that one
+// 16-byte load gives two (a, a) pairs.  A lane owns columns 2 lane and
+// 2 lane + 1 when B is [step][column] (one 32-bit load per step), lane and
+// lane + 32 when B is [column][step] (16-byte loads of 8 steps, conflict-free
+// at the 144-byte row pitch).  Requires 16-byte aligned rows of whole 16-byte
+// units.
+constexpr int SK_R = 4;        // most output rows
+constexpr int SK_STEPS = 64;   // contraction steps per stage (= columns per warp)
+template <typename T>
+__host__ __device__ constexpr int sk_stages() { return sizeof(T) == 4 ? 10 : 16; }
+template <typename T>
+struct SkinnyStage {
+    static constexpr int PADE = 16 / sizeof(T);
+    T b[64][64 + PADE];  // [step][column], or [column][step] when B is contraction-contiguous
+    T a[SK_R][SK_STEPS];
+};
+
+// Two adjacent elements at p (4-byte aligned for 16-bit types, 8 for f32),
+// widened: (first, second) as the low and high lanes of a paired-FMA operand.
+template <typename T>
+__device__ __forceinline__ uint64_t widen_pair(const T* p) {
+    if (sizeof(T) == 4) return *reinterpret_cast<const uint64_t*>(p);
+    const uint32_t w = *reinterpret_cast<const uint32_t*>(p);
+    uint32_t lo, hi;
+    if (sizeof(T) == 2 && Elem<T>::is_bf16) {  // bf16: the high half of an f32
+        lo = w << 16;
+        hi = w & 0xffff0000u;
+    } else {
+        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w));
+        lo = __float_as_uint(f.x);
+        hi = __float_as_uint(f.y);
+    }
+    return (static_cast<uint64_t>(hi) << 32) | lo;
+}
+
+template <typename T, bool BT, int RR>  // RR: rows computed (R <= RR <= SK_R)
+__global__ void __launch_bounds__(32) scalar_rows_skinny_kernel(const RowsArgs p) {
+    constexpr int STAGES = sk_stages<T>();
+    using Stage = SkinnyStage<T>;
+    extern __shared__ __align__(16) uint8_t smem_sk[];
+    Stage* ring = reinterpret_cast<Stage*>(smem_sk);
+    uint64_t(*aw)[SK_STEPS] = reinterpret_cast<uint64_t(*)[SK_STEPS]>(smem_sk + STAGES * sizeof(Stage));
+    const int lane = threadIdx.x;
+    const T* A = static_cast<const T*>(p.a);
+    const T* B = static_cast<const T*>(p.b);
+    const int64_t R = p.R, L = p.L, C = p.C;
+    const int64_t c0 = static_cast<int64_t>(blockIdx.x) * 64;
+    constexpr int U = 16 / sizeof(T);   // elements per 16-byte unit
+    constexpr int UPR = 64 / U;         // units per 64-element row of a stage
+    constexpr int RPI = 32 / UPR;       // stage rows one pass of the warp covers
+    constexpr int NB = 64 / RPI;        // B units per lane per stage
+    const int useg = (lane % UPR) * U, urow = lane / UPR;
+    // B unit i of this lane: stage row urow + RPI i, elements useg .. useg + U - 1
+    const T* bp = BT ? B + (c0 + urow) * L + useg : B + urow * C + c0 + useg;
+    const int64_t brow = BT ? RPI * L : RPI * C;   // between this lane's units
+    const int64_t bstage = BT ? SK_STEPS : SK_STEPS * C;
+    uint32_t brow_ok = 0;  // BT: output rows of B inside C
+    if (BT) {
+#pragma unroll
+        for (int i = 0; i < NB; ++i) brow_ok |= (c0 + urow + RPI * i < C ? 1u : 0u) << i;
+    }
+    const bool bcol_ok = BT || c0 + useg < C;
+    const int64_t nkb = (L + SK_STEPS - 1) / SK_STEPS;
+    auto issue = [&](int64_t kb) {
+        Stage& st = ring[kb % STAGES];
+        const int64_t l0 = kb * SK_STEPS;
+        const T* q = bp + kb * bstage;
+#pragma unroll
+        for (int i = 0; i < NB; ++i) {
+            const int row = urow + RPI * i;
+            const bool ok = BT ? (((brow_ok >> i) & 1u) != 0 && l0 + useg < L) : (bcol_ok && l0 + row < L);
+            cp_async16(&st.b[row][useg], ok ? q + i * brow : B, ok ? 16u : 0u);
+        }
+        for (int u = lane; u < SK_R * UPR; u += 32) {
+            const int r = u / UPR, sg = (u % UPR) * U;
+            const bool ok = r < R && l0 + sg < L;
+            cp_async16(&st.a[r][sg], ok ? A + r * L + l0 + sg : A, ok ? 16u : 0u);
+        }
+    };
+    // prologue: STAGES - 1 blocks in flight (empty groups keep the count)
+    for (int64_t kb = 0; kb < STAGES - 1; ++kb) {
+        if (kb < nkb) issue(kb);
+        cp_async_commit();
+    }
+    uint64_t acc[RR];
+#pragma unroll
+    for (int r = 0; r < RR; ++r) acc[r] = 0;  // (+0, +0)
+    for (int64_t kb = 0; kb < nkb; ++kb) {
+        cp_async_wait<STAGES - 2>();
+        __syncwarp();  // block kb has landed for every lane; block kb - 1 is no longer read
+        if (kb + STAGES - 1 < nkb) issue(kb + STAGES - 1);
+        cp_async_commit();
+        const Stage& st = ring[kb % STAGES];
+        for (int u = lane; u < RR * SK_STEPS; u += 32) {
+            const uint32_t v = __float_as_uint(Elem<T>::up(st.a[u / SK_STEPS][u % SK_STEPS]));
+            aw[u / SK_STEPS][u % SK_STEPS] = (static_cast<uint64_t>(v) << 32) | v;
+        }
+        __syncwarp();
+#pragma unroll
+        for (int l8 = 0; l8 < SK_STEPS; l8 += 8) {
+            uint64_t w[8];  // (column 0, column 1) of this lane at each of 8 steps
+            if (BT) {
+                float f0[8], f1[8];
+                smem_load8(&st.b[lane][l8], f0);
+                smem_load8(&st.b[lane + 32][l8], f1);
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    w[j] = (static_cast<uint64_t>(__float_as_uint(f1[j])) << 32) | __float_as_uint(f0[j]);
+            } else {
+#pragma unroll
+                for (int j = 0; j < 8; ++j) w[j] = widen_pair(&st.b[l8 + j][2 * lane]);
+            }
+#pragma unroll
+            for (int r = 0; r < RR; ++r) {
+                uint64_t av[8];
+#pragma unroll
+                for (int j = 0; j < 8; j += 2) {
+                    const ulonglong2 x = *reinterpret_cast<const ulonglong2*>(&aw[r][l8 + j]);
+                    av[j] = x.x;
+                    av[j + 1] = x.y;
+                }
+#pragma unroll
+                for (int j = 0; j < 8; ++j) fma2(acc[r], av[j], w[j]);
+            }
+        }
+        __syncwarp();  // aw is rewritten for the next block
+    }
+    cp_async_wait<0>();
+    T* out = static_cast<T*>(p.out);
+    const T* bias = static_cast<const T*>(p.bias);
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        const int64_t c = BT ? c0 + lane + 32 * h : c0 + 2 * lane + h;
+        if (c >= C) continue;
+        const float bc = bias != nullptr ? Elem<T>::up(bias[c]) : 0.0f;
+#pragma unroll
+        for (int r = 0; r < RR; ++r) {
+            if (r >= R) break;
+            const float a = __uint_as_float(static_cast<uint32_t>(h ? (acc[r] >> 32) : acc[r]));
+            out[r * C + c] = Elem<T>::down(bias != nullptr ? __fadd_rn(a, bc) : a);
+        }
+    }
+}
+
 // Chunk chains for outputs at most 64 columns wide: 16 x 64 tiles on 256
 // threads, 2 x 2 outputs per thread, one CTA per (tile, chunk).  Same chains as
 // scalar_dw_chunk_kernel (rows of the chunk ascending from +0).  Dense only.
@@ -907,6 +1062,33 @@ unsigned tree_grid(int64_t n, int sm) {
 }  // namespace
 
 template <typename T>
+bool skinny_ok(const RowsArgs& a) {
+    const int64_t unit = 16 / sizeof(T);
+    return aligned16(a.a) && aligned16(a.b) && a.L % unit == 0 && a.C % unit == 0;
+}
+
+template <typename T, bool BT, int RR>
+cudaError_t launch_skinny(const LaunchCtx& c, const RowsArgs& a) {
+    const size_t bytes = sk_stages<T>() * sizeof(SkinnyStage<T>) + SK_R * SK_STEPS * sizeof(uint64_t);
+    const cudaError_t e = allow_smem<scalar_rows_skinny_kernel<T, BT, RR>>(c, bytes);
+    if (e != cudaSuccess) return e;
+    scalar_rows_skinny_kernel<T, BT, RR><<<static_cast<unsigned>((a.C + 63) / 64), 32, bytes, c.stream>>>(a);
+    return cudaSuccess;
+}
+
+template <typename T>
+cudaError_t rows_skinny_t(const LaunchCtx& c, const RowsArgs& a, int bt) {
+    cudaError_t e;
+    if (bt) e = a.R <= 1 ? launch_skinny<T, true, 1>(c, a) : a.R <= 2 ? launch_skinny<T, true, 2>(c, a)
+                                                                      : launch_skinny<T, true, 4>(c, a);
+    else e = a.R <= 1 ? launch_skinny<T, false, 1>(c, a) : a.R <= 2 ? launch_skinny<T, false, 2>(c, a)
+                                                                     : launch_skinny<T, false, 4>(c, a);
+    if (e != cudaSuccess) return e;
+    c.count();
+    return cudaGetLastError();
+}
+
+template <typename T>
 cudaError_t rows_narrow_t(const LaunchCtx& c, const RowsArgs& a, int bt) {
     const dim3 grid(static_cast<unsigned>((a.R + NW_TM - 1) / NW_TM));
     if (bt) scalar_rows_narrow_kernel<T, true><<<grid, 256, 0, c.stream>>>(a);
@@ -918,6 +1100,13 @@ cudaError_t rows_narrow_t(const LaunchCtx& c, const RowsArgs& a, int bt) {
 cudaError_t scalar_rows(const LaunchCtx& c, bi_dtype dt, void* out, const void* a, const void* b,
                         const void* bias, int64_t R, int64_t L, int64_t C, int b_contr_contig) {
     RowsArgs args{out, a, b, bias, R, L, C, 0, nullptr, nullptr};
+    if (C > NW_TN && R <= SK_R) {  // a few rows: one lane per output column (the kernel changes no chain)
+        switch (dt) {
+            case BI_F32: if (skinny_ok<float>(args)) return rows_skinny_t<float>(c, args, b_contr_contig); break;
+            case BI_BF16: if (skinny_ok<__nv_bfloat16>(args)) return rows_skinny_t<__nv_bfloat16>(c, args, b_contr_contig); break;
+            default: if (skinny_ok<__half>(args)) return rows_skinny_t<__half>(c, args, b_contr_contig); break;
+        }
+    }
     if (C <= NW_TN) {  // narrow output: the tile shape changes no chain
         switch (dt) {
             case BI_F32: return rows_narrow_t<float>(c, args, b_contr_contig);

@@ -78,6 +78,21 @@ def test_scalar_tier_bit_exact(eng, case):
     assert np.array_equal(got2["dw"], oracle.backward_dw(xn, dyn, m, k, n, dtype, dw_f32=False))
 
 
+@pytest.mark.parametrize("dtype", ["f32", "bf16", "f16"])
+@pytest.mark.parametrize("m", [1, 2, 3, 4])
+def test_scalar_skinny_rows_bit_exact(eng, dtype, m):
+    """Batches of at most 4 rows take one lane per output column (forward and
+    dX): bit-exact with the oracle, with a ragged last column tile (136, 200
+    columns), a contraction shorter than one 64-step stage, and one of 81
+    stages that wraps the 16-stage ring."""
+    for k, n in ((200, 136), (5184, 264), (32, 72)):
+        x, w, dy, b = synth.dense_inputs(m, k, n, dtype)
+        got = run_dense(eng, x, w, dy, b, m, k, n, dtype, tc=0, passes=("y", "dx"))
+        xn, wn, dyn, bn = np_in(x, w, dy, b)
+        assert np.array_equal(got["y"], oracle.forward(xn, wn, bn, m, k, n, dtype)), (k, n)
+        assert np.array_equal(got["dx"], oracle.backward_dx(dyn, wn, m, k, n, dtype)), (k, n)
+
+
 @pytest.mark.parametrize("case", SCALAR_CASES, ids=lambda c: c[0])
 def test_tc_flag_on_scalar_shapes_is_scalar(eng, case):
     """With tensor_cores=1, passes whose shape the dispatcher keeps on the scalar
