@@ -36,12 +36,17 @@
  * Tensor-core tier (tensor_cores = 1, bf16/f16, non-M output dims >= 64, K and
  * N multiples of 8, 16-byte aligned pointers): tcgen05 MMA, f32 accumulation
  * in tensor memory, contracted index processed in fixed 64-wide blocks in
- * ascending order, no split of the contraction, no atomics, and no tile,
- * order or instruction choice that depends on M.  Results are bit-identical
- * across runs and per row for any M, and within the published tolerance of the
- * scalar tier (they are not bit-equal to it).  dW and grouped dweights chain
- * the row blocks in ascending order inside the accumulator (the degenerate,
- * single-chunk case of the fixed tree).
+ * ascending order, no atomics.  Y and dX never split their contraction and
+ * make no tile, order or instruction choice that depends on M, so each of
+ * their rows is bit-identical for any M.  dW and the grouped dweights chain
+ * the row blocks in ascending order inside the accumulator; an f32 result
+ * over more than 8192 rows is taken in pieces of 8192 rows counted from row 0,
+ * each added to the sum of the pieces before it.  A dense dW whose K x N
+ * output tiles leave a partial last wave on 76 CTA pairs contracts each of
+ * those tiles as up to 16 chunks of consecutive 64-row blocks, added by the
+ * dW reduction's fixed pairwise tree (the choice depends on M, K and N only).
+ * Results are bit-identical across runs and within the published tolerance
+ * of the scalar tier (they are not bit-equal to it).
  *
  * f32 operands on the tensor-core tier (dense passes, K and N multiples of 4)
  * run as 3xTF32: each operand x is split into hi = tf32(x) and
