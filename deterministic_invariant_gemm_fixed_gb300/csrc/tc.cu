@@ -1,8 +1,9 @@
 // Tensor-core tier: persistent, warp-specialised tcgen05 GEMM kernels for sm_103a.
 //
 // Contract (sgemm-bi 0.1.1.post2, "Determinism contracts", row "tensor cores"):
-// f32 accumulation, bit-identical across runs, each output row independent of M.
-// Every arithmetic choice is fixed by (pass, dtype, K, N):
+// f32 accumulation, bit-identical across runs, each output row of Y and dX
+// independent of M.  Every arithmetic choice for Y and dX is fixed by
+// (pass, dtype, K, N):
 //   - every pass, dense and grouped, runs tcgen05.mma.cta_group::2 M256 x N256
 //     on a CTA pair (tc_gemm_pair_kernel; K16 per instruction for bf16/f16),
 //     except a 16-bit dW whose K x N output has few 256 x 256 tiles, which runs
@@ -10,9 +11,12 @@
 //     memory;
 //   - the contracted index is walked in 64-wide blocks in ascending order, four
 //     K16 instructions per block, accumulating into the same TMEM tile;
-//   - no split of the contraction, no atomics, no stream-K;
-//   - M only decides how many tiles exist and which CTA runs which tile, which
-//     cannot change the arithmetic of any output element.
+//   - Y and dX never split their contraction; no atomics, no stream-K;
+//   - M only decides how many tiles of Y and dX exist and which CTA runs which
+//     tile, which cannot change the arithmetic of any output element.
+// dW contracts over M itself: a result kept in f32 takes pieces of 8192 rows,
+// and the tiles of its last, partial wave contract in chunks added by the dW
+// reduction's fixed pairwise tree (chosen from M, K and N; dw_split).
 //
 // Roles (192 threads per CTA):
 //   warp 0 lane 0  TMA producer: cp.async.bulk.tensor loads into a ring of stages
