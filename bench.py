@@ -495,7 +495,17 @@ def our_arm(args, rank, world):
     total_t = sum(d["t"] for d in per.values())
     dom = max(per, key=lambda p: per[p]["t"])
     pk, pk_kind = peaks()
-    peak = float(pk.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    burst = float(pk.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    sustained = float(pk.get("bf16_tflops_sustained", burst))
+    # The denominator follows the regime of the timed region: back-to-back dense
+    # GEMMs reach the power cap within a fraction of a second (measured: 40
+    # steps, 0.2 s, ran 6-7 % below 10 steps on one box, with sw_power_cap
+    # active), so a region of 0.1 s or more is compared with the sustained
+    # (power-capped) figure and a shorter one with the burst figure.
+    long_region = elapsed >= 0.1
+    peak = sustained if long_region else burst
+    peak_source = (f"{pk_kind} bf16_tflops_sustained (timed region {elapsed:.3f} s: power-capped regime)"
+                   if long_region else f"{pk_kind} bf16_tflops (burst; timed region {elapsed:.3f} s)")
     d = per[dom]
     achieved = d["fl"] / d["n"] / (d["t"] / d["n"]) / 1e12
     kernel_tag = {"fwd": "tc_gemm_pair_kernel fwd (A K-major, B MN-major)",
@@ -582,8 +592,8 @@ def our_arm(args, rank, world):
                        "parallelism": "replicas" if world > 1 else "single GPU"},
             "roofline": {"bound": "tensor", "kernel": kernel_tag, "achieved": achieved, "peak": peak,
                          "unit": "TFLOP/s", "frac": achieved / peak, "traffic": traffic,
-                         "peak_source": f"{pk_kind} bf16_tflops (burst; each launch is well under 1 s)",
-                         "frac_of_sustained": achieved / float(pk.get("bf16_tflops_sustained", peak))},
+                         "peak_source": peak_source,
+                         "frac_of_burst": achieved / burst, "frac_of_sustained": achieved / sustained},
             "step_frac_of_peak": value / world / peak,
             "passes": passes,
             "cpu_baseline": cpu,
