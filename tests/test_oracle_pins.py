@@ -8,7 +8,10 @@
 * the forward error bound of a recursive sum (gamma_L times the sum of |a*b|);
 * finite differences of f = sum(Y * G), which fix the gradient formulas and
   operand layouts of dX, dW and the grouped passes;
-* invariants (row-prefix invariance, grouped E=1 equals dense, padding rows).
+* invariants (row-prefix invariance, grouped E=1 equals dense, padding rows);
+* brute force on every shape up to 3 x 3 x 3: each fused multiply-add of the
+  chain evaluated in exact rational arithmetic and rounded to nearest-even
+  f32, then the bias add and the output rounding the same way.
 """
 import math
 
@@ -542,3 +545,108 @@ def test_fp8_matmuls_exact_on_small_integers(out):
         assert np.array_equal(dw, round_exact((xi.T @ gi) * sx * sg, out))
     rows = [3, 0, 39]
     assert np.array_equal(oracle.fp8_forward(xq, wq, bias, sx, sw, m, k, n, out, rows=rows), y[rows])
+
+
+# --------------------------------------------------------------------------- brute force, tiny shapes
+
+from fractions import Fraction  # noqa: E402
+
+_FMT = {"f32": (24, -126), "bf16": (8, -126), "f16": (11, -14)}  # significand bits, least normal exponent
+
+
+def round_ne(q, dtype):
+    """Exact rational q rounded to the nearest value of the format, ties to
+    even (subnormals included; no overflow at these sizes)."""
+    if q == 0:
+        return Fraction(0)
+    p, emin = _FMT[dtype]
+    a = abs(q)
+    e = a.numerator.bit_length() - a.denominator.bit_length()  # 2^e <= a < 2^(e+2)
+    if Fraction(2) ** e > a:
+        e -= 1
+    if Fraction(2) ** (e + 1) <= a:
+        e += 1
+    ulp = Fraction(2) ** (max(e, emin) - (p - 1))
+    t = a / ulp
+    n = t.numerator // t.denominator
+    r = t - n
+    if r > Fraction(1, 2) or (r == Fraction(1, 2) and n % 2 == 1):
+        n += 1
+    return (n * ulp) if q > 0 else -(n * ulp)
+
+
+def test_round_ne_matches_numpy_conversions():
+    """The exact rounding helper agrees with numpy's own f32 and f16
+    conversions (round to nearest even), normals and subnormals."""
+    rng = np.random.default_rng(7)
+    vals = np.concatenate([rng.normal(size=2000) * np.exp2(rng.integers(-30, 30, size=2000)),
+                           rng.normal(size=500) * 2.0 ** -140, rng.normal(size=500) * 2.0 ** -20])
+    for v in vals:
+        assert round_ne(Fraction(float(v)), "f32") == Fraction(float(np.float32(v)))
+        if abs(v) < 60000:
+            assert round_ne(Fraction(float(v)), "f16") == Fraction(float(np.float16(v)))
+
+
+def chain_exact(avals, bvals):
+    """acc = +0; acc = round_f32(a_l * b_l + acc) for l ascending."""
+    acc = Fraction(0)
+    for a, b in zip(avals, bvals):
+        acc = round_ne(Fraction(a) * Fraction(b) + acc, "f32")
+    return acc
+
+
+def out_bits(v, dtype):
+    """Encoding of an exactly representable value in the output type."""
+    return enc([float(v)], dtype)[0] if dtype != "f32" else np.float32(float(v))
+
+
+@pytest.mark.parametrize("dtype", DT)
+def test_brute_force_tiny_shapes(dtype):
+    rng = np.random.default_rng(2024)
+    for m in (1, 2, 3):
+        for k in (1, 2, 3):
+            for n in (1, 2, 3):
+                x = enc(rng.normal(size=(m, k)), dtype)
+                w = enc(rng.normal(size=(k, n)), dtype)
+                dy = enc(rng.normal(size=(m, n)), dtype)
+                b = enc(rng.normal(scale=0.5, size=n), dtype)
+                xv, wv, dyv, bv = dec(x, dtype), dec(w, dtype), dec(dy, dtype), dec(b, dtype)
+                y = oracle.forward(x, w, b, m, k, n, dtype)
+                dx = oracle.backward_dx(dy, w, m, k, n, dtype)
+                dw32 = oracle.backward_dw(x, dy, m, k, n, dtype, dw_f32=True)
+                dwr = oracle.backward_dw(x, dy, m, k, n, dtype, dw_f32=False)
+                for i in range(m):
+                    for j in range(n):
+                        acc = chain_exact(xv[i, :], wv[:, j])
+                        want = round_ne(round_ne(acc + Fraction(bv[j]), "f32"), dtype)
+                        assert y[i, j] == out_bits(want, dtype), ("y", m, k, n, i, j)
+                    for j in range(k):
+                        acc = chain_exact(dyv[i, :], wv[j, :])
+                        assert dx[i, j] == out_bits(round_ne(acc, dtype), dtype), ("dx", m, k, n, i, j)
+                for i in range(k):
+                    for j in range(n):
+                        acc = chain_exact(xv[:, i], dyv[:, j])  # one chunk: the plain chain over rows
+                        assert dw32[i, j] == np.float32(float(acc)), ("dw", m, k, n, i, j)
+                        assert dwr[i, j] == out_bits(round_ne(acc, dtype), dtype), ("dw rounded", m, k, n, i, j)
+
+
+@pytest.mark.parametrize("dtype", DT)
+def test_brute_force_tiny_grouped_forward(dtype):
+    rng = np.random.default_rng(2025)
+    e = 2
+    for m in (1, 2, 3):
+        for k in (1, 2, 3):
+            for n in (1, 2, 3):
+                x = enc(rng.normal(size=(m, k)), dtype)
+                w = enc(rng.normal(size=(e * n * k,)), dtype)  # [E, N, K]
+                ids = rng.integers(0, e + 1, size=m).astype(np.uint32)  # id e: a padding row
+                xv, wv = dec(x, dtype), dec(w, dtype).reshape(e, n, k)
+                y = oracle.grouped_forward(x, w, ids, m, k, n, e, dtype)
+                for i in range(m):
+                    for j in range(n):
+                        if ids[i] >= e:
+                            want = Fraction(0)
+                        else:
+                            want = round_ne(chain_exact(xv[i, :], wv[ids[i], j, :]), dtype)
+                        assert y[i, j] == out_bits(want, dtype), (m, k, n, i, j, int(ids[i]))
+
