@@ -650,3 +650,33 @@ def test_brute_force_tiny_grouped_forward(dtype):
                             want = round_ne(chain_exact(xv[i, :], wv[ids[i], j, :]), dtype)
                         assert y[i, j] == out_bits(want, dtype), (m, k, n, i, j, int(ids[i]))
 
+
+@pytest.mark.parametrize("dtype", DT)
+def test_brute_force_tiny_grouped_backward(dtype):
+    """dinput chains over n with W[e(m)]; dweights chains over the expert's rows
+    in ascending original index (one chunk at these sizes); padding rows give a
+    zero dinput row and touch no dweights; an expert without rows gets zeros."""
+    rng = np.random.default_rng(2026)
+    e = 2
+    for m in (1, 2, 3):
+        for k in (1, 2, 3):
+            for n in (1, 2, 3):
+                x = enc(rng.normal(size=(m, k)), dtype)
+                w = enc(rng.normal(size=(e * n * k,)), dtype)  # [E, N, K]
+                dy = enc(rng.normal(size=(m, n)), dtype)
+                ids = rng.integers(0, e + 1, size=m).astype(np.uint32)
+                xv, wv, dyv = dec(x, dtype), dec(w, dtype).reshape(e, n, k), dec(dy, dtype)
+                dx = oracle.grouped_dinput(w, dy, ids, m, k, n, e, dtype)
+                dw = oracle.grouped_dweights(x, dy, ids, m, k, n, e, dtype)
+                for i in range(m):
+                    for j in range(k):
+                        want = Fraction(0) if ids[i] >= e else round_ne(chain_exact(dyv[i, :], wv[ids[i], :, j]), dtype)
+                        assert dx[i, j] == out_bits(want, dtype), ("dx", m, k, n, i, j)
+                dw = dw.reshape(e, n, k)
+                for g in range(e):
+                    rows = [i for i in range(m) if ids[i] == g]
+                    for j in range(n):
+                        for l in range(k):
+                            acc = chain_exact([dyv[i, j] for i in rows], [xv[i, l] for i in rows])
+                            assert dw[g, j, l] == np.float32(float(acc)), ("dw", m, k, n, g, j, l)
+
