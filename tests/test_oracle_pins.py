@@ -680,3 +680,58 @@ def test_brute_force_tiny_grouped_backward(dtype):
                             acc = chain_exact([dyv[i, j] for i in rows], [xv[i, l] for i in rows])
                             assert dw[g, j, l] == np.float32(float(acc)), ("dw", m, k, n, g, j, l)
 
+
+def e4m3_exact(code):
+    """Value of an e4m3 (fn) code from its fields: sign, 4-bit exponent (bias
+    7), 3-bit mantissa; exponent 0 is subnormal (m * 2^-9)."""
+    code = int(code)
+    sign = -1 if code & 0x80 else 1
+    ex, mant = (code >> 3) & 0xF, code & 0x7
+    if ex == 0:
+        return sign * Fraction(mant, 512)
+    return sign * (1 + Fraction(mant, 8)) * Fraction(2) ** (ex - 7)
+
+
+@pytest.mark.parametrize("out", ["f32", "bf16"])
+def test_brute_force_tiny_fp8_forward(out):
+    """y = rne(round_f32(round_f32(chain * round_f32(sx * sw)) + bias)) with the
+    chain over exactly decoded e4m3 values; every shape up to 3 x 3 x 3."""
+    rng = np.random.default_rng(2027)
+    finite = np.array([c for c in range(256) if (c & 0x7F) != 0x7F], dtype=np.uint8)
+    sx, sw = 0.375, 1.25
+    s32 = round_ne(Fraction(sx) * Fraction(sw), "f32")
+    for m in (1, 2, 3):
+        for k in (1, 2, 3):
+            for n in (1, 2, 3):
+                xq = rng.choice(finite, size=(m, k)).astype(np.uint8)
+                wq = rng.choice(finite, size=(k, n)).astype(np.uint8)
+                bias = enc(rng.normal(size=n), out) if out != "f32" else None
+                y = oracle.fp8_forward(xq, wq, bias, sx, sw, m, k, n, out)
+                bv = dec(bias, out) if bias is not None else None
+                for i in range(m):
+                    for j in range(n):
+                        acc = chain_exact([e4m3_exact(c) for c in xq[i, :]], [e4m3_exact(c) for c in wq[:, j]])
+                        v = round_ne(acc * s32, "f32")
+                        if bv is not None:
+                            v = round_ne(v + Fraction(bv[j]), "f32")
+                        assert y[i, j] == out_bits(round_ne(v, out), out), (m, k, n, i, j)
+
+
+@pytest.mark.parametrize("dtype", DT)
+def test_brute_force_tiny_bias_grad(dtype):
+    """db[n] = ((+0 + dY[0,n]) + dY[1,n]) + ... with f32 additions (one chunk at
+    these sizes), then one rounding unless kept in f32."""
+    rng = np.random.default_rng(2028)
+    for m in (1, 2, 3):
+        for n in (1, 2, 3):
+            dy = enc(rng.normal(size=(m, n)), dtype)
+            dyv = dec(dy, dtype)
+            db32 = oracle.bias_grad(dy, m, n, dtype, out_f32=True)
+            dbr = oracle.bias_grad(dy, m, n, dtype)
+            for j in range(n):
+                acc = Fraction(0)
+                for i in range(m):
+                    acc = round_ne(acc + Fraction(dyv[i, j]), "f32")
+                assert db32[j] == np.float32(float(acc))
+                assert dbr[j] == out_bits(round_ne(acc, dtype), dtype)
+
