@@ -19,6 +19,7 @@ no exchange step); the time is the max over ranks.
 from __future__ import annotations
 
 import argparse
+import datetime
 import hashlib
 import json
 import os
@@ -27,6 +28,7 @@ import statistics
 import subprocess
 import sys
 import threading
+import time
 import time
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
@@ -61,7 +63,10 @@ def peaks():
 # ---------------------------------------------------------------- clocks
 
 class ClockSampler:
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    """nvidia-smi samples (every 50 ms) with their timestamps; started before the
+    warm-up so that it is producing when the timed region begins, and
+    summarised over the samples inside the region's wall-clock window."""
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
@@ -74,7 +79,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                 "--format=csv,noheader,nounits", "-lms", "50"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.t = threading.Thread(target=self._read, daemon=True)
             self.t.start()
@@ -94,27 +99,33 @@ class ClockSampler:
             except subprocess.TimeoutExpired:
                 self.proc.kill()
 
-    def summary(self):
-        if not self.lines:
-            return None
-        sm, mx, reasons = [], None, set()
+    def summary(self, t0=None, t1=None):
+        """Median SM clock, max clock and throttle reasons over the samples whose
+        timestamps lie in [t0, t1] (epoch seconds); without one there, the first
+        sample after t0."""
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
+        rows = []
+        for ln in list(self.lines):
             parts = [p.strip() for p in ln.split(",")]
             if len(parts) < 9:
                 continue
             try:
-                sm.append(float(parts[1]))
-                mx = float(parts[2])
+                ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                rows.append((ts, float(parts[1]), float(parts[2]),
+                             {nm for nm, v in zip(names, parts[5:9]) if v.lower().startswith("active")}))
             except ValueError:
                 continue
-            for nm, v in zip(names, parts[5:9]):
-                if v.lower().startswith("active"):
-                    reasons.add(nm)
-        if not sm:
+        if not rows:
             return None
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
-                "samples": len(sm)}
+        inside = [r for r in rows if t0 is None or t0 <= r[0] <= t1]
+        where = "inside the timed region"
+        if not inside:
+            after = [r for r in rows if r[0] >= t0]
+            inside = after[:1] if after else rows[-1:]
+            where = "first sample after the timed region began (none inside it)"
+        reasons = set().union(*(r[3] for r in inside))
+        return {"sm_mhz": statistics.median(r[1] for r in inside), "sm_max_mhz": inside[-1][2],
+                "reasons": sorted(reasons), "samples": len(inside), "window": where}
 
 
 # ---------------------------------------------------------------- workload
@@ -461,16 +472,17 @@ def our_arm(args, rank, world):
     bufs, m = make_inputs("cuda")
     fl_step = step_flops()
     torch.cuda.synchronize()
-    with torch.cuda.stream(stream):
-        for _ in range(max(3, args.warmup)):
-            run_step(eng, bufs, m, stream)
-    eng.check(stream)
+    with ClockSampler(local) as clk:  # producing samples before the timed region begins
+        with torch.cuda.stream(stream):
+            for _ in range(max(3, args.warmup)):
+                run_step(eng, bufs, m, stream)
+        eng.check(stream)
 
-    # ---- device-resident timing
-    events = []
-    launches0 = eng.launches()
-    barrier()
-    with ClockSampler(local) as clk:
+        # ---- device-resident timing
+        events = []
+        launches0 = eng.launches()
+        barrier()
+        w0 = time.time()
         t0 = torch.cuda.Event(enable_timing=True)
         t1 = torch.cuda.Event(enable_timing=True)
         t0.record(stream)
@@ -478,7 +490,10 @@ def our_arm(args, rank, world):
             run_step(eng, bufs, m, stream, events)
         t1.record(stream)
         t1.synchronize()
+        w1 = time.time()
         barrier()
+        time.sleep(0.12)  # the sample that follows the region's end has been read
+    clocks = clk.summary(w0, w1)
     launches = eng.launches() - launches0
     eng.check(stream)
     elapsed = max_over_ranks(t0.elapsed_time(t1) / 1e3, dist, "cuda")
@@ -600,7 +615,7 @@ def our_arm(args, rank, world):
             "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "steps": e2e_steps, "ms_per_step": e2e_t / e2e_steps * 1e3},
             "gpu_launches": launches,
-            "clocks": clk.summary(),
+            "clocks": clocks,
             "secondary": sec,
         }
         print(json.dumps(line), flush=True)
