@@ -46,6 +46,7 @@ SIGNATURES = {
     "bi_dispatch_tier": (_i32, [_i32, _i32, _i32, _i64, _i64]),
     "bi_launch_count": (_u64, [_p]),
     "bi_engine_set_wait_limit": (_i32, [_p, _u64]),
+    "bi_engine_fail_allocations": (_i32, [_p, _i64]),
     "bi_selftest_wait_timeout": (_i32, [_p, _p]),
     "bi_version": (ctypes.c_char_p, []),
     "bi_grouped_forward_segmented": (_i32, [_p, _p, _p, _p, _p, _i64, _i64, _i64, _i64, _i32, _p, _i32]),
@@ -234,6 +235,10 @@ def bi_launch_count(engine) -> int:
 
 def bi_engine_set_wait_limit(engine, nanoseconds: int) -> int:
     return _lib.bi_engine_set_wait_limit(engine, int(nanoseconds))
+
+
+def bi_engine_fail_allocations(engine, count: int) -> int:
+    return _lib.bi_engine_fail_allocations(engine, int(count))
 
 
 def bi_selftest_wait_timeout(engine, stream=None) -> int:

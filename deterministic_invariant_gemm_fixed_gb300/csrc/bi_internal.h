@@ -18,6 +18,7 @@ struct bi_engine_s {
     uint64_t wait_limit_ns = 2000000000ull; // bounded device-side waits
     cudaStream_t side = nullptr;            // engine-owned stream for independent work within a call
     std::atomic<uint64_t> launches{0};
+    std::atomic<int64_t> failing_allocs{0}; // injected scratch-allocation failures still to give (-1 = all)
     std::mutex mu;                          // guards last_error
     std::string last_error;
 };
@@ -194,6 +195,13 @@ cudaError_t fp8_quantize(const LaunchCtx& c, bi_dtype dt, uint8_t* q, float* ama
 }  // namespace bi
 
 namespace bi {
+// Size limits every matmul entry point applies before it enqueues anything:
+// BI_ERR_INVALID_ARG for a bad dtype, m < 0 or k, n <= 0 (e <= 0 for the
+// grouped calls, e < 0 means "not grouped"), BI_ERR_UNSUPPORTED for sizes
+// beyond the kernels' indexing (2^31 - 1 per dimension, k and n at most
+// 8388480, e at most 65535, the grouped calls' U32 element counts).  Returns
+// BI_OK or the status, with the reason in *why.
+bi_status check_sizes(bi_dtype dt, int64_t m, int64_t k, int64_t n, int64_t e, const char** why);
 // Records `msg` as this thread's last error (bi_last_error(NULL)) and returns st.
 bi_status set_thread_error(bi_status st, const std::string& msg);
 __host__ __device__ __forceinline__ int64_t lmin(int64_t a, int64_t b) { return a < b ? a : b; }

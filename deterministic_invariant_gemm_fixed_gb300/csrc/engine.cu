@@ -52,7 +52,20 @@ struct Scratch {
     void* ptr = nullptr;
     cudaError_t err = cudaSuccess;
     Scratch(bi_engine e, cudaStream_t s, size_t bytes) : eng(e), stream(s) {
-        if (bytes) err = cudaMallocFromPoolAsync(&ptr, bytes, e->pool, s);
+        if (!bytes) return;
+        if (take_injected_failure(e)) {  // bi_engine_fail_allocations: fail as an exhausted pool would
+            err = cudaErrorMemoryAllocation;
+            return;
+        }
+        err = cudaMallocFromPoolAsync(&ptr, bytes, e->pool, s);
+    }
+    static bool take_injected_failure(bi_engine e) {
+        int64_t v = e->failing_allocs.load();
+        while (v != 0) {
+            if (v < 0) return true;
+            if (e->failing_allocs.compare_exchange_weak(v, v - 1)) return true;
+        }
+        return false;
     }
     ~Scratch() {
         if (ptr) cudaFreeAsync(ptr, stream);
@@ -63,15 +76,9 @@ const int64_t kMaxDim = (int64_t(1) << 31) - 1;
 
 bi_status check_common(bi_engine eng, bi_dtype dt, int64_t m, int64_t k, int64_t n) {
     if (!eng) return fail(nullptr, BI_ERR_INVALID_ARG, "engine is NULL");
-    if (dt != BI_F32 && dt != BI_BF16 && dt != BI_F16)
-        return fail(eng, BI_ERR_INVALID_ARG, "dtype must be BI_F32, BI_BF16 or BI_F16");
-    if (m < 0) return fail(eng, BI_ERR_INVALID_ARG, "m must be >= 0");
-    if (k <= 0 || n <= 0) return fail(eng, BI_ERR_INVALID_ARG, "k and n must be > 0");
-    if (m > kMaxDim || k > kMaxDim || n > kMaxDim)
-        return fail(eng, BI_ERR_UNSUPPORTED, "a dimension exceeds 2^31 - 1");
-    if (n > int64_t(65535) * 128 || k > int64_t(65535) * 128)
-        return fail(eng, BI_ERR_UNSUPPORTED, "k and n are limited to 8388480");
-    return BI_OK;
+    const char* why = "";
+    const bi_status st = bi::check_sizes(dt, m, k, n, -1, &why);
+    return st == BI_OK ? BI_OK : fail(eng, st, why);
 }
 
 bi::LaunchCtx ctx(bi_engine eng, void* stream) {
@@ -115,6 +122,31 @@ bi_status tf32x3(bi_engine eng, const bi::LaunchCtx& c, const Tf32Operand& a, co
 
 namespace bi {
 bi_status set_thread_error(bi_status st, const std::string& msg) { return fail(nullptr, st, msg); }
+
+bi_status check_sizes(bi_dtype dt, int64_t m, int64_t k, int64_t n, int64_t e, const char** why) {
+    if (dt != BI_F32 && dt != BI_BF16 && dt != BI_F16) {
+        *why = "dtype must be BI_F32, BI_BF16 or BI_F16";
+        return BI_ERR_INVALID_ARG;
+    }
+    if (m < 0) { *why = "m must be >= 0"; return BI_ERR_INVALID_ARG; }
+    if (k <= 0 || n <= 0) { *why = "k and n must be > 0"; return BI_ERR_INVALID_ARG; }
+    if (m > kMaxDim || k > kMaxDim || n > kMaxDim) { *why = "a dimension exceeds 2^31 - 1"; return BI_ERR_UNSUPPORTED; }
+    if (n > int64_t(65535) * 128 || k > int64_t(65535) * 128) {
+        *why = "k and n are limited to 8388480";
+        return BI_ERR_UNSUPPORTED;
+    }
+    if (e < 0) return BI_OK;  // not a grouped call
+    if (e == 0) { *why = "e must be > 0"; return BI_ERR_INVALID_ARG; }
+    if (e > 65535) { *why = "e is limited to 65535 experts"; return BI_ERR_UNSUPPORTED; }
+    // the same U32 indexing limits as the grouped matmul of rublas (GroupedMatmulError)
+    const uint64_t lim = 0xffffffffull;
+    if (uint64_t(m) * uint64_t(k) > lim || uint64_t(m) * uint64_t(n) > lim ||
+        uint64_t(e) * uint64_t(n) * uint64_t(k) > lim) {
+        *why = "grouped matmul exceeds U32 indexing";
+        return BI_ERR_UNSUPPORTED;
+    }
+    return BI_OK;
+}
 }  // namespace bi
 
 extern "C" {
@@ -199,6 +231,12 @@ const char* bi_last_error(bi_engine eng) {
 }
 
 uint64_t bi_launch_count(bi_engine eng) { return eng ? eng->launches.load() : 0; }
+
+bi_status bi_engine_fail_allocations(bi_engine eng, int64_t count) {
+    if (!eng) return fail(nullptr, BI_ERR_INVALID_ARG, "engine is NULL");
+    eng->failing_allocs.store(count < 0 ? -1 : count);
+    return BI_OK;
+}
 
 bi_status bi_engine_set_wait_limit(bi_engine eng, uint64_t ns) {
     if (!eng) return fail(nullptr, BI_ERR_INVALID_ARG, "engine is NULL");
@@ -397,16 +435,10 @@ bi_status bi_fp8_backward_dw(bi_engine eng, void* dw, const uint8_t* xq, const u
 namespace {
 
 bi_status check_grouped(bi_engine eng, bi_dtype dt, int64_t m, int64_t k, int64_t n, int64_t e) {
-    bi_status st = check_common(eng, dt, m, k, n);
-    if (st != BI_OK) return st;
-    if (e <= 0) return fail(eng, BI_ERR_INVALID_ARG, "e must be > 0");
-    if (e > 65535) return fail(eng, BI_ERR_UNSUPPORTED, "e is limited to 65535 experts");
-    // the same U32 indexing limits as the grouped matmul of rublas (GroupedMatmulError)
-    const uint64_t lim = 0xffffffffull;
-    if (uint64_t(m) * uint64_t(k) > lim || uint64_t(m) * uint64_t(n) > lim ||
-        uint64_t(e) * uint64_t(n) * uint64_t(k) > lim)
-        return fail(eng, BI_ERR_UNSUPPORTED, "grouped matmul exceeds U32 indexing");
-    return BI_OK;
+    if (!eng) return fail(nullptr, BI_ERR_INVALID_ARG, "engine is NULL");
+    const char* why = "";
+    const bi_status st = bi::check_sizes(dt, m, k, n, e < 0 ? 0 : e, &why);
+    return st == BI_OK ? BI_OK : fail(eng, st, why);
 }
 
 }  // namespace

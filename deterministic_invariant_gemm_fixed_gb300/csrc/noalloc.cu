@@ -27,7 +27,12 @@
 // Set-up: the first call on a device looks up the array's device address with
 // cudaGetSymbolAddress (the host-side name of the array is only a stand-in and
 // must never be passed to a kernel) while that device is current, and caches
-// it.  Make that first call before any stream capture begins.
+// it together with the context it belongs to.  Make that first call before any
+// stream capture begins.  If the device's context is later destroyed and
+// recreated (cudaDeviceReset), the next call finds a different current context
+// and looks the address up again before launching anything.
+#include <cuda.h>
+
 #include <mutex>
 
 #include "bi_internal.h"
@@ -36,12 +41,16 @@ namespace {
 
 constexpr size_t kNoAllocScratchBytes = size_t(4) << 20;  // 4 MiB
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+// Status word for the launchers (they may record a device-side condition);
+// nothing in this entry point's kernels writes it today.
+static __device__ __align__(16) int g_noalloc_status[4];
 
 struct DeviceSlot {
-    std::once_flag once;
+    std::mutex mu;
+    CUcontext ctx = nullptr;        // context the addresses below belong to
     void* scratch = nullptr;        // device address of g_noalloc_scratch on this device
+    int* status = nullptr;          // device address of g_noalloc_status
     int sm_count = 0;
-    cudaError_t err = cudaSuccess;
     bi_engine_s counters;           // launch counter only; owns no device memory
 };
 
@@ -50,19 +59,52 @@ DeviceSlot g_slots[kMaxDevices];
 
 int64_t round256(int64_t b) { return (b + 255) / 256 * 256; }
 
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+
+CtxGetCurrentFn ctx_get_current() {
+    static CtxGetCurrentFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<CtxGetCurrentFn>(p);
+    });
+    return fn;
+}
+
+// Resolves (or re-resolves, after a context change) the device addresses of
+// the fixed arrays for device `dev`, which is current.  Called with slot.mu held.
+cudaError_t resolve(DeviceSlot& slot, int dev) {
+    cudaError_t err = cudaSetDevice(dev);  // initialises the device's primary context if it has none yet
+    if (err != cudaSuccess) return err;
+    CtxGetCurrentFn get = ctx_get_current();
+    if (!get) return cudaErrorNotSupported;
+    CUcontext cur = nullptr;
+    if (get(&cur) != CUDA_SUCCESS || cur == nullptr) return cudaErrorDeviceUninitialized;
+    if (cur == slot.ctx && slot.scratch && slot.status) return cudaSuccess;
+    slot.counters.device = dev;  // per-device kernel set-up is keyed on it
+    void* sc = nullptr;
+    void* st = nullptr;
+    if ((err = cudaGetSymbolAddress(&sc, g_noalloc_scratch)) != cudaSuccess) return err;
+    if ((err = cudaGetSymbolAddress(&st, g_noalloc_status)) != cudaSuccess) return err;
+    if ((err = cudaDeviceGetAttribute(&slot.sm_count, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return err;
+    slot.scratch = sc;
+    slot.status = static_cast<int*>(st);
+    slot.ctx = cur;
+    return cudaSuccess;
+}
+
 }  // namespace
 
 extern "C" bi_status bi_grouped_forward_noalloc(void* y, const void* x, const void* w,
                                                 const uint32_t* row_experts, int64_t m, int64_t k,
                                                 int64_t n, int64_t e, bi_dtype dtype, void* stream) {
-    if (dtype != BI_F32 && dtype != BI_BF16 && dtype != BI_F16)
-        return bi::set_thread_error(BI_ERR_INVALID_ARG, "dtype must be BI_F32, BI_BF16 or BI_F16");
-    if (m < 0 || k <= 0 || n <= 0 || e <= 0)
-        return bi::set_thread_error(BI_ERR_INVALID_ARG, "need m >= 0 and k, n, e > 0");
-    const uint64_t lim = 0xffffffffull;
-    if (uint64_t(m) * uint64_t(k) > lim || uint64_t(m) * uint64_t(n) > lim ||
-        uint64_t(e) * uint64_t(n) * uint64_t(k) > lim || e > 65535 || n > int64_t(65535) * 128)
-        return bi::set_thread_error(BI_ERR_UNSUPPORTED, "grouped matmul exceeds U32 indexing");
+    // the same size limits as bi_grouped_forward
+    const char* why = "";
+    const bi_status size_st = bi::check_sizes(dtype, m, k, n, e < 0 ? 0 : e, &why);
+    if (size_st != BI_OK) return bi::set_thread_error(size_st, std::string("bi_grouped_forward_noalloc: ") + why);
     if (m == 0) return BI_OK;
     if (!y || !x || !w || !row_experts)
         return bi::set_thread_error(BI_ERR_INVALID_ARG, "y, x, w and row_experts must not be NULL");
@@ -82,20 +124,20 @@ extern "C" bi_status bi_grouped_forward_noalloc(void* y, const void* x, const vo
     if (dev < 0 || dev >= kMaxDevices)
         return bi::set_thread_error(BI_ERR_UNSUPPORTED, "device ordinal beyond 63");
     DeviceSlot& slot = g_slots[dev];
-    std::call_once(slot.once, [&slot, dev] {
-        // the current device is `dev`: resolve the array's address on it
-        slot.counters.device = dev;  // per-device kernel set-up is keyed on it
-        slot.err = cudaGetSymbolAddress(&slot.scratch, g_noalloc_scratch);
-        if (slot.err == cudaSuccess)
-            slot.err = cudaDeviceGetAttribute(&slot.sm_count, cudaDevAttrMultiProcessorCount, dev);
-    });
-    if (slot.err != cudaSuccess || !slot.scratch)
-        return bi::set_thread_error(BI_ERR_CUDA, std::string("scratch set-up failed: ") +
-                                                     cudaGetErrorName(slot.err));
+    void* scratch = nullptr;
+    int* status = nullptr;
+    {
+        std::lock_guard<std::mutex> g(slot.mu);
+        err = resolve(slot, dev);
+        scratch = slot.scratch;
+        status = slot.status;
+    }
+    if (err != cudaSuccess || !scratch)
+        return bi::set_thread_error(BI_ERR_CUDA, std::string("scratch set-up failed: ") + cudaGetErrorName(err));
 
-    const bi::LaunchCtx c{&slot.counters, static_cast<cudaStream_t>(stream), slot.sm_count, nullptr,
+    const bi::LaunchCtx c{&slot.counters, static_cast<cudaStream_t>(stream), slot.sm_count, status,
                           slot.counters.wait_limit_ns};
-    unsigned char* base = static_cast<unsigned char*>(slot.scratch);
+    unsigned char* base = static_cast<unsigned char*>(scratch);
     uint32_t* seg = reinterpret_cast<uint32_t*>(base);
     uint32_t* perm = reinterpret_cast<uint32_t*>(base + seg_b);
     void* hist = base + seg_b + perm_b;

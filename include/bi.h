@@ -267,7 +267,9 @@ bi_status bi_grouped_backward_segmented(bi_engine engine, void* dx, float* dw, c
  * bytes, each part rounded up to 256) return BI_ERR_UNSUPPORTED.  All calls on a
  * device share the array: calls whose GPU work overlaps (unordered streams or
  * threads) race and give wrong results.  The first call on a device resolves
- * the array's address on that device; make it before any stream capture.
+ * the array's address on that device; make it before any stream capture.  If
+ * the device's context is destroyed and recreated (cudaDeviceReset), the next
+ * call resolves the address again in the new context before launching.
  * Errors are reported through bi_last_error(NULL). */
 bi_status bi_grouped_forward_noalloc(void* y, const void* x, const void* w,
                                      const uint32_t* row_experts, int64_t m, int64_t k, int64_t n,
@@ -285,6 +287,15 @@ int bi_dispatch_tier(int pass, bi_dtype dtype, int tensor_cores, int64_t k, int6
 
 /* Number of kernels this engine has launched since it was created. */
 uint64_t bi_launch_count(bi_engine engine);
+
+/* Host-side fault injection for allocation failure (no counterpart on the
+ * pages).  The next `count` scratch allocations of this engine fail as if its
+ * memory pool were exhausted (count < 0: every allocation until the setting is
+ * changed; 0: none).  A call whose scratch allocation fails returns BI_ERR_OOM
+ * with nothing enqueued and its outputs untouched; the engine stays usable.
+ * Calls that need no scratch are unaffected.  It lets callers and tests
+ * exercise their out-of-memory handling without exhausting a GPU. */
+bi_status bi_engine_fail_allocations(bi_engine engine, int64_t count);
 
 /* Set the limit (nanoseconds) after which a device-side pipeline wait gives up
  * and records BI_ERR_TIMEOUT.  Default 2e9 (2 s); 0 restores the default. */

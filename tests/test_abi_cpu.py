@@ -100,3 +100,23 @@ def test_binding_refuses_host_and_strided_tensors(bi):
         with pytest.raises(ValueError):
             bi._ptr(torch.zeros(4, 4, device="cuda").t())
     assert bi._ptr(None) is None and bi._ptr(1234) == 1234
+
+
+def test_noalloc_applies_the_allocating_path_size_limits_on_the_host(bi):
+    # The allocation-free grouped forward refuses exactly what bi_grouped_forward
+    # refuses, before it looks for a device: k beyond 8388480 with tiny U32
+    # element counts, too many experts, a zero expert count, a bad dtype.
+    limit = 65535 * 128
+    assert bi.bi_grouped_forward_noalloc(16, 16, 16, 16, 1, limit + 8, 1, 1, "bf16", 0) == bi.BI_ERR_UNSUPPORTED
+    assert "8388480" in bi.bi_last_error(None)
+    assert bi.bi_grouped_forward_noalloc(16, 16, 16, 16, 1, 8, 8, 65536, "bf16", 0) == bi.BI_ERR_UNSUPPORTED
+    assert bi.bi_grouped_forward_noalloc(16, 16, 16, 16, 1, 8, 8, 0, "bf16", 0) == bi.BI_ERR_INVALID_ARG
+    assert bi.bi_grouped_forward_noalloc(16, 16, 16, 16, 1, 8, 8, 2, 7, 0) == bi.BI_ERR_INVALID_ARG
+    assert bi.bi_grouped_forward_noalloc(16, 16, 16, 16, 1 << 20, 1 << 12, 8, 2, "bf16", 0) == bi.BI_ERR_UNSUPPORTED
+    # m = 0 is a no-op once the sizes pass
+    assert bi.bi_grouped_forward_noalloc(None, None, None, None, 0, 8, 8, 2, "bf16", 0) == bi.BI_OK
+
+
+def test_allocation_failure_setter_checks_its_engine(bi):
+    assert bi.bi_engine_fail_allocations(None, 1) == bi.BI_ERR_INVALID_ARG
+    assert "NULL" in bi.bi_last_error(None)
