@@ -125,3 +125,54 @@ def test_from_torch_keeps_the_function(eng):
     want = (x.double() @ ref.weight.double().t() + ref.bias.double()).float()
     got = lay(x)
     assert torch.allclose(got, want, rtol=1e-5, atol=1e-5)
+
+
+@pytest.mark.parametrize("scales", [(1.0, 1.0, 1.0), (0.5, 2.0, 0.25)])
+def test_fp8_route_matches_the_oracle_on_exact_integers(eng, scales):
+    # Small integers and power-of-two scales: every e4m3 code, product and sum is
+    # exact, so the layer's forward, dX, dW and bias gradient must equal the
+    # oracle's FP8 definitions (quantize, scaled matmul, one rounding) bit for bit.
+    from deterministic_invariant_gemm_fixed_gb300.nn import Fp8Scales
+    m, k, n, dtype = 96, 64, 48, "bf16"
+    sx, sw, sg = scales
+    x = synth.small_ints((m, k), -8, 8, dtype, 31) * sx
+    w = synth.small_ints((k, n), -8, 8, dtype, 32) * sw
+    g = synth.small_ints((m, n), -8, 8, dtype, 33) * sg
+    b = synth.small_ints((n,), -8, 8, dtype, 34) * 0.5
+    X = x.cuda().requires_grad_(True)
+    W = w.cuda().requires_grad_(True)
+    B = b.cuda().requires_grad_(True)
+    amax = torch.zeros(3, device="cuda")
+    fp8 = Fp8Scales(sx, torch.tensor([sw], device="cuda"), sg, amax=amax)
+    y = deterministic_linear(X.reshape(4, 24, k), W, B, fp8=fp8)
+    y.backward(g.cuda().reshape(4, 24, n))
+    xn, wn, gn, bn = (synth.to_np(t) for t in (x, w, g, b))
+    xq, ax = oracle.fp8_quantize(xn, dtype, np.float32(1.0) / np.float32(sx))
+    wq, aw = oracle.fp8_quantize(wn, dtype, np.float32(1.0) / np.float32(sw))
+    gq, ag = oracle.fp8_quantize(gn, dtype, np.float32(1.0) / np.float32(sg))
+    torch.cuda.synchronize()
+    assert np.array_equal(out_np(amax), np.array([ax, aw, ag], dtype=np.float32))
+    assert np.array_equal(out_np(y.detach().reshape(m, n)), oracle.fp8_forward(xq, wq, bn, sx, sw, m, k, n, dtype))
+    assert np.array_equal(out_np(X.grad), oracle.fp8_backward_dx(gq, wq, sg, sw, m, k, n, dtype))
+    assert np.array_equal(out_np(W.grad), oracle.fp8_backward_dw(xq, gq, sx, sg, m, k, n, dtype))
+    assert np.array_equal(out_np(B.grad), oracle.bias_grad(gn, m, n, dtype))
+
+
+def test_fp8_route_trains_bit_identically_twice(eng):
+    from deterministic_invariant_gemm_fixed_gb300.nn import Fp8Scales
+
+    def train():
+        torch.manual_seed(99)
+        lay = Linear(128, 96, device="cuda", dtype=torch.bfloat16)
+        opt = torch.optim.SGD(lay.parameters(), lr=0.05)
+        xs = synth.normal((6, 160, 128), 1.0, "bf16", 41).cuda()
+        ts = synth.normal((6, 160, 96), 1.0, "bf16", 42).cuda()
+        for i in range(6):
+            opt.zero_grad(set_to_none=True)
+            out = deterministic_linear(xs[i], lay.weight, lay.bias, fp8=Fp8Scales(1 / 64, 1 / 2048, 1 / 8192))
+            torch.nn.functional.mse_loss(out.float(), ts[i].float()).backward()
+            opt.step()
+        return lay
+    a, b = train(), train()
+    for pa, pb in zip(a.parameters(), b.parameters()):
+        assert torch.equal(pa.detach().view(torch.int16), pb.detach().view(torch.int16))
