@@ -47,6 +47,7 @@ SIGNATURES = {
     "bi_launch_count": (_u64, [_p]),
     "bi_engine_set_wait_limit": (_i32, [_p, _u64]),
     "bi_engine_fail_allocations": (_i32, [_p, _i64]),
+    "bi_engine_set_tile_cols": (_i32, [_p, _i32]),
     "bi_selftest_wait_timeout": (_i32, [_p, _p]),
     "bi_version": (ctypes.c_char_p, []),
     "bi_grouped_forward_segmented": (_i32, [_p, _p, _p, _p, _p, _i64, _i64, _i64, _i64, _i32, _p, _i32]),
@@ -239,6 +240,10 @@ def bi_engine_set_wait_limit(engine, nanoseconds: int) -> int:
 
 def bi_engine_fail_allocations(engine, count: int) -> int:
     return _lib.bi_engine_fail_allocations(engine, int(count))
+
+
+def bi_engine_set_tile_cols(engine, cols: int) -> int:
+    return _lib.bi_engine_set_tile_cols(engine, int(cols))
 
 
 def bi_selftest_wait_timeout(engine, stream=None) -> int:

@@ -19,6 +19,7 @@ struct bi_engine_s {
     cudaStream_t side = nullptr;            // engine-owned stream for independent work within a call
     std::atomic<uint64_t> launches{0};
     std::atomic<int64_t> failing_allocs{0}; // injected scratch-allocation failures still to give (-1 = all)
+    int tile_cols = 0;                      // forced tensor-core column tile (0 = chosen from the shape)
     std::mutex mu;                          // guards last_error
     std::string last_error;
 };
@@ -148,7 +149,7 @@ cudaError_t tc_dx(const LaunchCtx& c, bi_dtype dt, void* dx, const void* dy, con
 // dW: the output tiles of the last, partial wave run their contraction in
 // chunks added by the dW tree; ws holds their f32 results (tc_dw_workspace_bytes,
 // 0 = no split for this shape, ws may be null).
-int64_t tc_dw_workspace_bytes(int dw_f32, int64_t M, int64_t K, int64_t N);
+int64_t tc_dw_workspace_bytes(const LaunchCtx& c, int dw_f32, int64_t M, int64_t K, int64_t N);
 cudaError_t tc_dw(const LaunchCtx& c, bi_dtype dt, void* dw, int dw_f32, const void* x,
                   const void* dy, int64_t M, int64_t K, int64_t N, float* ws);
 // Grouped forward / dinput on a row-sorted operand a_sorted [M, K or N] (row
@@ -157,9 +158,12 @@ cudaError_t tc_grouped_rows(const LaunchCtx& c, bi_dtype dt, int pass_dinput, vo
                             const void* w, int64_t M, int64_t K, int64_t N, int64_t E, const uint32_t* seg,
                             const uint32_t* perm);
 // Grouped dweights [E,N,K] f32 from row-sorted dY and X plus their tail buffers.
+// The units of the last partial wave contract in chunks summed by the dW tree;
+// ws holds their f32 results (tc_grouped_dw_workspace_bytes; 0 = no split).
+int64_t tc_grouped_dw_workspace_bytes(int64_t M, int64_t K, int64_t N, int64_t E);
 cudaError_t tc_grouped_dw(const LaunchCtx& c, bi_dtype dt, float* dw, const void* dy_sorted, const void* x_sorted,
                           const void* dy_tail, const void* x_tail, int64_t M, int64_t K, int64_t N, int64_t E,
-                          const uint32_t* seg);
+                          const uint32_t* seg, float* ws);
 // FP8 e4m3 scaled matmuls on the CTA pair (pass 0 forward, 1 dX, 2 dW): the
 // f32 product is multiplied by *sa * *sb, then (+ bias), then rounded to out_dt.
 // The dW splits its last wave of tiles as tc_dw does (ws: tc_fp8_dw_workspace_bytes).

@@ -238,6 +238,14 @@ bi_status bi_engine_fail_allocations(bi_engine eng, int64_t count) {
     return BI_OK;
 }
 
+bi_status bi_engine_set_tile_cols(bi_engine eng, int cols) {
+    if (!eng) return fail(nullptr, BI_ERR_INVALID_ARG, "engine is NULL");
+    if (cols != 0 && cols != 128 && cols != 176 && cols != 192 && cols != 256)
+        return fail(eng, BI_ERR_INVALID_ARG, "tile columns must be 0 (automatic), 128, 176, 192 or 256");
+    eng->tile_cols = cols;
+    return BI_OK;
+}
+
 bi_status bi_engine_set_wait_limit(bi_engine eng, uint64_t ns) {
     if (!eng) return fail(nullptr, BI_ERR_INVALID_ARG, "engine is NULL");
     eng->wait_limit_ns = ns ? ns : 2000000000ull;
@@ -332,7 +340,7 @@ bi_status bi_backward_dw(bi_engine eng, void* dw, int dw_f32, const void* x, con
     if (tier && dtype == BI_F32)  // dw = x^T dy: both transposed (contraction over m)
         return tf32x3(eng, c, {x, m, k, true}, {dy, m, n, true}, dw, n, nullptr, k, n, m, "bi_backward_dw");
     if (tier) {
-        Scratch ws(eng, s, static_cast<size_t>(bi::tc_dw_workspace_bytes(out_f32, m, k, n)));
+        Scratch ws(eng, s, static_cast<size_t>(bi::tc_dw_workspace_bytes(c, out_f32, m, k, n)));
         if (ws.err != cudaSuccess) return cuda_fail(eng, ws.err, "dW chunk scratch");
         cudaError_t e = bi::tc_dw(c, dtype, dw, out_f32, x, dy, m, k, n, static_cast<float*>(ws.ptr));
         return e == cudaSuccess ? BI_OK : cuda_fail(eng, e, "bi_backward_dw");
@@ -532,7 +540,7 @@ bi_status grouped_backward_impl(bi_engine eng, void* dx, float* dw, const void* 
                                           round256(e * bi::GROUPED_TAIL_ROWS * k * 2)
                                     : 0;
     const int64_t max_chunks = (m + BI_DW_CHUNK - 1) / BI_DW_CHUNK + e;
-    const int64_t part_b = tier_dw ? 0 : max_chunks * n * k * 4;
+    const int64_t part_b = tier_dw ? round256(bi::tc_grouped_dw_workspace_bytes(m, k, n, e)) : max_chunks * n * k * 4;
     Scratch sc(eng, s, static_cast<size_t>(seg_b + perm_b + hist_b + dys_b + xs_b + tails_b + part_b));
     if (sc.err != cudaSuccess) return cuda_fail(eng, sc.err, "grouped scratch");
     uint8_t* base = static_cast<uint8_t*>(sc.ptr);
@@ -599,7 +607,7 @@ bi_status grouped_backward_impl(bi_engine eng, void* dx, float* dw, const void* 
         if (tier_dw) {
             if (!overlap) err = prepare_dw(c);
             if (err == cudaSuccess)
-                err = bi::tc_grouped_dw(c, dtype, dw, dy_sorted, x_sorted, dyt, xt, m, k, n, e, seg);
+                err = bi::tc_grouped_dw(c, dtype, dw, dy_sorted, x_sorted, dyt, xt, m, k, n, e, seg, part);
         } else {
             err = bi::scalar_dw_grouped(c, dtype, dw, dy, x, m, n, k, e, seg, perm, part, max_chunks);
         }

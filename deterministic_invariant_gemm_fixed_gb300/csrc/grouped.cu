@@ -42,6 +42,169 @@ __device__ __forceinline__ void rank_in_step(const uint32_t* sb, int tid, uint32
     last = after == 0;
 }
 
+// ---- fast path: E + 1 <= 1024 buckets and (E + 1) x blocks <= 16384 ------
+//
+// 512 rows per block, one per thread.  Within a warp, __match_any_sync finds
+// the lanes holding the same bucket; a row's rank among them is the number of
+// such lanes below it.  Each warp's count per bucket goes to shared memory,
+// and a prefix over the 16 warps (per bucket, warp order) gives each warp's
+// first rank in the block.  So a row's rank in its block is a pure function of
+// the ids (rows in ascending order), without atomics, and two launches do the
+// whole grouping: one writes every block's count per bucket, the other
+// recomputes the ranks, adds the block's base (all rows of lower buckets plus
+// the bucket's rows in earlier blocks) and scatters.
+constexpr int SEGF_THREADS = 512;
+constexpr int SEGF_WARPS = SEGF_THREADS / 32;
+constexpr int SEGF_MAX_BUCKETS = 1024;
+constexpr int64_t SEGF_MAX_TABLE = 16384;
+
+// Ranks of this thread's row (row b * 512 + tid) within its warp and the warp's
+// first rank per bucket: on return wc[w * (E + 1) + g] holds the number of
+// rows of bucket g in warps 0 .. w-1 of the block, and tot[g] the block's
+// count of bucket g.  Returns the row's bucket (NONE past M) and its rank
+// among the block's rows of that bucket.
+__device__ __forceinline__ uint32_t block_rank(const uint32_t* ids, int64_t M, uint32_t E, int64_t b, uint16_t* wc,
+                                               uint32_t* tot, uint32_t& rank) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const uint32_t nb = E + 1;
+    const int64_t r = b * SEGF_THREADS + tid;
+    const uint32_t g = r < M ? bucket_of(ids[r], E) : NONE;
+    for (uint32_t i = tid; i < SEGF_WARPS * nb; i += SEGF_THREADS) wc[i] = 0;
+    __syncthreads();
+    const uint32_t peers = __match_any_sync(0xffffffffu, g);
+    const uint32_t lower = peers & ((1u << lane) - 1u);
+    if (g != NONE && lower == 0) wc[warp * nb + g] = static_cast<uint16_t>(__popc(peers));
+    __syncthreads();
+    for (uint32_t q = tid; q < nb; q += SEGF_THREADS) {
+        uint32_t run = 0;
+#pragma unroll
+        for (int w = 0; w < SEGF_WARPS; ++w) {
+            const uint32_t t = wc[w * nb + q];
+            wc[w * nb + q] = static_cast<uint16_t>(run);
+            run += t;
+        }
+        tot[q] = run;
+    }
+    __syncthreads();
+    rank = g != NONE ? wc[warp * nb + g] + __popc(lower) : 0;
+    return g;
+}
+
+// counts[b * (E + 1) + g] = rows of bucket g in block b.
+__global__ void __launch_bounds__(SEGF_THREADS)
+    seg_count_fast_kernel(const uint32_t* ids, int64_t M, uint32_t E, uint32_t* counts) {
+    grid_dep_wait();
+    grid_dep_launch();
+    __shared__ uint16_t wc[SEGF_WARPS * SEGF_MAX_BUCKETS];
+    __shared__ uint32_t tot[SEGF_MAX_BUCKETS];
+    uint32_t rank;
+    block_rank(ids, M, E, blockIdx.x, wc, tot, rank);
+    for (uint32_t q = threadIdx.x; q <= E; q += SEGF_THREADS) counts[blockIdx.x * (E + 1) + q] = tot[q];
+}
+
+// In-place exclusive prefix sum of v[0 .. n) (n <= 1024) by one block of 512
+// threads (two entries per thread); returns the total to every thread.
+__device__ uint32_t block_exclusive_scan(uint32_t* v, uint32_t n, uint32_t* warp_tmp) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const uint32_t i0 = 2 * tid, i1 = 2 * tid + 1;
+    const uint32_t a = i0 < n ? v[i0] : 0, c = i1 < n ? v[i1] : 0;
+    uint32_t x = a + c;  // inclusive scan of the pair sums within the warp
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) warp_tmp[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+        uint32_t s = lane < SEGF_WARPS ? warp_tmp[lane] : 0;
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t y = __shfl_up_sync(0xffffffffu, s, o);
+            if (lane >= o) s += y;
+        }
+        if (lane < SEGF_WARPS) warp_tmp[lane] = s;  // inclusive over warps
+    }
+    __syncthreads();
+    const uint32_t before = (warp ? warp_tmp[warp - 1] : 0) + x - (a + c);
+    const uint32_t total = warp_tmp[SEGF_WARPS - 1];
+    __syncthreads();
+    if (i0 < n) v[i0] = before;
+    if (i1 < n) v[i1] = before + a;
+    __syncthreads();
+    return total;
+}
+
+__device__ void write_tile_starts(uint32_t* seg, uint32_t E);
+
+// perm[position] = row; block 0 also writes the segment table.
+__global__ void __launch_bounds__(SEGF_THREADS)
+    seg_scatter_fast_kernel(const uint32_t* ids, int64_t M, uint32_t E, const uint32_t* counts, int64_t NB,
+                            uint32_t* seg, uint32_t* perm) {
+    grid_dep_wait();
+    grid_dep_launch();
+    __shared__ __align__(16) uint16_t wc[SEGF_WARPS * SEGF_MAX_BUCKETS];  // later reused for 2 x 512 u32
+    __shared__ uint32_t tot[SEGF_MAX_BUCKETS];
+    __shared__ uint32_t base[SEGF_MAX_BUCKETS];
+    __shared__ uint32_t warp_tmp[32];
+    const int64_t b = blockIdx.x;
+    uint32_t rank;
+    const uint32_t g = block_rank(ids, M, E, b, wc, tot, rank);
+    // all rows of bucket q (tot) and those in blocks before this one (base).
+    // With at most 512 buckets, the threads split the blocks among them
+    // (thread = bucket + nb * slice, blocks slice, slice + slices, ...; coalesced
+    // rows of counts) and one thread per bucket adds the slices' sums.
+    const uint32_t nb = E + 1;
+    if (nb <= SEGF_THREADS) {
+        const uint32_t slices = SEGF_THREADS / nb;
+        uint32_t* red_all = reinterpret_cast<uint32_t*>(wc);  // the warp ranks are in registers now
+        uint32_t* red_before = red_all + SEGF_THREADS;
+        __syncthreads();
+        if (threadIdx.x < slices * nb) {
+            const uint32_t q = threadIdx.x % nb, sl = threadIdx.x / nb;
+            uint32_t all = 0, before = 0;
+            for (int64_t bb = sl; bb < NB; bb += slices) {
+                const uint32_t v = counts[bb * nb + q];
+                before += bb < b ? v : 0;
+                all += v;
+            }
+            red_all[threadIdx.x] = all;
+            red_before[threadIdx.x] = before;
+        }
+        __syncthreads();
+        if (threadIdx.x < nb) {
+            uint32_t all = 0, before = 0;
+            for (uint32_t sl = 0; sl < slices; ++sl) {
+                all += red_all[sl * nb + threadIdx.x];
+                before += red_before[sl * nb + threadIdx.x];
+            }
+            tot[threadIdx.x] = all;
+            base[threadIdx.x] = before;
+        }
+    } else {
+        for (uint32_t q = threadIdx.x; q < nb; q += SEGF_THREADS) {
+            uint32_t all = 0, before = 0;
+#pragma unroll 8
+            for (int64_t bb = 0; bb < NB; ++bb) {
+                const uint32_t v = counts[bb * nb + q];
+                before += bb < b ? v : 0;
+                all += v;
+            }
+            tot[q] = all;
+            base[q] = before;
+        }
+    }
+    __syncthreads();
+    block_exclusive_scan(tot, E + 1, warp_tmp);  // tot[q] = first sorted position of bucket q
+    if (g != NONE) perm[tot[g] + base[g] + rank] = static_cast<uint32_t>(b * SEGF_THREADS + threadIdx.x);
+    if (b == 0) {
+        for (uint32_t q = threadIdx.x; q <= E; q += SEGF_THREADS) seg[q] = tot[q];
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            seg[E + 1] = static_cast<uint32_t>(M);
+            write_tile_starts(seg, E);
+        }
+    }
+}
+
 __global__ void __launch_bounds__(SEG_THREADS)
     seg_count_kernel(const uint32_t* ids, int64_t M, uint32_t E, uint32_t* hist, int64_t NB) {
     grid_dep_wait();
@@ -274,6 +437,20 @@ int64_t segment_scratch_bytes(int64_t M, int64_t E) {
 
 cudaError_t segment(const LaunchCtx& c, const uint32_t* ids, int64_t M, int64_t E, uint32_t* seg,
                     uint32_t* perm, void* scratch) {
+    const int64_t NBF = (M + SEGF_THREADS - 1) / SEGF_THREADS;
+    if (M > 0 && E + 1 <= SEGF_MAX_BUCKETS && (E + 1) * NBF <= SEGF_MAX_TABLE) {
+        // two launches; counts[(E+1) * NBF] fits in the scratch of the general path
+        uint32_t* counts = static_cast<uint32_t*>(scratch);
+        cudaError_t e = launch_pdl(seg_count_fast_kernel, dim3(static_cast<unsigned>(NBF)), dim3(SEGF_THREADS), 0,
+                                   c.stream, ids, M, static_cast<uint32_t>(E), counts);
+        if (e != cudaSuccess) return e;
+        c.count();
+        e = launch_pdl(seg_scatter_fast_kernel, dim3(static_cast<unsigned>(NBF)), dim3(SEGF_THREADS), 0, c.stream,
+                       ids, M, static_cast<uint32_t>(E), static_cast<const uint32_t*>(counts), NBF, seg, perm);
+        if (e != cudaSuccess) return e;
+        c.count();
+        return cudaGetLastError();
+    }
     const int64_t NB = num_seg_blocks(M) > 0 ? num_seg_blocks(M) : 1;
     uint32_t* hist = static_cast<uint32_t*>(scratch);
     if (M > 0) {

@@ -38,17 +38,14 @@ constexpr int TM = 128, TN = 128, TK = 16, NT = 256, PAD = 4;
 
 template <typename T> struct Elem;
 template <> struct Elem<float> {
-    static constexpr bool is_bf16 = false;
     static __device__ __forceinline__ float up(float v) { return v; }
     static __device__ __forceinline__ float down(float v) { return v; }
 };
 template <> struct Elem<__nv_bfloat16> {
-    static constexpr bool is_bf16 = true;
     static __device__ __forceinline__ float up(__nv_bfloat16 v) { return __bfloat162float(v); }
     static __device__ __forceinline__ __nv_bfloat16 down(float v) { return __float2bfloat16_rn(v); }
 };
 template <> struct Elem<__half> {
-    static constexpr bool is_bf16 = false;
     static __device__ __forceinline__ float up(__half v) { return __half2float(v); }
     static __device__ __forceinline__ __half down(float v) { return __float2half_rn(v); }
 };
@@ -406,10 +403,11 @@ __global__ void __launch_bounds__(2 * TMV, TMV == 128 ? 1 : (VEC ? 4 : 3)) scala
 // ------------------------------------------------------------------ narrow rows kernel
 
 // Outputs at most 64 columns wide (an output dimension below the tensor-core
-// threshold): 16 x 64 tiles on 256 threads, 2 x 2 outputs per thread, so a
-// narrow output still spreads over many CTAs.  Same chains as above: each
-// output is fmaf over l ascending from +0 (paired FMA lanes), then (+ bias)
-// and one rounding.  Dense only.
+// threshold), and small outputs that the 128-column tiles would spread over
+// fewer CTAs than the GPU has SMs: 16 x 64 tiles on 256 threads (column tile
+// blockIdx.y), 2 x 2 outputs per thread, so a small output still spreads over
+// many CTAs.  Same chains as above: each output is fmaf over l ascending from
+// +0 (paired FMA lanes), then (+ bias) and one rounding.  Dense only.
 constexpr int NW_TM = 16, NW_TN = 64, NW_TK = 32;
 
 template <typename T, bool BT>
@@ -421,6 +419,7 @@ __global__ void __launch_bounds__(256) scalar_rows_narrow_kernel(const RowsArgs 
     const T* B = static_cast<const T*>(p.b);
     const int64_t L = p.L, C = p.C;
     const int64_t r0 = static_cast<int64_t>(blockIdx.x) * NW_TM;
+    const int64_t c0 = static_cast<int64_t>(blockIdx.y) * NW_TN;
     const int64_t rvalid = lmin(NW_TM, p.R - r0);
     // staging: A 16 rows x 32 steps (2 per thread), B 32 steps x 64 cols (8 per thread)
     const int a_row = tid >> 4, a_l = (tid & 15) * 2;
@@ -436,10 +435,10 @@ __global__ void __launch_bounds__(256) scalar_rows_narrow_kernel(const RowsArgs 
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
             if (BT) {  // b(l, c) = B[c * L + l]
-                const int64_t c = b_i, l = l0 + b_j + i;
+                const int64_t c = c0 + b_i, l = l0 + b_j + i;
                 rb[i] = (c < C && l < L) ? Elem<T>::up(B[c * L + l]) : 0.0f;
             } else {   // b(l, c) = B[l * C + c]
-                const int64_t l = l0 + b_i, c = b_j + i;
+                const int64_t l = l0 + b_i, c = c0 + b_j + i;
                 rb[i] = (l < L && c < C) ? Elem<T>::up(B[l * C + c]) : 0.0f;
             }
         }
@@ -483,7 +482,7 @@ __global__ void __launch_bounds__(256) scalar_rows_narrow_kernel(const RowsArgs 
         if (lr >= rvalid) continue;
 #pragma unroll
         for (int j = 0; j < 2; ++j) {
-            const int64_t c = 2 * tx + j;
+            const int64_t c = c0 + 2 * tx + j;
             if (c >= C) continue;
             float v = __uint_as_float(static_cast<uint32_t>(j ? (acc[i] >> 32) : acc[i]));
             if (bias) v = v + Elem<T>::up(bias[c]);
@@ -663,161 +662,149 @@ __global__ void __launch_bounds__(NT, 2) scalar_dw_chunk_kernel(const DwArgs p) 
     }
 }
 
-// Outputs of at most SK_R rows (a matrix-vector product, or a few rows): one
-// warp per 64 output columns, two columns per lane advanced together by the
-// paired FMA, one accumulator per row and column, each the same chain as
-// above (fmaf over l ascending from +0, then (+ bias) and one rounding).  The
-// parallelism is one chain per output, so the chain's per-step latency and
-// the instructions one warp issues per step bound the kernel.  Operands stream
-// through a deep cp.async ring of raw 64-step blocks (each lane copies fixed
-// 16-byte units whose addresses advance by a fixed stride), and the A steps of
-// a block are widened once into shared memory, each stored twice so that one
-// 16-byte load gives two (a, a) pairs.  A lane owns columns 2 lane and
-// 2 lane + 1 when B is [step][column] (one 32-bit load per step), lane and
-// lane + 32 when B is [column][step] (16-byte loads of 8 steps, conflict-free
-// at the 144-byte row pitch).  Requires 16-byte aligned rows of whole 16-byte
-// units.
-constexpr int SK_R = 4;        // most output rows
-constexpr int SK_STEPS = 64;   // contraction steps per stage (= columns per warp)
+constexpr int SK_R = 4;  // most output rows of the matrix-vector kernel
+
+// ------------------------------------------------------------------ matrix-vector kernel
+
+// Batches of at most 4 rows (a matrix-vector product): one warp per 32 output
+// columns, one column per lane, so every output column is a chain of its own
+// lane: acc = fmaf(up(a[r, l]), up(b(l, c)), acc) for l ascending from +0, one
+// plain fmaf per step (RR rows = RR independent chains per lane), then (+ bias)
+// and one rounding -- the chain of every other kernel of this tier.  The
+// operands stream through a 16-stage (f32: 10) cp.async ring of 64-step blocks: B as
+// [step][32 columns] (one 2- or 4-byte shared load per step and lane) or, when
+// B is contraction-contiguous, [column][64 steps] (one 16-byte load per 8
+// steps); the rows of A are widened once per block into shared memory and read
+// as broadcasts.  Each group of 8 steps loads its operands into registers
+// while the previous group's FMAs run, so the dependent fmaf chain, not the
+// loads, sets the pace.  Requires 16-byte aligned rows of whole 16-byte units.
+constexpr int GV_STEPS = 64;   // contraction steps per stage
+// ring depth: enough 64-step blocks in flight to cover the DRAM latency at the
+// chain's pace (16-bit stages are 4.5-5 KB, f32 stages 9-9.5 KB)
 template <typename T>
-__host__ __device__ constexpr int sk_stages() { return sizeof(T) == 4 ? 10 : 16; }
-template <typename T>
-struct SkinnyStage {
-    static constexpr int PADE = 16 / sizeof(T);
-    T b[64][64 + PADE];  // [step][column], or [column][step] when B is contraction-contiguous
-    T a[SK_R][SK_STEPS];
+__host__ __device__ constexpr int gv_stages() { return sizeof(T) == 4 ? 10 : 16; }
+template <typename T, bool BT>
+struct GemvStage {
+    static constexpr int PADE = BT ? 16 / sizeof(T) : 0;
+    T b[BT ? 32 : GV_STEPS][(BT ? GV_STEPS : 32) + PADE];
+    T a[SK_R][GV_STEPS];
 };
 
-// Two adjacent elements at p (4-byte aligned for 16-bit types, 8 for f32),
-// widened: (first, second) as the low and high lanes of a paired-FMA operand.
-template <typename T>
-__device__ __forceinline__ uint64_t widen_pair(const T* p) {
-    if (sizeof(T) == 4) return *reinterpret_cast<const uint64_t*>(p);
-    const uint32_t w = *reinterpret_cast<const uint32_t*>(p);
-    uint32_t lo, hi;
-    if (sizeof(T) == 2 && Elem<T>::is_bf16) {  // bf16: the high half of an f32
-        lo = w << 16;
-        hi = w & 0xffff0000u;
-    } else {
-        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w));
-        lo = __float_as_uint(f.x);
-        hi = __float_as_uint(f.y);
-    }
-    return (static_cast<uint64_t>(hi) << 32) | lo;
-}
-
-template <typename T, bool BT, int RR>  // RR: rows computed (R <= RR <= SK_R)
-__global__ void __launch_bounds__(32) scalar_rows_skinny_kernel(const RowsArgs p) {
-    constexpr int STAGES = sk_stages<T>();
-    using Stage = SkinnyStage<T>;
-    extern __shared__ __align__(16) uint8_t smem_sk[];
-    Stage* ring = reinterpret_cast<Stage*>(smem_sk);
-    uint64_t(*aw)[SK_STEPS] = reinterpret_cast<uint64_t(*)[SK_STEPS]>(smem_sk + STAGES * sizeof(Stage));
+template <typename T, bool BT, int RR>  // RR: rows computed (R <= RR <= 4)
+__global__ void __launch_bounds__(32) scalar_rows_gemv_kernel(const RowsArgs p) {
+    using Stage = GemvStage<T, BT>;
+    constexpr int GV_STAGES = gv_stages<T>();
+    extern __shared__ __align__(16) uint8_t smem_gv[];
+    Stage* ring = reinterpret_cast<Stage*>(smem_gv);
+    float(*aw)[GV_STEPS] = reinterpret_cast<float(*)[GV_STEPS]>(smem_gv + GV_STAGES * sizeof(Stage));  // [RR][steps]
     const int lane = threadIdx.x;
     const T* A = static_cast<const T*>(p.a);
     const T* B = static_cast<const T*>(p.b);
     const int64_t R = p.R, L = p.L, C = p.C;
-    const int64_t c0 = static_cast<int64_t>(blockIdx.x) * 64;
-    constexpr int U = 16 / sizeof(T);   // elements per 16-byte unit
-    constexpr int UPR = 64 / U;         // units per 64-element row of a stage
-    constexpr int RPI = 32 / UPR;       // stage rows one pass of the warp covers
-    constexpr int NB = 64 / RPI;        // B units per lane per stage
-    const int useg = (lane % UPR) * U, urow = lane / UPR;
-    // B unit i of this lane: stage row urow + RPI i, elements useg .. useg + U - 1
-    const T* bp = BT ? B + (c0 + urow) * L + useg : B + urow * C + c0 + useg;
-    const int64_t brow = BT ? RPI * L : RPI * C;   // between this lane's units
-    const int64_t bstage = BT ? SK_STEPS : SK_STEPS * C;
-    uint32_t brow_ok = 0;  // BT: output rows of B inside C
-    if (BT) {
-#pragma unroll
-        for (int i = 0; i < NB; ++i) brow_ok |= (c0 + urow + RPI * i < C ? 1u : 0u) << i;
-    }
-    const bool bcol_ok = BT || c0 + useg < C;
-    const int64_t nkb = (L + SK_STEPS - 1) / SK_STEPS;
+    const int64_t c0 = static_cast<int64_t>(blockIdx.x) * 32;
+    constexpr int U = 16 / sizeof(T);               // elements per 16-byte unit
+    // B units of one stage: [step][32 columns] = 64 rows of 32/U units, or
+    // [32 columns][64 steps] = 32 rows of 64/U units; 32 lanes take them in turn
+    constexpr int B_UPR = BT ? GV_STEPS / U : 32 / U;
+    constexpr int B_ROWS = BT ? 32 : GV_STEPS;
+    constexpr int B_UNITS = B_UPR * B_ROWS;
+    static_assert(B_UNITS % 32 == 0, "whole passes of the warp");
+    constexpr int A_UPR = GV_STEPS / U;
+    const int64_t nkb = (L + GV_STEPS - 1) / GV_STEPS;
     auto issue = [&](int64_t kb) {
-        Stage& st = ring[kb % STAGES];
-        const int64_t l0 = kb * SK_STEPS;
-        const T* q = bp + kb * bstage;
+        Stage& st = ring[kb % GV_STAGES];
+        const int64_t l0 = kb * GV_STEPS;
 #pragma unroll
-        for (int i = 0; i < NB; ++i) {
-            const int row = urow + RPI * i;
-            const bool ok = BT ? (((brow_ok >> i) & 1u) != 0 && l0 + useg < L) : (bcol_ok && l0 + row < L);
-            cp_async16(&st.b[row][useg], ok ? q + i * brow : B, ok ? 16u : 0u);
+        for (int i = 0; i < B_UNITS / 32; ++i) {
+            const int u = lane + 32 * i;
+            const int row = u / B_UPR, seg = (u % B_UPR) * U;
+            bool ok;
+            const T* src;
+            if (BT) {  // column c0 + row, steps l0 + seg ..
+                ok = c0 + row < C && l0 + seg < L;
+                src = B + (c0 + row) * L + l0 + seg;
+            } else {   // step l0 + row, columns c0 + seg ..
+                ok = l0 + row < L && c0 + seg < C;
+                src = B + (l0 + row) * C + c0 + seg;
+            }
+            cp_async16(&st.b[row][seg], ok ? src : B, ok ? 16u : 0u);
         }
-        for (int u = lane; u < SK_R * UPR; u += 32) {
-            const int r = u / UPR, sg = (u % UPR) * U;
-            const bool ok = r < R && l0 + sg < L;
-            cp_async16(&st.a[r][sg], ok ? A + r * L + l0 + sg : A, ok ? 16u : 0u);
+        for (int u = lane; u < RR * A_UPR; u += 32) {
+            const int r = u / A_UPR, seg = (u % A_UPR) * U;
+            const bool ok = r < R && l0 + seg < L;
+            cp_async16(&st.a[r][seg], ok ? A + r * L + l0 + seg : A, ok ? 16u : 0u);
         }
     };
-    // prologue: STAGES - 1 blocks in flight (empty groups keep the count)
-    for (int64_t kb = 0; kb < STAGES - 1; ++kb) {
+    for (int64_t kb = 0; kb < GV_STAGES - 1; ++kb) {
         if (kb < nkb) issue(kb);
         cp_async_commit();
     }
-    uint64_t acc[RR];
+    float acc[RR];
 #pragma unroll
-    for (int r = 0; r < RR; ++r) acc[r] = 0;  // (+0, +0)
+    for (int r = 0; r < RR; ++r) acc[r] = 0.0f;
     for (int64_t kb = 0; kb < nkb; ++kb) {
-        cp_async_wait<STAGES - 2>();
+        cp_async_wait<GV_STAGES - 2>();
         __syncwarp();  // block kb has landed for every lane; block kb - 1 is no longer read
-        if (kb + STAGES - 1 < nkb) issue(kb + STAGES - 1);
+        if (kb + GV_STAGES - 1 < nkb) issue(kb + GV_STAGES - 1);
         cp_async_commit();
-        const Stage& st = ring[kb % STAGES];
-        for (int u = lane; u < RR * SK_STEPS; u += 32) {
-            const uint32_t v = __float_as_uint(Elem<T>::up(st.a[u / SK_STEPS][u % SK_STEPS]));
-            aw[u / SK_STEPS][u % SK_STEPS] = (static_cast<uint64_t>(v) << 32) | v;
-        }
+        const Stage& st = ring[kb % GV_STAGES];
+        for (int u = lane; u < RR * GV_STEPS; u += 32) aw[u / GV_STEPS][u % GV_STEPS] = Elem<T>::up(st.a[u / GV_STEPS][u % GV_STEPS]);
         __syncwarp();
-#pragma unroll
-        for (int l8 = 0; l8 < SK_STEPS; l8 += 8) {
-            uint64_t w[8];  // (column 0, column 1) of this lane at each of 8 steps
+        // group g of 8 steps: operands in registers one group ahead of the FMAs
+        float bc[8], ac[RR][8];
+        auto fetch = [&](int j0, float (&bv)[8], float (&av)[RR][8]) {
             if (BT) {
-                float f0[8], f1[8];
-                smem_load8(&st.b[lane][l8], f0);
-                smem_load8(&st.b[lane + 32][l8], f1);
-#pragma unroll
-                for (int j = 0; j < 8; ++j)
-                    w[j] = (static_cast<uint64_t>(__float_as_uint(f1[j])) << 32) | __float_as_uint(f0[j]);
+                smem_load8<T>(&st.b[lane][j0], bv);
             } else {
 #pragma unroll
-                for (int j = 0; j < 8; ++j) w[j] = widen_pair(&st.b[l8 + j][2 * lane]);
+                for (int i = 0; i < 8; ++i) bv[i] = Elem<T>::up(st.b[j0 + i][lane]);
             }
 #pragma unroll
             for (int r = 0; r < RR; ++r) {
-                uint64_t av[8];
+                const float4 x0 = *reinterpret_cast<const float4*>(&aw[r][j0]);
+                const float4 x1 = *reinterpret_cast<const float4*>(&aw[r][j0 + 4]);
+                av[r][0] = x0.x; av[r][1] = x0.y; av[r][2] = x0.z; av[r][3] = x0.w;
+                av[r][4] = x1.x; av[r][5] = x1.y; av[r][6] = x1.z; av[r][7] = x1.w;
+            }
+        };
+        fetch(0, bc, ac);
 #pragma unroll
-                for (int j = 0; j < 8; j += 2) {
-                    const ulonglong2 x = *reinterpret_cast<const ulonglong2*>(&aw[r][l8 + j]);
-                    av[j] = x.x;
-                    av[j + 1] = x.y;
+        for (int j0 = 0; j0 < GV_STEPS; j0 += 8) {
+            float bn[8], an[RR][8];
+            if (j0 + 8 < GV_STEPS) fetch(j0 + 8, bn, an);
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+#pragma unroll
+                for (int r = 0; r < RR; ++r) acc[r] = fmaf(ac[r][i], bc[i], acc[r]);
+            if (j0 + 8 < GV_STEPS) {
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    bc[i] = bn[i];
+#pragma unroll
+                    for (int r = 0; r < RR; ++r) ac[r][i] = an[r][i];
                 }
-#pragma unroll
-                for (int j = 0; j < 8; ++j) fma2(acc[r], av[j], w[j]);
             }
         }
         __syncwarp();  // aw is rewritten for the next block
     }
     cp_async_wait<0>();
+    const int64_t c = c0 + lane;
+    if (c >= C) return;
     T* out = static_cast<T*>(p.out);
     const T* bias = static_cast<const T*>(p.bias);
+    const float bc = bias != nullptr ? Elem<T>::up(bias[c]) : 0.0f;
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
-        const int64_t c = BT ? c0 + lane + 32 * h : c0 + 2 * lane + h;
-        if (c >= C) continue;
-        const float bc = bias != nullptr ? Elem<T>::up(bias[c]) : 0.0f;
-#pragma unroll
-        for (int r = 0; r < RR; ++r) {
-            if (r >= R) break;
-            const float a = __uint_as_float(static_cast<uint32_t>(h ? (acc[r] >> 32) : acc[r]));
-            out[r * C + c] = Elem<T>::down(bias != nullptr ? __fadd_rn(a, bc) : a);
-        }
+    for (int r = 0; r < RR; ++r) {
+        if (r >= R) break;
+        out[r * C + c] = Elem<T>::down(bias != nullptr ? __fadd_rn(acc[r], bc) : acc[r]);
     }
 }
 
-// Chunk chains for outputs at most 64 columns wide: 16 x 64 tiles on 256
-// threads, 2 x 2 outputs per thread, one CTA per (tile, chunk).  Same chains as
-// scalar_dw_chunk_kernel (rows of the chunk ascending from +0).  Dense only.
+// Chunk chains for outputs at most 64 columns wide, and for small outputs that
+// the 128 x 128 tiles would spread over fewer CTAs than the GPU has SMs: 16 x 64
+// tiles on 256 threads (column tile blockIdx.z), 2 x 2 outputs per thread, one
+// CTA per (tile, chunk).  Same chains as scalar_dw_chunk_kernel (rows of the
+// chunk ascending from +0).  Dense only.
 template <typename T>
 __global__ void __launch_bounds__(256) scalar_dw_narrow_kernel(const DwArgs p) {
     __shared__ __align__(16) float as[2][NW_TK][2 * NW_TM + 4];  // A doubled: [l][2r], [l][2r+1]
@@ -827,6 +814,7 @@ __global__ void __launch_bounds__(256) scalar_dw_narrow_kernel(const DwArgs p) {
     const T* Bm = static_cast<const T*>(p.b);
     const int64_t R = p.R, C = p.C;
     const int64_t r0 = static_cast<int64_t>(blockIdx.x) * NW_TM;
+    const int64_t c0 = static_cast<int64_t>(blockIdx.z) * NW_TN;
     const int64_t z = blockIdx.y;
     const int64_t pos0 = z * BI_DW_CHUNK;
     const int64_t cnt = lmin(BI_DW_CHUNK, p.M - pos0);
@@ -840,7 +828,7 @@ __global__ void __launch_bounds__(256) scalar_dw_narrow_kernel(const DwArgs p) {
         for (int i = 0; i < 2; ++i)
             ra[i] = (ok && r0 + sa + i < R) ? Elem<T>::up(A[row * R + r0 + sa + i]) : 0.0f;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) rb[i] = (ok && sb + i < C) ? Elem<T>::up(Bm[row * C + sb + i]) : 0.0f;
+        for (int i = 0; i < 8; ++i) rb[i] = (ok && c0 + sb + i < C) ? Elem<T>::up(Bm[row * C + c0 + sb + i]) : 0.0f;
     };
     auto store = [&](int buf) {
         *reinterpret_cast<float4*>(&as[buf][sl][2 * sa]) = make_float4(ra[0], ra[0], ra[1], ra[1]);
@@ -874,7 +862,7 @@ __global__ void __launch_bounds__(256) scalar_dw_narrow_kernel(const DwArgs p) {
         if (r >= R) continue;
 #pragma unroll
         for (int j = 0; j < 2; ++j) {
-            const int64_t c = 2 * tx + j;
+            const int64_t c = c0 + 2 * tx + j;
             if (c >= C) continue;
             const float v = __uint_as_float(static_cast<uint32_t>(j ? (acc[i] >> 32) : acc[i]));
             if (p.partials) p.partials[(z * R + r) * C + c] = v;
@@ -1062,35 +1050,51 @@ unsigned tree_grid(int64_t n, int sm) {
 }  // namespace
 
 template <typename T>
-bool skinny_ok(const RowsArgs& a) {
+bool gemv_ok(const RowsArgs& a) {
     const int64_t unit = 16 / sizeof(T);
     return aligned16(a.a) && aligned16(a.b) && a.L % unit == 0 && a.C % unit == 0;
 }
 
 template <typename T, bool BT, int RR>
-cudaError_t launch_skinny(const LaunchCtx& c, const RowsArgs& a) {
-    const size_t bytes = sk_stages<T>() * sizeof(SkinnyStage<T>) + SK_R * SK_STEPS * sizeof(uint64_t);
-    const cudaError_t e = allow_smem<scalar_rows_skinny_kernel<T, BT, RR>>(c, bytes);
+cudaError_t launch_gemv(const LaunchCtx& c, const RowsArgs& a) {
+    const size_t bytes = gv_stages<T>() * sizeof(GemvStage<T, BT>) + RR * GV_STEPS * sizeof(float);
+    const cudaError_t e = allow_smem<scalar_rows_gemv_kernel<T, BT, RR>>(c, bytes);
     if (e != cudaSuccess) return e;
-    scalar_rows_skinny_kernel<T, BT, RR><<<static_cast<unsigned>((a.C + 63) / 64), 32, bytes, c.stream>>>(a);
+    scalar_rows_gemv_kernel<T, BT, RR><<<static_cast<unsigned>((a.C + 31) / 32), 32, bytes, c.stream>>>(a);
     return cudaSuccess;
 }
 
 template <typename T>
-cudaError_t rows_skinny_t(const LaunchCtx& c, const RowsArgs& a, int bt) {
+cudaError_t rows_gemv_t(const LaunchCtx& c, const RowsArgs& a, int bt) {
     cudaError_t e;
-    if (bt) e = a.R <= 1 ? launch_skinny<T, true, 1>(c, a) : a.R <= 2 ? launch_skinny<T, true, 2>(c, a)
-                                                                      : launch_skinny<T, true, 4>(c, a);
-    else e = a.R <= 1 ? launch_skinny<T, false, 1>(c, a) : a.R <= 2 ? launch_skinny<T, false, 2>(c, a)
-                                                                     : launch_skinny<T, false, 4>(c, a);
+    if (bt) e = a.R <= 1 ? launch_gemv<T, true, 1>(c, a) : a.R <= 2 ? launch_gemv<T, true, 2>(c, a)
+                                                                   : launch_gemv<T, true, 4>(c, a);
+    else e = a.R <= 1 ? launch_gemv<T, false, 1>(c, a) : a.R <= 2 ? launch_gemv<T, false, 2>(c, a)
+                                                                  : launch_gemv<T, false, 4>(c, a);
     if (e != cudaSuccess) return e;
     c.count();
     return cudaGetLastError();
 }
 
+// The narrow kernels take an output when it is at most 64 columns wide, or when
+// it is small: the 128-column tiles would give fewer CTAs than the GPU has SMs
+// while the 16 x 64 tiles give more, and its column tiles fit a grid dimension.
+// (Any tiling gives every output the same chain.)
+bool narrow_rows(const LaunchCtx& c, int64_t R, int64_t C) {
+    if (C <= NW_TN) return true;
+    const int64_t col_tiles = (C + NW_TN - 1) / NW_TN;
+    return col_tiles <= 65535 && ((R + 63) / 64) * ((C + TN - 1) / TN) < c.sm_count &&
+           ((R + NW_TM - 1) / NW_TM) * col_tiles > ((R + 63) / 64) * ((C + TN - 1) / TN);
+}
+bool narrow_dw(const LaunchCtx& c, int64_t R, int64_t C, int64_t J) {
+    if (C <= NW_TN) return true;
+    const int64_t col_tiles = (C + NW_TN - 1) / NW_TN;
+    return col_tiles <= 65535 && J <= 65535 && ((R + TM - 1) / TM) * ((C + TN - 1) / TN) * J < c.sm_count;
+}
+
 template <typename T>
 cudaError_t rows_narrow_t(const LaunchCtx& c, const RowsArgs& a, int bt) {
-    const dim3 grid(static_cast<unsigned>((a.R + NW_TM - 1) / NW_TM));
+    const dim3 grid(static_cast<unsigned>((a.R + NW_TM - 1) / NW_TM), static_cast<unsigned>((a.C + NW_TN - 1) / NW_TN));
     if (bt) scalar_rows_narrow_kernel<T, true><<<grid, 256, 0, c.stream>>>(a);
     else scalar_rows_narrow_kernel<T, false><<<grid, 256, 0, c.stream>>>(a);
     c.count();
@@ -1102,12 +1106,12 @@ cudaError_t scalar_rows(const LaunchCtx& c, bi_dtype dt, void* out, const void* 
     RowsArgs args{out, a, b, bias, R, L, C, 0, nullptr, nullptr};
     if (C > NW_TN && R <= SK_R) {  // a few rows: one lane per output column (the kernel changes no chain)
         switch (dt) {
-            case BI_F32: if (skinny_ok<float>(args)) return rows_skinny_t<float>(c, args, b_contr_contig); break;
-            case BI_BF16: if (skinny_ok<__nv_bfloat16>(args)) return rows_skinny_t<__nv_bfloat16>(c, args, b_contr_contig); break;
-            default: if (skinny_ok<__half>(args)) return rows_skinny_t<__half>(c, args, b_contr_contig); break;
+            case BI_F32: if (gemv_ok<float>(args)) return rows_gemv_t<float>(c, args, b_contr_contig); break;
+            case BI_BF16: if (gemv_ok<__nv_bfloat16>(args)) return rows_gemv_t<__nv_bfloat16>(c, args, b_contr_contig); break;
+            default: if (gemv_ok<__half>(args)) return rows_gemv_t<__half>(c, args, b_contr_contig); break;
         }
     }
-    if (C <= NW_TN) {  // narrow output: the tile shape changes no chain
+    if (narrow_rows(c, R, C)) {  // narrow or small output: the tile shape changes no chain
         switch (dt) {
             case BI_F32: return rows_narrow_t<float>(c, args, b_contr_contig);
             case BI_BF16: return rows_narrow_t<__nv_bfloat16>(c, args, b_contr_contig);
@@ -1137,8 +1141,9 @@ cudaError_t scalar_dw(const LaunchCtx& c, bi_dtype dt, void* out, int out_f32, c
     const int64_t J = (M + BI_DW_CHUNK - 1) / BI_DW_CHUNK;
     DwArgs args{out, out_f32, J > 1 ? partials : nullptr, a, b, M, R, C, 0, nullptr, nullptr};
     cudaError_t e;
-    if (C <= NW_TN) {  // narrow output: the tile shape changes no chain
-        const dim3 grid(static_cast<unsigned>((R + NW_TM - 1) / NW_TM), static_cast<unsigned>(J));
+    if (narrow_dw(c, R, C, J)) {  // narrow or small output: the tile shape changes no chain
+        const dim3 grid(static_cast<unsigned>((R + NW_TM - 1) / NW_TM), static_cast<unsigned>(J),
+                        static_cast<unsigned>((C + NW_TN - 1) / NW_TN));
         switch (dt) {
             case BI_F32: scalar_dw_narrow_kernel<float><<<grid, 256, 0, c.stream>>>(args); break;
             case BI_BF16: scalar_dw_narrow_kernel<__nv_bfloat16><<<grid, 256, 0, c.stream>>>(args); break;

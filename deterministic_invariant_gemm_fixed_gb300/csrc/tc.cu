@@ -60,7 +60,6 @@ struct Params {
     const float* scale_a;    // FP8: per-tensor scales applied to the f32 product
     const float* scale_b;
     int accum_out;           // f32 out, a contraction piece after the first: out += result
-    int piece_kb0, piece_kbn;  // grouped dweights: contraction blocks [kb0, kb0 + kbn) of each expert
     int split_from, split_s; // dense: tiles from split_from on run their contraction as split_s chunks
     float* partials;         // ... whose f32 results go here, 256 x BN per (tile, chunk)
     int* status;
@@ -213,18 +212,35 @@ template <> struct OutT<1> {
 // (each CTA, commit multicast), tempty[b] (CTA 0, 8 arrivals: the 4 epilogue
 // warps of each CTA).
 constexpr int P_A_BYTES = 128 * BK * 2;  // one 128 x 128-byte tile
+constexpr int SMEM_LIMIT = 227 * 1024;
 // B holds bnt / 2 rows of 128 bytes per CTA (bnt = the tile's columns).
 __host__ __device__ constexpr int p_b_bytes(int bnt) { return (bnt / 2) * BK * 2; }
 // Stage layout per operand type: one A and one B tile, or for the 3xTF32 mode
 // (IN = 3) the high and low parts of both (A_hi, B_hi, A_lo, B_lo).
 __host__ __device__ constexpr int p_tiles(int in) { return in == 3 ? 2 : 1; }
-__host__ __device__ constexpr int p_stage_bytes(int in, int bnt) { return p_tiles(in) * (P_A_BYTES + p_b_bytes(bnt)); }
-__host__ __device__ constexpr int p_stages(int in, int bnt) { return in == 3 ? 3 : (bnt == 256 ? 7 : 9); }
-__host__ __device__ constexpr int p_smem_bytes(int in, int bnt) {
-    return 1024 + p_stages(in, bnt) * p_stage_bytes(in, bnt) + BAR_BYTES;
+// bytes the copies of one stage deliver to one CTA
+__host__ __device__ constexpr int p_load_bytes(int in, int bnt) { return p_tiles(in) * (P_A_BYTES + p_b_bytes(bnt)); }
+// a stage starts on a 1024-byte boundary (the 128-byte swizzle's atom)
+__host__ __device__ constexpr int p_stage_bytes(int in, int bnt) { return (p_load_bytes(in, bnt) + 1023) / 1024 * 1024; }
+// Output staging of the TMA-store epilogue: per epilogue warp two slices of
+// 32 rows x 128 bytes (double-buffered), 32 KB per CTA.
+constexpr int OUT_STAGE_BYTES = 4 * 2 * 32 * 128;
+// as many stages as fit beside the output staging (3 for the 3xTF32 mode's
+// 64 KB stages)
+__host__ __device__ constexpr int p_stages(int in, int bnt, bool tma_out) {
+    return (SMEM_LIMIT - 1024 - BAR_BYTES - (tma_out ? OUT_STAGE_BYTES : 0)) / p_stage_bytes(in, bnt);
 }
-static_assert(p_smem_bytes(0, 256) <= 227 * 1024 && p_smem_bytes(0, 128) <= 227 * 1024 &&
-              p_smem_bytes(3, 256) <= 227 * 1024, "stages fit the shared memory of one CTA");
+__host__ __device__ constexpr int p_smem_bytes(int in, int bnt, bool tma_out) {
+    return 1024 + p_stages(in, bnt, tma_out) * p_stage_bytes(in, bnt) + (tma_out ? OUT_STAGE_BYTES : 0) + BAR_BYTES;
+}
+static_assert(p_stages(0, 256, false) == 7 && p_stages(0, 256, true) == 6 && p_stages(0, 128, true) == 8 &&
+              p_stages(3, 256, true) == 3 && p_stages(0, 176, false) == 8, "ring depths");
+static_assert(p_smem_bytes(0, 256, true) <= SMEM_LIMIT && p_smem_bytes(0, 128, true) <= SMEM_LIMIT &&
+              p_smem_bytes(3, 256, true) <= SMEM_LIMIT && p_smem_bytes(0, 256, false) <= SMEM_LIMIT,
+              "stages fit the shared memory of one CTA");
+// TMEM columns: the power of two that holds two accumulators of bnt columns;
+// accumulator b starts at column b * (allocation / 2).
+__host__ __device__ constexpr int p_tmem_cols(int bnt) { return 2 * bnt <= 256 ? 256 : 512; }
 
 __device__ __forceinline__ uint32_t mapa_rank(uint32_t saddr, uint32_t rank) {
     uint32_t r;
@@ -250,6 +266,28 @@ __device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const CUtensorMap
         : "memory");
 }
 
+// TMA store of a staged 32-row slice (2-D, or 3-D with the expert as z), in a
+// bulk async-group of the issuing thread; the group's smem reads finish before
+// cp.async.bulk.wait_group.read returns, its global writes before wait_group.
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t src, int x, int y) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(src), "r"(x), "r"(y)
+                 : "memory");
+}
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, uint32_t src, int x, int y, int z) {
+    asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(src), "r"(x), "r"(y), "r"(z)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory"); }
+template <int N>
+__device__ __forceinline__ void bulk_wait() { asm volatile("cp.async.bulk.wait_group %0;" ::"n"(N) : "memory"); }
+__device__ __forceinline__ void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
 // Raster of the dense tiles: GROUP_M row pairs share a sweep over the column
 // tiles (L2 reuse of the B columns).
 __host__ __device__ __forceinline__ void dense_raster(int t, int units_m, int num_n, int& mpair, int& nb) {
@@ -271,14 +309,36 @@ struct PairTile {
     int row0;     // grouped: first sorted row of the unit (rows) / of the expert (dweights)
     int row_end;  // grouped: end of the expert's sorted rows
     int full_kb;  // dweights: blocks read in place; block full_kb is the tail block
-    int kb0;      // first contraction block of this unit (dweights pieces, dense chunks)
-    int part;     // dense chunk: its slot in p.partials; -1 = the unit writes the output
+    int kb0;      // first contraction block of this unit (dweights chunks, dense chunks)
+    int part;     // chunk unit: its slot in p.partials; -1 = the unit writes the output
+    int npiece;   // contraction pieces (grouped dweights: runs of at most DW_PIECE_KB blocks)
 };
+
+// Contraction pieces of a unit: a grouped dweights unit walks its blocks
+// [kb0, kb0 + nkb) in pieces cut at multiples of DW_PIECE_KB blocks counted
+// from the expert's first row, each piece one run of the accumulator, the
+// pieces' f32 results added in order by the epilogue; every other unit is one
+// piece (a dense f32 dW takes its pieces as separate launches).
+constexpr int DW_PIECE_KB = static_cast<int>(TC_PIECE_ROWS / BK);
+template <int MODE>
+__device__ __forceinline__ void unit_piece(const PairTile& u, int pc, int& kb0, int& nkb) {
+    if (MODE != GROUPED_DW || u.nkb == 0) {
+        kb0 = u.kb0;
+        nkb = u.nkb;
+        return;
+    }
+    const int first = u.kb0 / DW_PIECE_KB;
+    const int lo = max(u.kb0, (first + pc) * DW_PIECE_KB);
+    const int hi = min(u.kb0 + u.nkb, (first + pc + 1) * DW_PIECE_KB);
+    kb0 = lo;
+    nkb = hi - lo;
+}
 
 template <int MODE>
 __device__ __forceinline__ bool pair_tile(const Params& p, int t, PairTile& u) {
     const int units_m = (p.num_m + 1) / 2;
     u.part = -1;
+    u.npiece = 1;
     if (MODE == DENSE) {
         // tiles [0, split_from) whole; each later tile as split_s consecutive
         // units, chunk j contracting blocks [j nkb / s, (j + 1) nkb / s)
@@ -324,10 +384,20 @@ __device__ __forceinline__ bool pair_tile(const Params& p, int t, PairTile& u) {
         u.kb0 = 0;
         return true;
     }
+    // units [0, split_from) whole; each later unit as split_s consecutive chunk
+    // units, chunk j contracting blocks [j nkb / s, (j + 1) nkb / s) of the
+    // unit's blocks in this piece (possibly none: an empty chunk)
+    int tile = t, chunk = -1;
+    if (p.split_s > 1 && t >= p.split_from) {
+        const int q = t - p.split_from;
+        tile = p.split_from + q / p.split_s;
+        chunk = q - (q / p.split_s) * p.split_s;
+        u.part = q;
+    }
     const int per = units_m * p.num_n;
-    const int g = t / per;
+    const int g = tile / per;
     if (g >= p.E) return false;
-    const int r = t - g * per;
+    const int r = tile - g * per;
     const int cnt = static_cast<int>(off[g + 1] - off[g]);
     u.g = g;
     u.mpair = r / p.num_n;
@@ -335,9 +405,14 @@ __device__ __forceinline__ bool pair_tile(const Params& p, int t, PairTile& u) {
     u.row0 = static_cast<int>(off[g]);
     u.row_end = u.row0 + cnt;
     u.full_kb = cnt / BK;
-    const int all_kb = (cnt + BK - 1) / BK;  // this piece: blocks [kb0, kb0 + nkb) of the expert
-    u.kb0 = min(p.piece_kb0, all_kb);
-    u.nkb = min(all_kb, p.piece_kb0 + p.piece_kbn) - u.kb0;
+    u.kb0 = 0;  // all of the expert's blocks, or this chunk's share of them
+    u.nkb = (cnt + BK - 1) / BK;
+    if (chunk >= 0) {
+        const int c0 = chunk * u.nkb / p.split_s;
+        u.nkb = (chunk + 1) * u.nkb / p.split_s - c0;
+        u.kb0 = c0;
+    }
+    u.npiece = u.nkb == 0 ? 1 : (u.kb0 + u.nkb - 1) / DW_PIECE_KB - u.kb0 / DW_PIECE_KB + 1;
     return true;
 }
 
@@ -411,17 +486,26 @@ template <int IN, int OUT, bool A_MN, bool B_MN, int MODE, int BNT>
 __global__ void __launch_bounds__(THREADS, 1)
     tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ CUtensorMap tmA2, const __grid_constant__ CUtensorMap tmB2,
-                        const Params p) {
+                        const __grid_constant__ CUtensorMap tmO, const Params p) {
     constexpr int ES = IN == 2 ? 1 : (IN == 3 ? 4 : 2);  // operand element size, bytes
     // the tf32 operands are always staged K-major (the split kernel transposes)
     static_assert(IN != 3 || (!A_MN && !B_MN), "3xTF32 takes K-major operands only");
     static_assert(MODE == DENSE || IN <= 1, "grouped passes take bf16 / f16 operands");
-    static_assert(BNT == 256 || (BNT == 128 && IN <= 1 && MODE == DENSE), "the 128-column tile: 16-bit dense");
+    // tile widths: 256, or for 16-bit operands any multiple of 16 from 128 up;
+    // an MN-major B tile is whole 64-column swizzle atoms per CTA (128 or 256)
+    static_assert(BNT == 256 || (IN <= 1 && BNT % 16 == 0 && BNT >= 128 && BNT < 256 && MODE != GROUPED_DW &&
+                                 (!B_MN || BNT == 128)),
+                  "tile width");
     constexpr int BN = BNT;                 // tile columns = MMA N
-    constexpr int TMEM_COLS = 2 * BN;
+    constexpr int TMEM_COLS = p_tmem_cols(BN);
+    constexpr int ACC_STRIDE = TMEM_COLS / 2;  // TMEM columns from one accumulator to the next
     constexpr int P_B_BYTES = p_b_bytes(BN);
-    constexpr int P_STAGES = p_stages(IN, BN);
+    // the TMA-store epilogue writes every output laid out as rows of the tile
+    // (not the grouped rows, which go to rows perm[s])
+    constexpr bool TMAO = MODE != GROUPED_ROWS;
+    constexpr int P_STAGES = p_stages(IN, BN, TMAO);
     constexpr int P_STAGE_BYTES = p_stage_bytes(IN, BN);
+    constexpr int P_LOAD_BYTES = p_load_bytes(IN, BN);
     constexpr int BKE = 128 / ES;           // contraction elements per block
     constexpr int NACC = IN == 3 ? 1 : 2;   // accumulator buffers in flight
     constexpr int MN_ATOMS = ES;            // 128-byte atoms across a 128-wide MN-major tile
@@ -431,7 +515,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     const uint32_t raw = smem_u32(smem_raw);
     uint8_t* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
     const uint32_t sbase = smem_u32(smem);
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + P_STAGES * P_STAGE_BYTES);
+    uint8_t* out_stage = smem + P_STAGES * P_STAGE_BYTES;  // 1024-aligned; used when TMAO
+    uint64_t* bars = reinterpret_cast<uint64_t*>(out_stage + (TMAO ? OUT_STAGE_BYTES : 0));
     const uint32_t bar0 = smem_u32(bars);
     auto full_bar = [&](int s) { return bar0 + 8u * s; };
     auto empty_bar = [&](int s) { return bar0 + 8u * (P_STAGES + s); };
@@ -486,14 +571,17 @@ __global__ void __launch_bounds__(THREADS, 1)
             // A rows (MN-major: A columns) and B columns of this CTA
             const int arow = (MODE == GROUPED_ROWS ? u.row0 : u.mpair * 256) + static_cast<int>(crank) * 128;
             const int bcol = u.nb * BN + static_cast<int>(crank) * (BN / 2);
-            for (int kb = 0; kb < u.nkb; ++kb) {
+            for (int pc = 0; pc < u.npiece; ++pc) {
+            int pkb0, pnkb;
+            unit_piece<MODE>(u, pc, pkb0, pnkb);
+            for (int kb = 0; kb < pnkb; ++kb) {
                 if (!mbar_wait(empty_bar(s), ph ^ 1u, abort_flag, p, DEV_TIMEOUT_PRODUCER)) goto done_p;
                 const uint32_t fb_leader = mapa_rank(full_bar(s), 0);
-                if (crank == 0) mbar_expect_tx(full_bar(s), 2 * P_STAGE_BYTES);
-                int kofs = (u.kb0 + kb) * BKE;  // contraction coordinate
+                if (crank == 0) mbar_expect_tx(full_bar(s), 2 * P_LOAD_BYTES);
+                int kofs = (pkb0 + kb) * BKE;  // contraction coordinate
                 bool tail = false;
                 if (MODE == GROUPED_DW) {  // the expert's rows in place, or its tail block
-                    const int kba = u.kb0 + kb;
+                    const int kba = pkb0 + kb;
                     tail = kba == u.full_kb;
                     kofs = tail ? u.g * BKE : u.row0 + kba * BKE;
                 }
@@ -526,6 +614,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 }
                 if (++s == P_STAGES) { s = 0; ph ^= 1u; }
             }
+            }
         }
     done_p:;
         // Copies of this CTA complete on CTA 0's barriers; CTA 0's MMA thread
@@ -540,13 +629,15 @@ __global__ void __launch_bounds__(THREADS, 1)
         uint32_t aph = 0;
         PairTile u;
         for (int t = cidx; pair_tile<MODE>(p, t, u); t += ncl) {
-            if (u.nkb == 0) continue;  // empty expert: the epilogue writes +0
-            if (!mbar_wait(tempty_bar(ab), aph ^ 1u, abort_flag, p, DEV_TIMEOUT_MMA)) break;
+          for (int pc = 0; pc < u.npiece; ++pc) {
+            int pkb0, pnkb;
+            unit_piece<MODE>(u, pc, pkb0, pnkb);
+            if (pnkb == 0) continue;  // empty expert or chunk: the epilogue writes +0 (-0 for a chunk)
+            if (!mbar_wait(tempty_bar(ab), aph ^ 1u, abort_flag, p, DEV_TIMEOUT_MMA)) goto done_m;
             tc_fence_after();
-            const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(ab * BN);
-            bool ok = true;
-            for (int kb = 0; kb < u.nkb; ++kb) {
-                if (!mbar_wait(full_bar(s), ph, abort_flag, p, DEV_TIMEOUT_MMA)) { ok = false; break; }
+            const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(ab * ACC_STRIDE);
+            for (int kb = 0; kb < pnkb; ++kb) {
+                if (!mbar_wait(full_bar(s), ph, abort_flag, p, DEV_TIMEOUT_MMA)) goto done_m;
                 tc_fence_after();
                 const uint32_t a_s = sbase + s * P_STAGE_BYTES;
                 const uint32_t b_s = a_s + P_A_BYTES;
@@ -573,10 +664,11 @@ __global__ void __launch_bounds__(THREADS, 1)
                 mma_commit_pair_mc(empty_bar(s), 0x3);
                 if (++s == P_STAGES) { s = 0; ph ^= 1u; }
             }
-            if (!ok) break;
             mma_commit_pair_mc(tfull_bar(ab), 0x3);
             if (++ab == NACC) { ab = 0; aph ^= 1u; }
+          }
         }
+    done_m:
         mma_commit_pair(drain_bar);
         mbar_wait(drain_bar, 0, abort_flag, p, DEV_TIMEOUT_MMA);
     } else if (warp >= 2) {
@@ -588,6 +680,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         int ab = 0;
         uint32_t aph = 0;
         const float scale = IN == 2 ? __fmul_rn(__ldg(p.scale_a), __ldg(p.scale_b)) : 1.0f;
+        int oslot = 0;  // output slices this warp has staged (TMA-store epilogue)
         PairTile u;
         for (int t = cidx; pair_tile<MODE>(p, t, u); t += ncl) {
             int64_t orow = -1;  // output row of this thread, or -1
@@ -612,20 +705,34 @@ __global__ void __launch_bounds__(THREADS, 1)
                             : 0.0f;
             }
             static_assert(BN <= 8 * 32, "one 8-column bias slice per lane");
-            if (u.nkb == 0) {  // no rows of the expert in this piece: +0 from the first piece only
-                if (orow >= 0 && !p.accum_out)
+          for (int pc = 0; pc < u.npiece; ++pc) {
+            int pkb0, pnkb;
+            unit_piece<MODE>(u, pc, pkb0, pnkb);
+            // the result is added to the sum so far: a grouped dweights piece after
+            // the first, or a dense f32 dW launch after the first
+            const bool add_prev = MODE == GROUPED_DW ? pc > 0 : p.accum_out != 0;
+            if (pnkb == 0) {
+                if (MODE == GROUPED_DW && u.part >= 0) {
+                    // an empty chunk: -0, the exact identity of the chunk sum's additions
+                    float* dst = p.partials + static_cast<int64_t>(u.part) * (256 * BN) +
+                                 static_cast<int64_t>(crank * 128 + r) * BN;
+                    for (int c = 0; c < BN; ++c) dst[c] = -0.0f;
+                } else if (orow >= 0 && !add_prev) {  // an expert with no rows: +0
                     for (int64_t c = col0; c < col0 + BN && c < p.cols; ++c)
                         static_cast<float*>(out)[orow * p.ldo + c] = 0.0f;
+                }
                 continue;
             }
             bool ok = mbar_wait(tfull_bar(ab), aph, abort_flag, p, DEV_TIMEOUT_EPILOGUE);
             ok = __all_sync(0xffffffffu, ok);
-            if (!ok) break;
+            if (!ok) goto done_e;
             tc_fence_after();
             const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
-                                   static_cast<uint32_t>(ab * BN);
-            for (int c0 = 0; c0 < BN; c0 += 16) {
-                if (col0 + c0 >= p.cols) break;
+                                   static_cast<uint32_t>(ab * ACC_STRIDE);
+            // f = the finished f32 results of columns col0 + c0 .. c0 + 15 of this
+            // thread's row: the accumulator (+ the 3xTF32 cross terms, x the FP8
+            // scales), + the earlier pieces' sum, + the bias.  All lanes take part.
+            auto values16 = [&](int c0, float (&f)[16]) {
                 __syncwarp();  // lanes past the output rows rejoin before the aligned load
                 uint32_t v[16];
                 tmem_ld16(tbase + c0, v);
@@ -636,18 +743,6 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
                     for (int i = 0; i < 16; ++i) bias16[i] = __shfl_sync(0xffffffffu, bv[i & 7], (c0 >> 3) + (i >> 3));
                 }
-                if (IN <= 2 && MODE == DENSE && u.part >= 0) {  // a chunk's raw f32 sum (unscaled)
-                    float* dst = p.partials + static_cast<int64_t>(u.part) * (256 * BN) +
-                                 static_cast<int64_t>(crank * 128 + r) * BN + c0;
-#pragma unroll
-                    for (int i = 0; i < 16; i += 4)
-                        *reinterpret_cast<float4*>(dst + i) =
-                            make_float4(__uint_as_float(v[i]), __uint_as_float(v[i + 1]), __uint_as_float(v[i + 2]),
-                                        __uint_as_float(v[i + 3]));
-                    continue;
-                }
-                if (orow < 0) continue;
-                float f[16];
 #pragma unroll
                 for (int i = 0; i < 16; ++i) f[i] = __uint_as_float(v[i]);
                 if (IN == 3) {
@@ -661,18 +756,92 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
                     for (int i = 0; i < 16; ++i) f[i] = __fmul_rn(f[i], scale);
                 }
-                if (OUT == 2 && p.accum_out) {  // the earlier pieces' sum, left by the previous launch
-                    const float* prev = static_cast<const float*>(out) + orow * p.ldo + col0 + c0;
+                const int64_t cb = col0 + c0;
+                if (OUT == 2 && add_prev && orow >= 0) {  // the earlier pieces' sum, left in the output
+                    const float* prev = static_cast<const float*>(out) + orow * p.ldo + cb;
 #pragma unroll
                     for (int i = 0; i < 16; ++i)
-                        if (col0 + c0 + i < p.cols) f[i] = __fadd_rn(prev[i], f[i]);
+                        if (cb + i < p.cols) f[i] = __fadd_rn(prev[i], f[i]);
                 }
-                const int64_t cb = col0 + c0;
                 if (p.bias != nullptr) {  // the bias has the output's type
 #pragma unroll
                     for (int i = 0; i < 16; ++i)
                         if (cb + i < p.cols) f[i] = __fadd_rn(f[i], bias16[i]);
                 }
+            };
+            const bool to_partials = IN <= 2 && MODE != GROUPED_ROWS && u.part >= 0;
+            if (TMAO && !to_partials && !(MODE == GROUPED_DW && u.npiece > 1)) {
+                // TMA-store epilogue: this warp's 32 rows go out in slices of 128
+                // bytes per row, staged in shared memory with the 128-byte swizzle
+                // (16-byte chunk c of row r at chunk c ^ (r % 8)), two slices in
+                // flight per warp
+                constexpr int OES = OUT == 2 ? 4 : 2;  // output element size
+                constexpr int CPS = 128 / OES;         // columns per slice
+                const int rowbase = u.mpair * 256 + static_cast<int>(crank) * 128 + q * 32;
+                for (int cs = 0; cs < BN; cs += CPS) {
+                    if (col0 + cs >= p.cols) break;
+                    if (lane == 0) bulk_wait_read<1>();  // the slice stored two slices ago has been read
+                    __syncwarp();
+                    const uint32_t buf = smem_u32(out_stage) + static_cast<uint32_t>(q * 8192 + (oslot & 1) * 4096);
+                    const uint32_t rowaddr = buf + static_cast<uint32_t>(lane * 128);
+#pragma unroll
+                    for (int c16 = 0; c16 < CPS; c16 += 16) {
+                        float f[16];
+                        values16(cs + c16, f);
+                        const int cc0 = c16 * OES / 16;  // first 16-byte chunk of these columns
+                        if (OUT == 2) {
+#pragma unroll
+                            for (int i = 0; i < 4; ++i)
+                                asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(
+                                                 rowaddr + static_cast<uint32_t>(((cc0 + i) ^ (lane & 7)) * 16)),
+                                             "f"(f[4 * i]), "f"(f[4 * i + 1]), "f"(f[4 * i + 2]), "f"(f[4 * i + 3])
+                                             : "memory");
+                        } else {
+                            using O = OutT<OUT == 1 ? 1 : 0>;
+#pragma unroll
+                            for (int i = 0; i < 2; ++i)
+                                asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(
+                                                 rowaddr + static_cast<uint32_t>(((cc0 + i) ^ (lane & 7)) * 16)),
+                                             "r"(O::pack(f[8 * i], f[8 * i + 1])), "r"(O::pack(f[8 * i + 2], f[8 * i + 3])),
+                                             "r"(O::pack(f[8 * i + 4], f[8 * i + 5])), "r"(O::pack(f[8 * i + 6], f[8 * i + 7]))
+                                             : "memory");
+                        }
+                    }
+                    fence_proxy_async_smem();  // this lane's rows are visible to the store
+                    __syncwarp();
+                    if (lane == 0) {
+                        if (MODE == GROUPED_DW) tma_store_3d(&tmO, buf, static_cast<int>(col0) + cs, rowbase, u.g);
+                        else tma_store_2d(&tmO, buf, static_cast<int>(col0) + cs, rowbase);
+                        bulk_commit();
+                    }
+                    ++oslot;
+                }
+            } else {
+            for (int c0 = 0; c0 < BN; c0 += 16) {
+                if (col0 + c0 >= p.cols) break;
+                if (to_partials) {  // a chunk's raw f32 sum (unscaled)
+                    __syncwarp();
+                    uint32_t v[16];
+                    tmem_ld16(tbase + c0, v);
+                    float* dst = p.partials + static_cast<int64_t>(u.part) * (256 * BN) +
+                                 static_cast<int64_t>(crank * 128 + r) * BN + c0;
+#pragma unroll
+                    for (int i = 0; i < 16; i += 4) {
+                        float4 w4 = make_float4(__uint_as_float(v[i]), __uint_as_float(v[i + 1]),
+                                                __uint_as_float(v[i + 2]), __uint_as_float(v[i + 3]));
+                        if (MODE == GROUPED_DW && add_prev) {  // the chunk's earlier pieces, left here
+                            const float4 pv = *reinterpret_cast<const float4*>(dst + i);
+                            w4 = make_float4(__fadd_rn(pv.x, w4.x), __fadd_rn(pv.y, w4.y), __fadd_rn(pv.z, w4.z),
+                                             __fadd_rn(pv.w, w4.w));
+                        }
+                        *reinterpret_cast<float4*>(dst + i) = w4;
+                    }
+                    continue;
+                }
+                float f[16];
+                values16(c0, f);
+                if (orow < 0) continue;
+                const int64_t cb = col0 + c0;
                 const bool full = cb + 16 <= p.cols;
                 if (OUT == 2) {
                     float* dst = static_cast<float*>(out) + orow * p.ldo + cb;
@@ -706,11 +875,15 @@ __global__ void __launch_bounds__(THREADS, 1)
                     }
                 }
             }
+            }
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive_cluster(ab ? tempty_leader1 : tempty_leader0);
             if (++ab == NACC) { ab = 0; aph ^= 1u; }
+          }
         }
+    done_e:
+        if (TMAO && lane == 0) bulk_wait<0>();  // this warp's stores are complete before the CTA exits
     }
 
     // ---------------------------------------------------------------- teardown
@@ -747,7 +920,7 @@ __global__ void __launch_bounds__(256) dw_chunk_sum_kernel(const float* __restri
                                                            int split_s, int split_tiles, int units_m, int num_n,
                                                            int bn, void* out, int64_t ldo, int64_t rows,
                                                            int64_t cols, int accum_out, const float* scale_a,
-                                                           const float* scale_b) {
+                                                           const float* scale_b, int grouped) {
     grid_dep_wait();
     grid_dep_launch();
     const int64_t slot = 256 * static_cast<int64_t>(bn);
@@ -758,7 +931,15 @@ __global__ void __launch_bounds__(256) dw_chunk_sum_kernel(const float* __restri
     const int64_t e = (idx - ti * per_tile) * 4;  // row * bn + first column within the tile
     const int row = static_cast<int>(e / bn), col = static_cast<int>(e - static_cast<int64_t>(row) * bn);
     int mpair, nb;
-    dense_raster(split_from + ti, units_m, num_n, mpair, nb);
+    if (grouped) {  // grouped dweights: unit = (expert, row pair-tile, column tile), out [E][rows][ldo]
+        const int t = split_from + ti, per = units_m * num_n;
+        const int g = t / per, rr = t - g * per;
+        mpair = rr / num_n;
+        nb = rr - mpair * num_n;
+        out = static_cast<float*>(out) + static_cast<int64_t>(g) * rows * ldo;
+    } else {
+        dense_raster(split_from + ti, units_m, num_n, mpair, nb);
+    }
     const int64_t gr = static_cast<int64_t>(mpair) * 256 + row, gc = static_cast<int64_t>(nb) * bn + col;
     if (gr >= rows || gc >= cols) return;  // cols is a multiple of 8: the 4 columns are inside
     const float* src = partials + static_cast<int64_t>(ti) * split_s * slot + e;
@@ -774,6 +955,7 @@ __global__ void __launch_bounds__(256) dw_chunk_sum_kernel(const float* __restri
         n = (n + 1) / 2;
     }
     float4 r = v[0];
+    if (grouped && !accum_out) r = add4(r, make_float4(0.f, 0.f, 0.f, 0.f));  // an expert with no rows: +0
     if (scale_a != nullptr) {
         const float sc = __fmul_rn(__ldg(scale_a), __ldg(scale_b));
         r = make_float4(__fmul_rn(r.x, sc), __fmul_rn(r.y, sc), __fmul_rn(r.z, sc), __fmul_rn(r.w, sc));
@@ -793,14 +975,14 @@ __global__ void __launch_bounds__(256) dw_chunk_sum_kernel(const float* __restri
 template <int OUT>
 cudaError_t launch_chunk_sum(const LaunchCtx& c, const float* ws, int split_from, int sp, int64_t split_tiles,
                              int units_m, int num_n, int bn, void* out, int64_t ldo, int64_t rows, int64_t cols,
-                             int accum_out, const float* sa, const float* sb) {
+                             int accum_out, const float* sa, const float* sb, int grouped = 0) {
     auto kern = sp <= 2 ? dw_chunk_sum_kernel<OUT, 2>
               : sp <= 4 ? dw_chunk_sum_kernel<OUT, 4>
               : sp <= 8 ? dw_chunk_sum_kernel<OUT, 8> : dw_chunk_sum_kernel<OUT, 16>;
     const int64_t threads = split_tiles * 256 * bn / 4;
     cudaError_t e = launch_pdl(kern, dim3(static_cast<unsigned>((threads + 255) / 256)), dim3(256), 0, c.stream, ws,
                                split_from, sp, static_cast<int>(split_tiles), units_m, num_n, bn, out, ldo, rows,
-                               cols, accum_out, sa, sb);
+                               cols, accum_out, sa, sb, grouped);
     if (e == cudaSuccess) c.count();
     return e;
 }
@@ -840,13 +1022,38 @@ cudaError_t make_map(CUtensorMap* m, bi_dtype dt, const void* ptr, uint64_t inne
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+// Output [depth][outer][inner] (row stride ld elements; out_fmt 0 f16, 1 bf16,
+// 2 f32) for the TMA-store epilogue: box {128 bytes of columns, 32 rows (, 1)},
+// 128-byte swizzle; stores past the extents are clipped.
+cudaError_t make_out_map(CUtensorMap* m, int out_fmt, const void* ptr, uint64_t inner, uint64_t outer, uint64_t ld,
+                         uint64_t depth = 1, bool rank3 = false) {
+    auto enc = encode_fn();
+    if (!enc) return cudaErrorNotSupported;
+    const CUtensorMapDataType t = out_fmt == 2 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                : out_fmt == 1 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                               : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    const uint64_t es = out_fmt == 2 ? 4 : 2;
+    cuuint64_t dims[3] = {inner, outer, depth};
+    cuuint64_t strides[2] = {ld * es, ld * outer * es};
+    cuuint32_t box[3] = {static_cast<cuuint32_t>(128 / es), 32, 1};
+    cuuint32_t el[3] = {1, 1, 1};
+    CUresult r = enc(m, t, rank3 ? 3 : 2, const_cast<void*>(ptr), dims, strides, box, el,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 // units: work units (or an upper bound, for the grouped modes, whose count is
 // known only on the device); -1 = the dense count.
+// o: the output's tensor map for the TMA-store epilogue (every mode but the
+// grouped rows, which pass null).
 template <int IN, int OUT, bool A_MN, bool B_MN, int MODE = DENSE, int BNT = BN>
 cudaError_t launch_pair(const LaunchCtx& c, const CUtensorMap& a, const CUtensorMap& b, Params p,
-                        const CUtensorMap* a2 = nullptr, const CUtensorMap* b2 = nullptr, int64_t units = -1) {
+                        const CUtensorMap* o, const CUtensorMap* a2 = nullptr, const CUtensorMap* b2 = nullptr,
+                        int64_t units = -1) {
     auto kern = tc_gemm_pair_kernel<IN, OUT, A_MN, B_MN, MODE, BNT>;
-    constexpr int P_SMEM_BYTES = p_smem_bytes(IN, BNT);
+    constexpr int P_SMEM_BYTES = p_smem_bytes(IN, BNT, MODE != GROUPED_ROWS);
+    if (MODE != GROUPED_ROWS && o == nullptr) return cudaErrorInvalidValue;
     static PerDeviceOnce setup;  // per device: the shared-memory opt-in and the co-resident clusters
     cudaLaunchAttribute at[1];
     at[0].id = cudaLaunchAttributeClusterDimension;
@@ -883,15 +1090,26 @@ cudaError_t launch_pair(const LaunchCtx& c, const CUtensorMap& a, const CUtensor
     la[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = la;
     cfg.numAttrs = 2;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, a, b, a2 ? *a2 : a, b2 ? *b2 : b, p);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, a, b, a2 ? *a2 : a, b2 ? *b2 : b, o ? *o : a, p);
     if (e != cudaSuccess) return e;
     c.count();
     return cudaGetLastError();
 }
 
-template <int FMT>
-cudaError_t forward_t(const LaunchCtx& c, bi_dtype dt, void* y, const void* x, const void* w,
-                      const void* bias, int64_t M, int64_t K, int64_t N) {
+// Column tile of a pass: the engine's forced width (bi_engine_set_tile_cols)
+// where the pass's B layout takes it, else the automatic choice.  Tile widths
+// only decide how outputs are grouped into work units: every output element is
+// the same ascending chain of 64-wide contraction blocks in one accumulator.
+int pick_cols(const LaunchCtx& c, int automatic, bool b_mn_major) {
+    const int f = c.eng ? c.eng->tile_cols : 0;
+    if (f == 256 || f == 128) return f;
+    if (!b_mn_major && (f == 176 || f == 192)) return f;
+    return automatic;
+}
+
+template <int FMT, int BNT>
+cudaError_t forward_impl(const LaunchCtx& c, bi_dtype dt, void* y, const void* x, const void* w,
+                         const void* bias, int64_t M, int64_t K, int64_t N) {
     CUtensorMap a, b;
     cudaError_t e;
     if ((e = make_map(&a, dt, x, K, M, 1, BM)) != cudaSuccess) return e;   // X [M,K], K-major
@@ -899,24 +1117,43 @@ cudaError_t forward_t(const LaunchCtx& c, bi_dtype dt, void* y, const void* x, c
     Params p{};
     p.out = y; p.ldo = N; p.rows = M; p.cols = N; p.bias = bias;
     p.num_m = static_cast<int>((M + BM - 1) / BM);
-    p.num_n = static_cast<int>((N + BN - 1) / BN);
+    p.num_n = static_cast<int>((N + BNT - 1) / BNT);
     p.num_kb = static_cast<int>((K + BK - 1) / BK);
-    return launch_pair<FMT, FMT, false, true>(c, a, b, p);
+    CUtensorMap o;
+    if ((e = make_out_map(&o, FMT, y, N, M, N)) != cudaSuccess) return e;
+    return launch_pair<FMT, FMT, false, true, DENSE, BNT>(c, a, b, p, &o);
+}
+
+template <int FMT>
+cudaError_t forward_t(const LaunchCtx& c, bi_dtype dt, void* y, const void* x, const void* w,
+                      const void* bias, int64_t M, int64_t K, int64_t N) {
+    return pick_cols(c, BN, true) == 128 ? forward_impl<FMT, 128>(c, dt, y, x, w, bias, M, K, N)
+                                         : forward_impl<FMT, 256>(c, dt, y, x, w, bias, M, K, N);
+}
+
+template <int FMT, int BNT>
+cudaError_t dx_impl(const LaunchCtx& c, bi_dtype dt, void* dx, const void* dy, const void* w,
+                    int64_t M, int64_t K, int64_t N) {
+    CUtensorMap a, b;
+    cudaError_t e;
+    if ((e = make_map(&a, dt, dy, N, M, 1, BM)) != cudaSuccess) return e;  // dY [M,N], K-major
+    if ((e = make_map(&b, dt, w, N, K, 1, BNT / 2)) != cudaSuccess) return e;  // W [K,N]: rows k, contraction n; half tile per CTA
+    Params p{};
+    p.out = dx; p.ldo = K; p.rows = M; p.cols = K;
+    p.num_m = static_cast<int>((M + BM - 1) / BM);
+    p.num_n = static_cast<int>((K + BNT - 1) / BNT);
+    p.num_kb = static_cast<int>((N + BK - 1) / BK);
+    CUtensorMap o;
+    if ((e = make_out_map(&o, FMT, dx, K, M, K)) != cudaSuccess) return e;
+    return launch_pair<FMT, FMT, false, false, DENSE, BNT>(c, a, b, p, &o);
 }
 
 template <int FMT>
 cudaError_t dx_t(const LaunchCtx& c, bi_dtype dt, void* dx, const void* dy, const void* w,
                  int64_t M, int64_t K, int64_t N) {
-    CUtensorMap a, b;
-    cudaError_t e;
-    if ((e = make_map(&a, dt, dy, N, M, 1, BM)) != cudaSuccess) return e;  // dY [M,N], K-major
-    if ((e = make_map(&b, dt, w, N, K, 1, BN / 2)) != cudaSuccess) return e;  // W [K,N]: rows k, contraction n; half tile per CTA
-    Params p{};
-    p.out = dx; p.ldo = K; p.rows = M; p.cols = K;
-    p.num_m = static_cast<int>((M + BM - 1) / BM);
-    p.num_n = static_cast<int>((K + BN - 1) / BN);
-    p.num_kb = static_cast<int>((N + BK - 1) / BK);
-    return launch_pair<FMT, FMT, false, false>(c, a, b, p);
+    // (W is K-major here, but dX instantiates the 128- and 256-column tiles only)
+    return pick_cols(c, BN, true) == 128 ? dx_impl<FMT, 128>(c, dt, dx, dy, w, M, K, N)
+                                         : dx_impl<FMT, 256>(c, dt, dx, dy, w, M, K, N);
 }
 
 // Tile width of the 16-bit dW, a function of K and N only: 128 columns when
@@ -947,10 +1184,11 @@ struct DwShape {
     int bnt;        // tile columns
     int64_t tiles;  // output tiles of K x N
 };
-DwShape dw_shape(int64_t K, int64_t N) {
-    const int bnt = narrow_dw(K, N) ? 128 : 256;
+DwShape dw_shape(int64_t K, int64_t N, int forced = 0) {
+    const int bnt = forced == 128 || forced == 256 ? forced : (narrow_dw(K, N) ? 128 : 256);
     return {bnt, ((K + BM - 1) / BM + 1) / 2 * ((N + bnt - 1) / bnt)};
 }
+int forced_cols(const LaunchCtx& c) { return c.eng ? c.eng->tile_cols : 0; }
 
 template <int FMT, bool F32, int BNT>
 cudaError_t dw_t(const LaunchCtx& c, bi_dtype dt, void* dw, const void* x, const void* dy,
@@ -980,7 +1218,9 @@ cudaError_t dw_t(const LaunchCtx& c, bi_dtype dt, void* dw, const void* x, const
         p.split_from = static_cast<int>(sp > 1 ? tiles - tiles % DW_WAVE : tiles);
         p.partials = ws;
         const int64_t split_tiles = tiles - p.split_from;
-        if ((e = launch_pair<FMT, F32 ? 2 : FMT, true, true, DENSE, BNT>(c, a, b, p, nullptr, nullptr,
+        CUtensorMap o;
+        if ((e = make_out_map(&o, F32 ? 2 : FMT, dw, N, K, N)) != cudaSuccess) return e;
+        if ((e = launch_pair<FMT, F32 ? 2 : FMT, true, true, DENSE, BNT>(c, a, b, p, &o, nullptr, nullptr,
                                                                           p.split_from + split_tiles * sp)) !=
             cudaSuccess)
             return e;
@@ -992,35 +1232,73 @@ cudaError_t dw_t(const LaunchCtx& c, bi_dtype dt, void* dw, const void* x, const
     return cudaSuccess;
 }
 
-template <int FMT>
-cudaError_t grouped_rows_t(const LaunchCtx& c, bi_dtype dt, int dinput, void* out, const void* a_sorted,
-                           const void* w, int64_t M, int64_t K, int64_t N, int64_t E, const uint32_t* seg,
-                           const uint32_t* perm) {
+template <int FMT, int BNT>
+cudaError_t grouped_rows_impl(const LaunchCtx& c, bi_dtype dt, int dinput, void* out, const void* a_sorted,
+                              const void* w, int64_t M, int64_t K, int64_t N, int64_t E, const uint32_t* seg,
+                              const uint32_t* perm) {
     const int64_t L = dinput ? N : K;  // contraction
     const int64_t C = dinput ? K : N;  // output columns
     CUtensorMap a, b;
     cudaError_t e;
     // A = the row-sorted operand [M,L], K-major, 128 rows per CTA
     if ((e = make_map(&a, dt, a_sorted, L, M, 1, BM)) != cudaSuccess) return e;
-    // B = W[g] [N,K] (3-D map): forward reads rows n (K-major, 128 per CTA);
+    // B = W[g] [N,K] (3-D map): forward reads rows n (K-major, BNT / 2 per CTA);
     // dinput reads it with the output index k contiguous (MN-major)
-    if ((e = make_map(&b, dt, w, K, N, E, dinput ? BK : BN / 2, true)) != cudaSuccess) return e;
+    if ((e = make_map(&b, dt, w, K, N, E, dinput ? BK : BNT / 2, true)) != cudaSuccess) return e;
     Params p{};
     p.seg = seg; p.perm = perm; p.E = static_cast<int>(E);
     p.out = out; p.ldo = C; p.rows = M; p.cols = C;
     p.num_m = 0;
-    p.num_n = static_cast<int>((C + BN - 1) / BN);
+    p.num_n = static_cast<int>((C + BNT - 1) / BNT);
     p.num_kb = static_cast<int>((L + BK - 1) / BK);
     // the experts' 256-row tiles number at most floor(M / 256) + E
     const int64_t units = (M / GROUPED_TILE_ROWS + E) * p.num_n;
-    return dinput ? launch_pair<FMT, FMT, false, true, GROUPED_ROWS>(c, a, b, p, nullptr, nullptr, units)
-                  : launch_pair<FMT, FMT, false, false, GROUPED_ROWS>(c, a, b, p, nullptr, nullptr, units);
+    if (dinput) {
+        if constexpr (BNT == 128 || BNT == 256)
+            return launch_pair<FMT, FMT, false, true, GROUPED_ROWS, BNT>(c, a, b, p, nullptr, nullptr, nullptr, units);
+        return cudaErrorInvalidValue;
+    }
+    return launch_pair<FMT, FMT, false, false, GROUPED_ROWS, BNT>(c, a, b, p, nullptr, nullptr, nullptr, units);
+}
+
+template <int FMT>
+cudaError_t grouped_rows_t(const LaunchCtx& c, bi_dtype dt, int dinput, void* out, const void* a_sorted,
+                           const void* w, int64_t M, int64_t K, int64_t N, int64_t E, const uint32_t* seg,
+                           const uint32_t* perm) {
+    // 256 columns unless forced: narrower tiles measured slower for the grouped
+    // workload (N = 1408 as 8 x 176 instead of 5.5 x 256: 112 against 103 us)
+    const int cols = pick_cols(c, BN, dinput != 0);
+    switch (cols) {
+        case 128: return grouped_rows_impl<FMT, 128>(c, dt, dinput, out, a_sorted, w, M, K, N, E, seg, perm);
+        case 176: return grouped_rows_impl<FMT, 176>(c, dt, dinput, out, a_sorted, w, M, K, N, E, seg, perm);
+        case 192: return grouped_rows_impl<FMT, 192>(c, dt, dinput, out, a_sorted, w, M, K, N, E, seg, perm);
+        default: return grouped_rows_impl<FMT, 256>(c, dt, dinput, out, a_sorted, w, M, K, N, E, seg, perm);
+    }
+}
+
+// Grouped dweights: E x (N / 256) x (K / 256) units whatever the batch; the
+// units of the last, partial wave on 76 CTA pairs contract in s chunks of
+// consecutive 64-row blocks of the expert's rows in the piece (s = min(76 /
+// tail units, 16, about 1 chunk per 8 blocks of an average expert), chosen
+// from M, E, N and K), added by the dW tree in dw_chunk_sum_kernel.
+struct GroupedDwSplit {
+    int64_t units, split_from;
+    int sp;
+};
+GroupedDwSplit grouped_dw_split(int64_t M, int64_t K, int64_t N, int64_t E) {
+    const int64_t units_m = ((N + BM - 1) / BM + 1) / 2, num_n = (K + BN - 1) / BN;
+    const int64_t units = E * units_m * num_n;
+    const int64_t tail = units % DW_WAVE;
+    const int64_t avg_kb = lmin(M / E, TC_PIECE_ROWS) / BK;  // blocks of an average expert in one piece
+    int64_t sp = tail ? lmin(lmin(DW_WAVE / tail, DW_MAX_CHUNKS), avg_kb / DW_MIN_CHUNK_KB) : 1;
+    if (sp < 2) sp = 1;
+    return {units, sp > 1 ? units - tail : units, static_cast<int>(sp)};
 }
 
 template <int FMT>
 cudaError_t grouped_dw_t(const LaunchCtx& c, bi_dtype dt, float* dw, const void* dy_sorted, const void* x_sorted,
                          const void* dy_tail, const void* x_tail, int64_t M, int64_t K, int64_t N, int64_t E,
-                         const uint32_t* seg) {
+                         const uint32_t* seg, float* ws) {
     // dW[g] [N,K] = sum over the expert's rows of dY^T X: both operands MN-major
     CUtensorMap a, b, a2, b2;
     cudaError_t e;
@@ -1034,16 +1312,23 @@ cudaError_t grouped_dw_t(const LaunchCtx& c, bi_dtype dt, float* dw, const void*
     p.num_m = static_cast<int>((N + BM - 1) / BM);
     p.num_n = static_cast<int>((K + BN - 1) / BN);
     p.num_kb = 0;
-    const int64_t units = E * int64_t((p.num_m + 1) / 2) * p.num_n;
-    // each expert's rows in pieces of TC_PIECE_ROWS (no expert has more than M
-    // rows); a unit with no rows in a later piece leaves dweights untouched
-    const int piece_kb = static_cast<int>(TC_PIECE_ROWS / BK);
-    for (int64_t j = 0; j * TC_PIECE_ROWS < M || j == 0; ++j) {
-        p.piece_kb0 = static_cast<int>(j) * piece_kb;
-        p.piece_kbn = piece_kb;
-        p.accum_out = j > 0 ? 1 : 0;
-        if ((e = launch_pair<FMT, 2, true, true, GROUPED_DW>(c, a, b, p, &a2, &b2, units)) != cudaSuccess) return e;
-    }
+    const GroupedDwSplit sd = grouped_dw_split(M, K, N, E);
+    if (sd.sp > 1 && ws == nullptr) return cudaErrorInvalidValue;
+    p.split_s = sd.sp;
+    p.split_from = static_cast<int>(sd.split_from);
+    p.partials = ws;
+    const int64_t split_units = sd.units - sd.split_from;
+    const int64_t launch_units = sd.split_from + split_units * sd.sp;
+    // one launch: each unit walks its expert's rows (or its chunk of them) in
+    // pieces of TC_PIECE_ROWS rows counted from the expert's first row, adding
+    // the pieces' results in order
+    CUtensorMap o;  // dW [E][N][K]
+    if ((e = make_out_map(&o, 2, dw, K, N, K, E, true)) != cudaSuccess) return e;
+    if ((e = launch_pair<FMT, 2, true, true, GROUPED_DW>(c, a, b, p, &o, &a2, &b2, launch_units)) != cudaSuccess)
+        return e;
+    if (sd.sp > 1)
+        return launch_chunk_sum<2>(c, ws, p.split_from, sd.sp, split_units, (p.num_m + 1) / 2, p.num_n, BN, dw, p.ldo,
+                                   p.rows, p.cols, 0, nullptr, nullptr, 1);
     return cudaSuccess;
 }
 
@@ -1076,7 +1361,9 @@ cudaError_t fp8_pass_t(const LaunchCtx& c, int pass, void* out, const uint8_t* a
         p.num_m = static_cast<int>((M + BM - 1) / BM);
         p.num_n = static_cast<int>((N + BN - 1) / BN);
         p.num_kb = static_cast<int>((K + 127) / 128);
-        return launch_pair<2, OUT, false, true>(c, ma, mb, p);
+        CUtensorMap o;
+        if ((e = make_out_map(&o, OUT, out, N, M, N)) != cudaSuccess) return e;
+        return launch_pair<2, OUT, false, true>(c, ma, mb, p, &o);
     }
     if (pass == 1) {         // dx = gq wq^T: A = gq [M,N] K-major, B = wq [K,N] rows k, contraction n
         if ((e = make_map8(&ma, a, N, M, 128)) != cudaSuccess) return e;
@@ -1085,7 +1372,9 @@ cudaError_t fp8_pass_t(const LaunchCtx& c, int pass, void* out, const uint8_t* a
         p.num_m = static_cast<int>((M + BM - 1) / BM);
         p.num_n = static_cast<int>((K + BN - 1) / BN);
         p.num_kb = static_cast<int>((N + 127) / 128);
-        return launch_pair<2, OUT, false, false>(c, ma, mb, p);
+        CUtensorMap o;
+        if ((e = make_out_map(&o, OUT, out, K, M, K)) != cudaSuccess) return e;
+        return launch_pair<2, OUT, false, false>(c, ma, mb, p, &o);
     }
     // dw = xq^T gq: A = xq [M,K] (out k, contraction m), B = gq [M,N] (out n, contraction m);
     // an f32 result in pieces of TC_PIECE_ROWS rows, as for the 16-bit dW
@@ -1108,7 +1397,9 @@ cudaError_t fp8_pass_t(const LaunchCtx& c, int pass, void* out, const uint8_t* a
         p.split_from = static_cast<int>(sp > 1 ? tiles - tiles % DW_WAVE : tiles);
         p.partials = ws;
         const int64_t split_tiles = tiles - p.split_from;
-        if ((e = launch_pair<2, OUT, true, true>(c, ma, mb, p, nullptr, nullptr, p.split_from + split_tiles * sp)) !=
+        CUtensorMap o;
+        if ((e = make_out_map(&o, OUT, out, N, K, N)) != cudaSuccess) return e;
+        if ((e = launch_pair<2, OUT, true, true>(c, ma, mb, p, &o, nullptr, nullptr, p.split_from + split_tiles * sp)) !=
             cudaSuccess)
             return e;
         if (sp > 1 && (e = launch_chunk_sum<OUT>(c, ws, p.split_from, sp, split_tiles, units_m, p.num_n, BN, out,
@@ -1146,8 +1437,8 @@ cudaError_t tc_dx(const LaunchCtx& c, bi_dtype dt, void* dx, const void* dy, con
     return dt == BI_BF16 ? dx_t<1>(c, dt, dx, dy, w, M, K, N) : dx_t<0>(c, dt, dx, dy, w, M, K, N);
 }
 
-int64_t tc_dw_workspace_bytes(int dw_f32, int64_t M, int64_t K, int64_t N) {
-    const DwShape d = dw_shape(K, N);
+int64_t tc_dw_workspace_bytes(const LaunchCtx& c, int dw_f32, int64_t M, int64_t K, int64_t N) {
+    const DwShape d = dw_shape(K, N, forced_cols(c));
     const int64_t len = dw_f32 ? lmin(M, TC_PIECE_ROWS) : M;  // the first (longest) contraction piece
     const int sp = dw_split(d.tiles, (len + BK - 1) / BK);
     return sp > 1 ? (d.tiles % DW_WAVE) * sp * 256 * d.bnt * 4 : 0;
@@ -1155,7 +1446,7 @@ int64_t tc_dw_workspace_bytes(int dw_f32, int64_t M, int64_t K, int64_t N) {
 
 cudaError_t tc_dw(const LaunchCtx& c, bi_dtype dt, void* dw, int dw_f32, const void* x,
                   const void* dy, int64_t M, int64_t K, int64_t N, float* ws) {
-    const bool nw = dw_shape(K, N).bnt == 128;
+    const bool nw = dw_shape(K, N, forced_cols(c)).bnt == 128;
     if (dt == BI_BF16) {
         if (dw_f32) return nw ? dw_t<1, true, 128>(c, dt, dw, x, dy, M, K, N, ws) : dw_t<1, true, 256>(c, dt, dw, x, dy, M, K, N, ws);
         return nw ? dw_t<1, false, 128>(c, dt, dw, x, dy, M, K, N, ws) : dw_t<1, false, 256>(c, dt, dw, x, dy, M, K, N, ws);
@@ -1191,7 +1482,9 @@ cudaError_t tc_tf32x3_pass(const LaunchCtx& c, const float* a_hi, const float* a
         p.num_m = static_cast<int>((rows + BM - 1) / BM);
         p.num_n = static_cast<int>((cols + BN - 1) / BN);
         p.num_kb = static_cast<int>((len + 31) / 32);
-        if ((e = launch_pair<3, 2, false, false>(c, ah, bh, p, &al, &bl)) != cudaSuccess) return e;
+        CUtensorMap o;
+        if ((e = make_out_map(&o, 2, out, cols, rows, ldo)) != cudaSuccess) return e;
+        if ((e = launch_pair<3, 2, false, false>(c, ah, bh, p, &o, &al, &bl)) != cudaSuccess) return e;
     }
     return cudaSuccess;
 }
@@ -1213,11 +1506,16 @@ cudaError_t tc_fp8_pass(const LaunchCtx& c, int pass, bi_dtype out_dt, void* out
     }
 }
 
+int64_t tc_grouped_dw_workspace_bytes(int64_t M, int64_t K, int64_t N, int64_t E) {
+    const GroupedDwSplit sd = grouped_dw_split(M, K, N, E);
+    return sd.sp > 1 ? (sd.units - sd.split_from) * sd.sp * 256 * BN * 4 : 0;
+}
+
 cudaError_t tc_grouped_dw(const LaunchCtx& c, bi_dtype dt, float* dw, const void* dy_sorted, const void* x_sorted,
                           const void* dy_tail, const void* x_tail, int64_t M, int64_t K, int64_t N, int64_t E,
-                          const uint32_t* seg) {
-    return dt == BI_BF16 ? grouped_dw_t<1>(c, dt, dw, dy_sorted, x_sorted, dy_tail, x_tail, M, K, N, E, seg)
-                         : grouped_dw_t<0>(c, dt, dw, dy_sorted, x_sorted, dy_tail, x_tail, M, K, N, E, seg);
+                          const uint32_t* seg, float* ws) {
+    return dt == BI_BF16 ? grouped_dw_t<1>(c, dt, dw, dy_sorted, x_sorted, dy_tail, x_tail, M, K, N, E, seg, ws)
+                         : grouped_dw_t<0>(c, dt, dw, dy_sorted, x_sorted, dy_tail, x_tail, M, K, N, E, seg, ws);
 }
 
 }  // namespace bi

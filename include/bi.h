@@ -288,6 +288,19 @@ int bi_dispatch_tier(int pass, bi_dtype dtype, int tensor_cores, int64_t k, int6
 /* Number of kernels this engine has launched since it was created. */
 uint64_t bi_launch_count(bi_engine engine);
 
+/* Force the column width of the tensor-core tier's output tiles (0 restores
+ * the automatic choice, which depends on the pass, K and N only).  Source:
+ * sgemm-bi 0.1.1.post2, "Determinism contracts" (the tensor-core tier has two
+ * tile families that give bit-identical results).  Here the families are the
+ * widths 256 and 128 for every 16-bit dense and grouped pass, plus 176 and 192
+ * for the grouped forward; a width a pass cannot take is ignored for that
+ * pass.  The width only decides how output elements are grouped into work
+ * units: each element is the same ascending chain of 64-wide contraction blocks
+ * in one f32 accumulator, so every result is bit-identical for every setting
+ * (the tests compare them).  Meant for tests and tuning; cols outside
+ * {0, 128, 176, 192, 256} is BI_ERR_INVALID_ARG. */
+bi_status bi_engine_set_tile_cols(bi_engine engine, int cols);
+
 /* Host-side fault injection for allocation failure (no counterpart on the
  * pages).  The next `count` scratch allocations of this engine fail as if its
  * memory pool were exhausted (count < 0: every allocation until the setting is

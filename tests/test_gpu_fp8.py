@@ -57,6 +57,21 @@ def test_quantize_bit_exact(eng, dtype, scale_inv):
         assert ((want_q & 0x7f) == 0x7e).sum() > 20  # saturation was exercised
 
 
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("offset", [0, 1, 3])  # 16-byte steps, and element by element from a misaligned start
+def test_quantize_vector_and_element_paths_agree(eng, dtype, offset):
+    count = 200003  # many 16-byte steps and a ragged tail
+    x = synth.normal((count + 8,), 2.0, dtype, 81)
+    src = x.cuda()[offset:offset + count]
+    q = torch.empty(count + 16, dtype=torch.uint8, device="cuda")[offset:offset + count]
+    amax = torch.zeros(1, device="cuda")
+    eng.fp8_quantize(q, amax, src, scal(3.0), count, dtype)
+    eng.check()
+    want_q, want_amax = oracle.fp8_quantize(synth.to_np(x)[offset:offset + count], dtype, 3.0)
+    assert np.array_equal(u8(q), want_q)
+    assert out_np(amax)[0] == want_amax
+
+
 def run_fp8(eng, xq, wq, gq, bias, sx, sw, sg, m, k, n, out):
     td = TD[out]
     y = torch.empty(m, n, dtype=td, device="cuda")

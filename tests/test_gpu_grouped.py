@@ -217,7 +217,7 @@ def test_grouped_tc_tile_edges_exact(eng, dtype):
     assert np.array_equal(out_np(DW), oracle.grouped_dweights(xn, dyn, grouped_ids, m, k, n, e, dtype))
 
 
-@pytest.mark.parametrize("e", [64, 300])
+@pytest.mark.parametrize("e", [64, 300, 1500])  # 1500: more buckets than the two-launch grouping takes
 @pytest.mark.parametrize("tc", [0, 1])
 def test_grouped_many_experts_exact(eng, e, tc):
     """Many experts, most of them small and some empty (ids drawn from a skewed
@@ -284,3 +284,39 @@ def test_grouped_long_expert_in_pieces(eng, tc):
                                    dev(dy[torch.from_numpy(order)]), offs, m, k, n, e, "bf16", None, strat)
     eng.check()
     assert np.array_equal(out_np(DW), want)
+
+
+def test_grouped_dweights_last_wave_in_chunks(eng):
+    """Grouped dweights whose last, partial wave of units contracts in chunks
+    added by the dW tree: 4 experts x 2 column tiles = 8 units on 76 CTA pairs,
+    about 31 blocks per expert, so each unit runs as 3 chunks (one expert has no
+    rows, so all of its chunks are empty).  Within tolerance of the oracle on
+    random data, bit-identical over runs, exact on small integers, and equal
+    to the scalar tier on them."""
+    m, k, n, e, dtype = 8000, 264, 136, 4, "bf16"
+    rng = np.random.default_rng(404)
+    ids = rng.integers(0, e, size=m).astype(np.uint32)
+    ids[ids == 1] = 0            # expert 1 gets no rows
+    ids[rng.choice(m, 300, replace=False)] = e  # padding
+    x, w, dy, _ = synth.grouped_inputs(m, k, n, e, dtype)
+    I = torch.from_numpy(ids.astype(np.int64))
+    _, _, dw = run_grouped(eng, x, w, dy, I, m, k, n, e, dtype, tc=1, with_dx=False)
+    for _ in range(2):
+        _, _, dw2 = run_grouped(eng, x, w, dy, I, m, k, n, e, dtype, tc=1, with_dx=False)
+        assert np.array_equal(dw.view(np.uint32), dw2.view(np.uint32))
+    xn, dyn = synth.to_np(x), synth.to_np(dy)
+    x64, dy64 = f64(xn, dtype), f64(dyn, dtype)
+    S = np.zeros((e, n, k))
+    for g in range(e):
+        rows = np.nonzero(ids == g)[0]
+        S[g] = np.abs(dy64[rows]).T @ np.abs(x64[rows])
+    ok, st = check_tc(dw, oracle.grouped_dweights(xn, dyn, ids, m, k, n, e, dtype), S, "f32")
+    assert ok, st
+    assert np.all(dw[1] == 0) and not np.signbit(dw[1]).any()
+    xi = synth.small_ints((m, k), -4, 4, dtype, 405)
+    wi = synth.small_ints((e, n, k), -4, 4, dtype, 406)
+    dyi = synth.small_ints((m, n), -4, 4, dtype, 407)
+    _, _, dwt = run_grouped(eng, xi, wi, dyi, I, m, k, n, e, dtype, tc=1, with_dx=False)
+    _, _, dws = run_grouped(eng, xi, wi, dyi, I, m, k, n, e, dtype, tc=0, with_dx=False)
+    want = oracle.grouped_dweights(synth.to_np(xi), synth.to_np(dyi), ids, m, k, n, e, dtype)
+    assert np.array_equal(dwt, want) and np.array_equal(dws, want)
