@@ -486,7 +486,8 @@ template <int IN, int OUT, bool A_MN, bool B_MN, int MODE, int BNT>
 __global__ void __launch_bounds__(THREADS, 1)
     tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ CUtensorMap tmA2, const __grid_constant__ CUtensorMap tmB2,
-                        const __grid_constant__ CUtensorMap tmO, const Params p) {
+                        const __grid_constant__ CUtensorMap tmO, const __grid_constant__ CUtensorMap tmP,
+                        const Params p) {
     constexpr int ES = IN == 2 ? 1 : (IN == 3 ? 4 : 2);  // operand element size, bytes
     // the tf32 operands are always staged K-major (the split kernel transposes)
     static_assert(IN != 3 || (!A_MN && !B_MN), "3xTF32 takes K-major operands only");
@@ -770,7 +771,38 @@ __global__ void __launch_bounds__(THREADS, 1)
                 }
             };
             const bool to_partials = IN <= 2 && MODE != GROUPED_ROWS && u.part >= 0;
-            if (TMAO && !to_partials && !(MODE == GROUPED_DW && u.npiece > 1)) {
+            if (TMAO && to_partials && u.npiece == 1) {
+                // a chunk unit's raw f32 sum goes to its 256 x BN slot of the
+                // partials through the same staging, a 2-D map over the slots
+                // (tmP, 32 columns per slice)
+                const int rowbase = u.part * 256 + static_cast<int>(crank) * 128 + q * 32;
+                for (int cs = 0; cs < BN; cs += 32) {
+                    if (col0 + cs >= p.cols) break;
+                    if (lane == 0) bulk_wait_read<1>();
+                    __syncwarp();
+                    const uint32_t buf = smem_u32(out_stage) + static_cast<uint32_t>(q * 8192 + (oslot & 1) * 4096);
+                    const uint32_t rowaddr = buf + static_cast<uint32_t>(lane * 128);
+#pragma unroll
+                    for (int c16 = 0; c16 < 32; c16 += 16) {
+                        __syncwarp();
+                        uint32_t v[16];
+                        tmem_ld16(tbase + cs + c16, v);
+#pragma unroll
+                        for (int i = 0; i < 4; ++i)
+                            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(
+                                             rowaddr + static_cast<uint32_t>(((c16 / 4 + i) ^ (lane & 7)) * 16)),
+                                         "r"(v[4 * i]), "r"(v[4 * i + 1]), "r"(v[4 * i + 2]), "r"(v[4 * i + 3])
+                                         : "memory");
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_2d(&tmP, buf, cs, rowbase);
+                        bulk_commit();
+                    }
+                    ++oslot;
+                }
+            } else if (TMAO && !to_partials && !(MODE == GROUPED_DW && u.npiece > 1)) {
                 // TMA-store epilogue: this warp's 32 rows go out in slices of 128
                 // bytes per row, staged in shared memory with the 128-byte swizzle
                 // (16-byte chunk c of row r at chunk c ^ (r % 8)), two slices in
@@ -1047,10 +1079,12 @@ cudaError_t make_out_map(CUtensorMap* m, int out_fmt, const void* ptr, uint64_t 
 // known only on the device); -1 = the dense count.
 // o: the output's tensor map for the TMA-store epilogue (every mode but the
 // grouped rows, which pass null).
+// pm: a map over the chunk partials (2-D [slots x 256][BN] f32) when the
+// launch has chunk units.
 template <int IN, int OUT, bool A_MN, bool B_MN, int MODE = DENSE, int BNT = BN>
 cudaError_t launch_pair(const LaunchCtx& c, const CUtensorMap& a, const CUtensorMap& b, Params p,
                         const CUtensorMap* o, const CUtensorMap* a2 = nullptr, const CUtensorMap* b2 = nullptr,
-                        int64_t units = -1) {
+                        int64_t units = -1, const CUtensorMap* pm = nullptr) {
     auto kern = tc_gemm_pair_kernel<IN, OUT, A_MN, B_MN, MODE, BNT>;
     constexpr int P_SMEM_BYTES = p_smem_bytes(IN, BNT, MODE != GROUPED_ROWS);
     if (MODE != GROUPED_ROWS && o == nullptr) return cudaErrorInvalidValue;
@@ -1090,7 +1124,8 @@ cudaError_t launch_pair(const LaunchCtx& c, const CUtensorMap& a, const CUtensor
     la[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = la;
     cfg.numAttrs = 2;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, a, b, a2 ? *a2 : a, b2 ? *b2 : b, o ? *o : a, p);
+    if (p.split_s > 1 && pm == nullptr) return cudaErrorInvalidValue;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, a, b, a2 ? *a2 : a, b2 ? *b2 : b, o ? *o : a, pm ? *pm : a, p);
     if (e != cudaSuccess) return e;
     c.count();
     return cudaGetLastError();
@@ -1218,10 +1253,12 @@ cudaError_t dw_t(const LaunchCtx& c, bi_dtype dt, void* dw, const void* x, const
         p.split_from = static_cast<int>(sp > 1 ? tiles - tiles % DW_WAVE : tiles);
         p.partials = ws;
         const int64_t split_tiles = tiles - p.split_from;
-        CUtensorMap o;
+        CUtensorMap o, pmap;
         if ((e = make_out_map(&o, F32 ? 2 : FMT, dw, N, K, N)) != cudaSuccess) return e;
+        if (sp > 1 && (e = make_out_map(&pmap, 2, ws, BNT, split_tiles * sp * 256, BNT)) != cudaSuccess) return e;
         if ((e = launch_pair<FMT, F32 ? 2 : FMT, true, true, DENSE, BNT>(c, a, b, p, &o, nullptr, nullptr,
-                                                                          p.split_from + split_tiles * sp)) !=
+                                                                          p.split_from + split_tiles * sp,
+                                                                          sp > 1 ? &pmap : nullptr)) !=
             cudaSuccess)
             return e;
         if (sp > 1 && (e = launch_chunk_sum<F32 ? 2 : FMT>(c, ws, p.split_from, sp, split_tiles, units_m, p.num_n, BNT,
@@ -1322,9 +1359,11 @@ cudaError_t grouped_dw_t(const LaunchCtx& c, bi_dtype dt, float* dw, const void*
     // one launch: each unit walks its expert's rows (or its chunk of them) in
     // pieces of TC_PIECE_ROWS rows counted from the expert's first row, adding
     // the pieces' results in order
-    CUtensorMap o;  // dW [E][N][K]
+    CUtensorMap o, pmap;  // dW [E][N][K]; the chunk partials
     if ((e = make_out_map(&o, 2, dw, K, N, K, E, true)) != cudaSuccess) return e;
-    if ((e = launch_pair<FMT, 2, true, true, GROUPED_DW>(c, a, b, p, &o, &a2, &b2, launch_units)) != cudaSuccess)
+    if (sd.sp > 1 && (e = make_out_map(&pmap, 2, ws, BN, split_units * sd.sp * 256, BN)) != cudaSuccess) return e;
+    if ((e = launch_pair<FMT, 2, true, true, GROUPED_DW>(c, a, b, p, &o, &a2, &b2, launch_units,
+                                                         sd.sp > 1 ? &pmap : nullptr)) != cudaSuccess)
         return e;
     if (sd.sp > 1)
         return launch_chunk_sum<2>(c, ws, p.split_from, sd.sp, split_units, (p.num_m + 1) / 2, p.num_n, BN, dw, p.ldo,
@@ -1397,9 +1436,11 @@ cudaError_t fp8_pass_t(const LaunchCtx& c, int pass, void* out, const uint8_t* a
         p.split_from = static_cast<int>(sp > 1 ? tiles - tiles % DW_WAVE : tiles);
         p.partials = ws;
         const int64_t split_tiles = tiles - p.split_from;
-        CUtensorMap o;
+        CUtensorMap o, pmap;
         if ((e = make_out_map(&o, OUT, out, N, K, N)) != cudaSuccess) return e;
-        if ((e = launch_pair<2, OUT, true, true>(c, ma, mb, p, &o, nullptr, nullptr, p.split_from + split_tiles * sp)) !=
+        if (sp > 1 && (e = make_out_map(&pmap, 2, ws, BN, split_tiles * sp * 256, BN)) != cudaSuccess) return e;
+        if ((e = launch_pair<2, OUT, true, true>(c, ma, mb, p, &o, nullptr, nullptr, p.split_from + split_tiles * sp,
+                                                 sp > 1 ? &pmap : nullptr)) !=
             cudaSuccess)
             return e;
         if (sp > 1 && (e = launch_chunk_sum<OUT>(c, ws, p.split_from, sp, split_tiles, units_m, p.num_n, BN, out,
