@@ -53,6 +53,8 @@ def parse():
     ap.add_argument("--no-secondary", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--only", default=None, help="restrict the step to one projection (profiling case)")
+    ap.add_argument("--profile-case", default=None, choices=["grouped", "f16-edge"],
+                    help="run one secondary workload's calls four times and exit (a case for profilers)")
     ap.add_argument("--oracle-sample", default=f"{SAMPLE_ROWS},{SAMPLE_COLS}",
                     help="rows,cols of the oracle's sample per projection (smaller for host-only checks)")
     return ap.parse_args()
@@ -630,6 +632,45 @@ def secondary(eng, stream, cpu=True, reps=5):
     return out
 
 
+def profile_case(name, reps=4):
+    """The calls one secondary figure times, `reps` times each, on cuda:0."""
+    import torch
+    import numpy as np
+    import deterministic_invariant_gemm_fixed_gb300 as bi
+    from deterministic_invariant_gemm_fixed_gb300 import synth
+    eng = bi.Engine(0)
+    stream = torch.cuda.current_stream()
+    if name == "grouped":
+        c = synth.GROUPED
+        m, k, n, e = c["m"], c["k"], c["n"], c["e"]
+        x, w, dy, ids = synth.grouped_inputs(m, k, n, e, "bf16", pad_frac=c["pad_frac"])
+        X, W, DY = x.cuda(), w.cuda(), dy.cuda()
+        I = torch.from_numpy(synth.to_np(ids).astype(np.int32)).cuda()
+        Y = torch.empty(m, n, dtype=torch.bfloat16, device="cuda")
+        DX = torch.empty(m, k, dtype=torch.bfloat16, device="cuda")
+        DW = torch.empty(e, n, k, dtype=torch.float32, device="cuda")
+        for _ in range(reps):
+            eng.grouped_forward(Y, X, W, I, m, k, n, e, "bf16", stream, 1)
+            eng.grouped_backward(DX, DW, X, W, DY, I, m, k, n, e, "bf16", stream, 1)
+    else:  # the f16 edge shapes: N = 48 on the scalar tier, the ragged 1000^3 and the GEMV
+        for nm, m, k, n in synth.F16_EDGE:
+            x, w, dy, b = synth.dense_inputs(m, k, n, "f16", x=("uniform", 1.0), w=("uniform", 1.0),
+                                             dy=("uniform", 1.0), b=("uniform", 1.0))
+            X, W, DY, B = x.cuda(), w.cuda(), dy.cuda(), b.cuda()
+            Y = torch.empty(m, n, dtype=torch.float16, device="cuda")
+            DX = torch.empty(m, k, dtype=torch.float16, device="cuda")
+            DW = torch.empty(k, n, dtype=torch.float32, device="cuda")
+            for tc in ((0,) if n < 64 else ((1, 0) if m == 1 else (1,))):
+                for _ in range(reps):
+                    eng.forward(Y, X, W, B, m, k, n, "f16", stream, tc)
+                    if m > 1:
+                        eng.backward_dx(DX, DY, W, m, k, n, "f16", stream, tc)
+                        eng.backward_dw(DW, 1, X, DY, m, k, n, "f16", stream, tc)
+    torch.cuda.synchronize()
+    eng.check(stream)
+    eng.close()
+
+
 # ---------------------------------------------------------------- arms
 
 def reference_arm(args, rank, world):
@@ -742,8 +783,7 @@ def our_arm(args, rank, world):
     # The host link's floor for one step: every input copied in and every
     # result copied out, both directions at once, nothing else running; taken
     # with 1, 2 and 4 copy streams per direction (each tensor split into that
-    # many contiguous chunks, one cudaMemcpyAsync each); the best split is the
-    # one the end-to-end step uses.
+    # many contiguous chunks, one cudaMemcpyAsync each), the fastest reported.
     def chunk_copy(dst, src_t, streams):
         d, s = dst.view(-1), src_t.view(-1)
         per = (d.numel() + len(streams) - 1) // len(streams)
@@ -771,56 +811,56 @@ def our_arm(args, rank, world):
         return best
 
     floors = {nsd: copy_floor(nsd) for nsd in (1, 2, 4)}
-    nsd = min(floors, key=floors.get)
-    floor_s = floors[nsd]
+    floor_s = min(floors.values())
 
-    # Copies run on their own streams and overlap the compute of other passes:
-    # the forward of projection i waits for its X and W, dX for its dY, dW for
-    # both; each result is copied out as soon as its pass ends; a pass waits for
-    # the copy-out of its output from the previous step, and the copy-in of an
-    # input waits for the last pass of the previous step that reads it.
-    s_in = [torch.cuda.Stream() for _ in range(nsd)]
-    s_out = [torch.cuda.Stream() for _ in range(nsd)]
+    # Copies run on their own streams (one per direction: the floor above is
+    # lowest that way) and overlap the compute of other passes: the forward of
+    # projection i waits for its X and W, dX for its dY, dW for both; each result
+    # is copied out as soon as its pass ends; a pass waits for the copy-out of
+    # its output from the previous step, and the copy-in of an input waits for
+    # the last pass of the previous step that reads it.  The events are made
+    # once and recorded again every step (a wait refers to the latest record),
+    # so the host enqueues a step in well under its GPU time.
+    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
     nb = len(bufs)
-    ev = {}
-
-    def record(key, streams):
-        evs = []
-        for st in streams:
-            e = torch.cuda.Event()
-            e.record(st)
-            evs.append(e)
-        ev[key] = evs
-
-    def wait(streams, key):
-        for e in ev.get(key, []):
-            for st in streams:
-                st.wait_event(e)
+    ev = {(key, i): torch.cuda.Event() for i in range(nb)
+          for key in ("in_xw", "in_dy", "y", "dx", "dw", "out_y", "out_dx", "out_dw")}
+    started = {"first": True}
 
     def e2e_step():
+        first = started["first"]
+        with torch.cuda.stream(s_in):
+            for i, b in enumerate(bufs):
+                if not first:
+                    s_in.wait_event(ev[("dw", i)])  # X, W, dY are read up to this projection's dW
+                b["x"].copy_(b["x_p"], non_blocking=True)
+                b["w"].copy_(b["w_p"], non_blocking=True)
+                ev[("in_xw", i)].record(s_in)
+                b["dy"].copy_(b["dy_p"], non_blocking=True)
+                ev[("in_dy", i)].record(s_in)
         for i, b in enumerate(bufs):
             k, n = b["k"], b["n"]
-            wait(s_in, ("dw", i))  # X, W, dY are read up to this projection's dW
-            chunk_copy(b["x"], b["x_p"], s_in)
-            chunk_copy(b["w"], b["w_p"], s_in)
-            record(("in_xw", i), s_in)
-            chunk_copy(b["dy"], b["dy_p"], s_in)
-            record(("in_dy", i), s_in)
-        for i, b in enumerate(bufs):
-            k, n = b["k"], b["n"]
-            wait([stream], ("in_xw", i)); wait([stream], ("out_y", i))
+            stream.wait_event(ev[("in_xw", i)])
+            if not first:
+                stream.wait_event(ev[("out_y", i)])
             eng.forward(b["y"], b["x"], b["w"], None, m, k, n, "bf16", stream, 1)
-            record(("y", i), [stream])
-            wait([stream], ("in_dy", i)); wait([stream], ("out_dx", i))
+            ev[("y", i)].record(stream)
+            stream.wait_event(ev[("in_dy", i)])
+            if not first:
+                stream.wait_event(ev[("out_dx", i)])
             eng.backward_dx(b["dx"], b["dy"], b["w"], m, k, n, "bf16", stream, 1)
-            record(("dx", i), [stream])
-            wait([stream], ("out_dw", i))
+            ev[("dx", i)].record(stream)
+            if not first:
+                stream.wait_event(ev[("out_dw", i)])
             eng.backward_dw(b["dw"], 1, b["x"], b["dy"], m, k, n, "bf16", stream, 1)
-            record(("dw", i), [stream])
-            for nm, key in (("y", "y"), ("dx", "dx"), ("dw", "dw")):
-                wait(s_out, (key, i))
-                chunk_copy(b[nm + "_p"], b[nm], s_out)
-                record(("out_" + key, i), s_out)
+            ev[("dw", i)].record(stream)
+        with torch.cuda.stream(s_out):
+            for i, b in enumerate(bufs):
+                for nm in ("y", "dx", "dw"):
+                    s_out.wait_event(ev[(nm, i)])
+                    b[nm + "_p"].copy_(b[nm], non_blocking=True)
+                    ev[("out_" + nm, i)].record(s_out)
+        started["first"] = False
 
     e2e_steps = max(3, min(10, args.steps))
     e2e_step()
@@ -828,11 +868,11 @@ def our_arm(args, rank, world):
     barrier()
     s0 = torch.cuda.Event(enable_timing=True); s1 = torch.cuda.Event(enable_timing=True)
     s0.record(stream)
-    for st in s_in + s_out:
+    for st in (s_in, s_out):
         st.wait_event(s0)
     for _ in range(e2e_steps):
         e2e_step()
-    for st in s_in + s_out:
+    for st in (s_in, s_out):
         e = torch.cuda.Event()
         e.record(st)
         stream.wait_event(e)
@@ -881,7 +921,7 @@ def our_arm(args, rank, world):
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "steps": e2e_steps, "ms_per_step": e2e_t / e2e_steps * 1e3,
-                    "copy_floor_ms": floor_s * 1e3, "copy_streams_per_direction": nsd,
+                    "copy_floor_ms": floor_s * 1e3, "copy_streams_per_direction": 1,
                     "copy_floor_ms_by_streams": {str(kk): vv * 1e3 for kk, vv in floors.items()},
                     "frac_of_copy_floor": floor_s / (e2e_t / e2e_steps)},
             "gpu_launches": launches,
@@ -900,7 +940,9 @@ def main():
     ONLY = args.only
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
-    if args.impl == "reference":
+    if args.profile_case:
+        profile_case(args.profile_case)
+    elif args.impl == "reference":
         reference_arm(args, rank, world)
     else:
         our_arm(args, rank, world)

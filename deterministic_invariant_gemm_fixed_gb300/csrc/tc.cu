@@ -6,9 +6,9 @@
 // (pass, dtype, K, N):
 //   - every pass, dense and grouped, runs tcgen05.mma.cta_group::2 M256 x N256
 //     on a CTA pair (tc_gemm_pair_kernel; K16 per instruction for bf16/f16),
-//     except a 16-bit dW whose K x N output has few 256 x 256 tiles, which runs
-//     M256 x N128 (chosen from K and N alone); f32 accumulators live in tensor
-//     memory;
+//     except a 16-bit dW whose 256-column tiling gives few work units, which
+//     runs M256 x N128 (the tile width never enters an element's chain); f32
+//     accumulators live in tensor memory;
 //   - the contracted index is walked in 64-wide blocks in ascending order, four
 //     K16 instructions per block, accumulating into the same TMEM tile;
 //   - Y and dX never split their contraction; no atomics, no stream-K;
@@ -1191,16 +1191,17 @@ cudaError_t dx_t(const LaunchCtx& c, bi_dtype dt, void* dx, const void* dy, cons
                                          : dx_impl<FMT, 256>(c, dt, dx, dy, w, M, K, N);
 }
 
-// Tile width of the 16-bit dW, a function of K and N only: 128 columns when
-// the K x N output has fewer 256 x 256 tiles than a 152-SM GPU has CTA pairs,
-// so that more pairs share a small weight gradient.  (A 128-column stage is
-// consumed in half the time of a 256-column one, and the deepest ring that
-// fits does not cover the load latency; with work for every pair the wider
-// tile is faster, so Y and dX, whose tile counts grow with M, keep it.)  The
-// tile width does not enter the accumulation order: every output element is
-// the same ascending chain of 64-wide contraction blocks.
-constexpr int64_t DW_FEW_TILES = 76;
-bool narrow_dw(int64_t K, int64_t N) { return ((K + 255) / 256) * ((N + 255) / 256) < DW_FEW_TILES; }
+// Tile width of the 16-bit dW.  dW's output does not grow with the batch and
+// the tile width does not enter the accumulation order (every output element
+// is the same ascending chain of 64-wide contraction blocks, and the chunk
+// split below is the same tree for either width), so the width may follow M,
+// K and N: 256-column tiles, whose last partial wave runs in chunks, unless
+// that gives fewer units than three quarters of a 152-SM GPU's 76 CTA pairs,
+// in which case the 128-column tile (twice the tiles) keeps more pairs busy.
+// Measured: GPT-2 up-projection dW (3 x 12 tiles of 256, 2 chunks each: 72
+// units) 25.0 us with 256 columns against 27.0 with 128; the ragged 1000^3
+// (16 tiles, 2 chunks: 32 units) 14.6 against 13.0.
+constexpr int64_t DW_BUSY_UNITS = 57;
 // dW's output tiles do not depend on M, and its contraction is the batch: the
 // tiles of the last, partial wave (on a 152-SM GPU's 76 CTA pairs) run their
 // contraction as s chunks of consecutive 64-row blocks, s pairs per tile, and
@@ -1219,9 +1220,15 @@ struct DwShape {
     int bnt;        // tile columns
     int64_t tiles;  // output tiles of K x N
 };
-DwShape dw_shape(int64_t K, int64_t N, int forced = 0) {
-    const int bnt = forced == 128 || forced == 256 ? forced : (narrow_dw(K, N) ? 128 : 256);
-    return {bnt, ((K + BM - 1) / BM + 1) / 2 * ((N + bnt - 1) / bnt)};
+int64_t dw_tiles(int64_t K, int64_t N, int bnt) { return ((K + BM - 1) / BM + 1) / 2 * ((N + bnt - 1) / bnt); }
+// len: rows of the first (longest) contraction piece
+DwShape dw_shape(int64_t K, int64_t N, int64_t len, int forced = 0) {
+    int bnt = forced;
+    if (bnt != 128 && bnt != 256) {
+        const int64_t t256 = dw_tiles(K, N, 256);
+        bnt = t256 * dw_split(t256, (len + BK - 1) / BK) >= DW_BUSY_UNITS ? 256 : 128;
+    }
+    return {bnt, dw_tiles(K, N, bnt)};
 }
 int forced_cols(const LaunchCtx& c) { return c.eng ? c.eng->tile_cols : 0; }
 
@@ -1479,15 +1486,15 @@ cudaError_t tc_dx(const LaunchCtx& c, bi_dtype dt, void* dx, const void* dy, con
 }
 
 int64_t tc_dw_workspace_bytes(const LaunchCtx& c, int dw_f32, int64_t M, int64_t K, int64_t N) {
-    const DwShape d = dw_shape(K, N, forced_cols(c));
     const int64_t len = dw_f32 ? lmin(M, TC_PIECE_ROWS) : M;  // the first (longest) contraction piece
+    const DwShape d = dw_shape(K, N, len, forced_cols(c));
     const int sp = dw_split(d.tiles, (len + BK - 1) / BK);
     return sp > 1 ? (d.tiles % DW_WAVE) * sp * 256 * d.bnt * 4 : 0;
 }
 
 cudaError_t tc_dw(const LaunchCtx& c, bi_dtype dt, void* dw, int dw_f32, const void* x,
                   const void* dy, int64_t M, int64_t K, int64_t N, float* ws) {
-    const bool nw = dw_shape(K, N, forced_cols(c)).bnt == 128;
+    const bool nw = dw_shape(K, N, dw_f32 ? lmin(M, TC_PIECE_ROWS) : M, forced_cols(c)).bnt == 128;
     if (dt == BI_BF16) {
         if (dw_f32) return nw ? dw_t<1, true, 128>(c, dt, dw, x, dy, M, K, N, ws) : dw_t<1, true, 256>(c, dt, dw, x, dy, M, K, N, ws);
         return nw ? dw_t<1, false, 128>(c, dt, dw, x, dy, M, K, N, ws) : dw_t<1, false, 256>(c, dt, dw, x, dy, M, K, N, ws);

@@ -7,7 +7,8 @@ the output-tile widths of the CTA-pair kernel (256 and 128 columns for every
 bi_engine_set_tile_cols forces one).  A tile's width only decides which outputs
 share a work unit; each output is the same ascending chain of 64-wide
 contraction blocks, so Y, dX and dW must be equal for every width, including
-the automatic choice (256 columns, or 128 for a 16-bit dW with few output tiles).
+the automatic choice (256 columns, or 128 for a 16-bit dW whose 256-column
+tiling gives few work units).
 """
 import numpy as np
 import pytest
