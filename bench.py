@@ -53,7 +53,7 @@ def parse():
     ap.add_argument("--no-secondary", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--only", default=None, help="restrict the step to one projection (profiling case)")
-    ap.add_argument("--profile-case", default=None, choices=["grouped", "f16-edge"],
+    ap.add_argument("--profile-case", default=None, choices=["grouped", "f16-edge", "gpt2"],
                     help="run one secondary workload's calls four times and exit (a case for profilers)")
     ap.add_argument("--oracle-sample", default=f"{SAMPLE_ROWS},{SAMPLE_COLS}",
                     help="rows,cols of the oracle's sample per projection (smaller for host-only checks)")
@@ -652,6 +652,18 @@ def profile_case(name, reps=4):
         for _ in range(reps):
             eng.grouped_forward(Y, X, W, I, m, k, n, e, "bf16", stream, 1)
             eng.grouped_backward(DX, DW, X, W, DY, I, m, k, n, e, "bf16", stream, 1)
+    elif name == "gpt2":  # the GPT-2-small MLP up-projection on the tensor-core tier
+        g = synth.GPT2_UP
+        m, k, n = g["m"], g["k"], g["n"]
+        x, w, dy, b = synth.dense_inputs(m, k, n, "bf16", x=g["x"], w=g["w"], dy=g["dy"], b=g["b"])
+        X, W, DY, B = x.cuda(), w.cuda(), dy.cuda(), b.cuda()
+        Y = torch.empty(m, n, dtype=torch.bfloat16, device="cuda")
+        DX = torch.empty(m, k, dtype=torch.bfloat16, device="cuda")
+        DW = torch.empty(k, n, dtype=torch.float32, device="cuda")
+        for _ in range(reps):
+            eng.forward(Y, X, W, B, m, k, n, "bf16", stream, 1)
+            eng.backward_dx(DX, DY, W, m, k, n, "bf16", stream, 1)
+            eng.backward_dw(DW, 1, X, DY, m, k, n, "bf16", stream, 1)
     else:  # the f16 edge shapes: N = 48 on the scalar tier, the ragged 1000^3 and the GEMV
         for nm, m, k, n in synth.F16_EDGE:
             x, w, dy, b = synth.dense_inputs(m, k, n, "f16", x=("uniform", 1.0), w=("uniform", 1.0),

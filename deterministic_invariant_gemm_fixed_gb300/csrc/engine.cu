@@ -324,7 +324,6 @@ bi_status bi_backward_dw(bi_engine eng, void* dw, int dw_f32, const void* x, con
     if (!dw) return fail(eng, BI_ERR_INVALID_ARG, "dw must not be NULL");
     if (m > 0 && (!x || !dy)) return fail(eng, BI_ERR_INVALID_ARG, "x and dy must not be NULL");
     const int64_t J = (m + BI_DW_CHUNK - 1) / BI_DW_CHUNK;
-    if (J > 65535) return fail(eng, BI_ERR_UNSUPPORTED, "m is limited to 65535 * 256 rows for dW");
     const int out_f32 = dw_f32 || dtype == BI_F32;
     const int tier = bi_dispatch_tier(BI_PASS_DW, dtype, tensor_cores, k, n);
     if (tier && m > 0 && (!aligned16(dw) || !aligned16(x) || !aligned16(dy)))
@@ -358,7 +357,6 @@ bi_status bi_bias_grad(bi_engine eng, void* db, int db_f32, const void* dy, int6
     if (!db) return fail(eng, BI_ERR_INVALID_ARG, "db must not be NULL");
     if (m > 0 && !dy) return fail(eng, BI_ERR_INVALID_ARG, "dy must not be NULL");
     const int64_t J = (m + BI_DW_CHUNK - 1) / BI_DW_CHUNK;
-    if (J > 65535) return fail(eng, BI_ERR_UNSUPPORTED, "m is limited to 65535 * 256 rows");
     const int out_f32 = db_f32 || dtype == BI_F32;
     DeviceGuard g(eng->device);
     if (!g.ok) return fail(eng, BI_ERR_CUDA, "cudaSetDevice failed");
