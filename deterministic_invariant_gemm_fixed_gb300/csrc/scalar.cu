@@ -930,9 +930,10 @@ __global__ void __launch_bounds__(32) scalar_rows_gemv_kernel(const RowsArgs p) 
     extern __shared__ __align__(16) uint8_t smem_gv[];
     Stage* ring = reinterpret_cast<Stage*>(smem_gv);
     const int lane = threadIdx.x;
-    const T* A = static_cast<const T*>(p.a);
-    const T* B = static_cast<const T*>(p.b);
-    const int64_t R = p.R, L = p.L, C = p.C;
+    const T* __restrict__ A = static_cast<const T*>(p.a);
+    const T* __restrict__ B = static_cast<const T*>(p.b);
+    const int64_t R = p.R, C = p.C;
+    const int L = static_cast<int>(p.L);  // a contraction is at most 8388480 long
     const int64_t c0 = static_cast<int64_t>(blockIdx.x) * 32;
     constexpr int U = 16 / sizeof(T);               // elements per 16-byte unit
     // B units of one stage: [step][32 columns] = 64 rows of 32/U units, or
@@ -943,11 +944,11 @@ __global__ void __launch_bounds__(32) scalar_rows_gemv_kernel(const RowsArgs p) 
     static_assert(B_UPR * B_ROWS % 32 == 0, "whole passes of the warp");
     constexpr int A_UPR = GV_STEPS / U;
     constexpr int A_PER = (RR * A_UPR + 31) / 32;
-    const int64_t nkb = (L + GV_STEPS - 1) / GV_STEPS;
+    const int nkb = (L + GV_STEPS - 1) / GV_STEPS;
     // Each lane's units keep their place in every stage: source pointers that
     // advance one block per issued stage, and the step bound of each unit.
     const T* bsrc[B_PER];
-    int64_t blim[B_PER];
+    int blim[B_PER];
 #pragma unroll
     for (int i = 0; i < B_PER; ++i) {
         const int u = lane + 32 * i, row = u / B_UPR, seg = (u % B_UPR) * U;
@@ -962,7 +963,7 @@ __global__ void __launch_bounds__(32) scalar_rows_gemv_kernel(const RowsArgs p) 
         }
     }
     const T* asrc[A_PER];
-    int64_t alim[A_PER];
+    int alim[A_PER];
 #pragma unroll
     for (int i = 0; i < A_PER; ++i) {
         const int u = lane + 32 * i, r = u / A_UPR, seg = (u % A_UPR) * U;
@@ -971,7 +972,7 @@ __global__ void __launch_bounds__(32) scalar_rows_gemv_kernel(const RowsArgs p) 
         alim[i] = ok ? L - seg : 0;
     }
     const int64_t bstep = BT ? GV_STEPS : GV_STEPS * C;
-    int64_t l_issue = 0;
+    int l_issue = 0;
     int slot_issue = 0;
     auto issue = [&]() {
         Stage& st = ring[slot_issue];
@@ -998,7 +999,7 @@ __global__ void __launch_bounds__(32) scalar_rows_gemv_kernel(const RowsArgs p) 
         l_issue += GV_STEPS;
         slot_issue = slot_issue + 1 == GV_STAGES ? 0 : slot_issue + 1;
     };
-    for (int64_t kb = 0; kb < GV_STAGES - 1; ++kb) {
+    for (int kb = 0; kb < GV_STAGES - 1; ++kb) {
         if (kb < nkb) issue();
         cp_async_commit();
     }
@@ -1006,7 +1007,7 @@ __global__ void __launch_bounds__(32) scalar_rows_gemv_kernel(const RowsArgs p) 
 #pragma unroll
     for (int r = 0; r < RR; ++r) acc[r] = 0.0f;
     int slot = 0;
-    for (int64_t kb = 0; kb < nkb; ++kb) {
+    for (int kb = 0; kb < nkb; ++kb) {
         cp_async_wait<GV_STAGES - 2>();
         __syncwarp();  // block kb has landed for every lane; block kb - 1 is no longer read
         if (kb + GV_STAGES - 1 < nkb) issue();
