@@ -67,6 +67,8 @@
  * - Every tensor is dense, row-major, contiguous, on the engine's device, and
  *   owned by the caller.  Pointers are device pointers.  bf16/f16 data are
  *   the IEEE encodings; f32 is binary32.
+ * - No output of a call may overlap any of its inputs: the kernels read the
+ *   inputs through the read-only data path while they write the outputs.
  * - `stream` is a cudaStream_t (NULL = the legacy default stream).  Calls only
  *   enqueue work; none of them synchronises with the host.
  * - Calls return a status and never throw or abort.  Arguments are checked on
