@@ -354,6 +354,31 @@ def test_k1_is_one_rounded_product():
     assert np.array_equal(y.view(np.uint32), ref.astype(np.float32).view(np.uint32))
 
 
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_chains_keep_a_negative_zero(dtype):
+    """Signed zeros through the chain.  Every product -1e-30 * 1e-20 lies far
+    below the smallest f32 subnormal, so round to nearest gives -0 for the
+    first fused multiply-add, RN(-1e-50 + +0) = -0, and for every later one,
+    RN(-1e-50 + -0) = -0: each output of Y, dX and dW (every chunk and every
+    tree sum, -0 + -0 = -0) is -0.  A product that is an exact zero instead
+    gives RN(-0 + +0) = +0, so the all-zero contraction is +0."""
+    m, k, n = 5, 37, 6  # dW over 5 rows; also a dW tree over chunks of 2 rows
+    neg, pos = enc([-1e-30], dtype)[0], enc([1e-20], dtype)[0]
+    x = np.full(m * k, neg, dtype=neg.dtype)
+    w = np.full(k * n, pos, dtype=pos.dtype)
+    dy_dx = np.full(m * n, neg, dtype=neg.dtype)
+    dy_dw = np.full(m * n, enc([1e-30], dtype)[0], dtype=neg.dtype)
+    outs = [oracle.forward(x, w, None, m, k, n, dtype, out_f32=True),
+            oracle.backward_dx(dy_dx, w, m, k, n, dtype, out_f32=True),
+            oracle.backward_dw(x, dy_dw, m, k, n, dtype, dw_f32=True),
+            oracle.backward_dw(x, dy_dw, m, k, n, dtype, dw_f32=True, chunk=2)]
+    for o in outs:
+        assert np.all(o == 0) and np.all(np.signbit(o))
+    zx = np.full(m * k, enc([-0.0], dtype)[0], dtype=neg.dtype)  # -0 * w: exact zero products
+    y0 = oracle.forward(zx, w, None, m, k, n, dtype, out_f32=True)
+    assert np.all(y0 == 0) and not np.any(np.signbit(y0))
+
+
 @pytest.mark.parametrize("dtype", DT)
 def test_dw_large_chunk_is_plain_chain(dtype):
     m, k, n = 40, 24, 31
