@@ -1382,7 +1382,7 @@ cudaError_t rows_gemv_t(const LaunchCtx& c, const RowsArgs& a, int bt) {
 
 // The narrow kernels take an output when it is at most 64 columns wide, or when
 // it is small: the 128-column tiles would give fewer CTAs than the GPU has SMs
-// while the 16 x 64 tiles give more, and its column tiles fit a grid dimension.
+// while the 32 x 32 tiles give more, and its column tiles fit a grid dimension.
 // (Any tiling gives every output the same chain.)
 constexpr int64_t NARROW_COLS = 64;  // outputs this wide or less always take the narrow kernels
 bool narrow_rows(const LaunchCtx& c, int64_t R, int64_t C) {
