@@ -502,22 +502,24 @@ struct NarrowRaw {  // rows kernel: A [32 rows][64 steps]; B [64 steps][32 cols]
 // are loaded first, then their 32 paired FMAs run (step order kept within each
 // accumulator), so one shared-memory latency covers 8 steps.
 __device__ __forceinline__ void narrow_block(const NarrowSmem& sm, int buf, int lane, int w, uint64_t (&acc)[4]) {
-#pragma unroll 1
+    const float2 (*a)[NW_TM] = sm.a[buf];
+    const float (*b)[NW_TN + 4] = sm.b[buf];
+#pragma unroll
     for (int l0 = 0; l0 < NW_TK; l0 += 8) {
-        uint64_t a[8];
+        uint64_t av[8];
         ulonglong2 b0[8], b1[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-            a[i] = *reinterpret_cast<const uint64_t*>(&sm.a[buf][l0 + i][lane]);
-            b0[i] = *reinterpret_cast<const ulonglong2*>(&sm.b[buf][l0 + i][8 * w]);
-            b1[i] = *reinterpret_cast<const ulonglong2*>(&sm.b[buf][l0 + i][8 * w + 4]);
+            av[i] = *reinterpret_cast<const uint64_t*>(&a[l0 + i][lane]);
+            b0[i] = *reinterpret_cast<const ulonglong2*>(&b[l0 + i][8 * w]);
+            b1[i] = *reinterpret_cast<const ulonglong2*>(&b[l0 + i][8 * w + 4]);
         }
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-            fma2(acc[0], a[i], b0[i].x);
-            fma2(acc[1], a[i], b0[i].y);
-            fma2(acc[2], a[i], b1[i].x);
-            fma2(acc[3], a[i], b1[i].y);
+            fma2(acc[0], av[i], b0[i].x);
+            fma2(acc[1], av[i], b0[i].y);
+            fma2(acc[2], av[i], b1[i].x);
+            fma2(acc[3], av[i], b1[i].y);
         }
     }
 }
