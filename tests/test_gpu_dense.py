@@ -341,6 +341,39 @@ def test_m_zero(eng):
         assert torch.all(dw == 0) and not torch.any(torch.signbit(dw))
 
 
+DEGENERATE = [(1, 1, 1), (1, 1, 7), (3, 1, 5), (5, 7, 1), (300, 1, 200), (300, 200, 1), (1, 4096, 1),
+              (2, 5, 3), (70, 3, 130), (4, 24, 1000)]
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16", "f16"])
+def test_degenerate_shapes_bit_exact(eng, dtype):
+    """Dimensions of 1 and a few: one-step chains (K = 1 forward, N = 1 dX,
+    M = 1 dW), one-column and one-row outputs, through the matrix-vector,
+    narrow and tiled kernels, bit-exact with the oracle."""
+    for m, k, n in DEGENERATE:
+        x, w, dy, b = synth.dense_inputs(m, k, n, dtype, w=("normal", 1.0))
+        got = run_dense(eng, x, w, dy, b, m, k, n, dtype, tc=0)
+        xn, wn, dyn, bn = np_in(x, w, dy, b)
+        assert np.array_equal(got["y"], oracle.forward(xn, wn, bn, m, k, n, dtype)), (m, k, n)
+        assert np.array_equal(got["dx"], oracle.backward_dx(dyn, wn, m, k, n, dtype)), (m, k, n)
+        assert np.array_equal(got["dw"], oracle.backward_dw(xn, dyn, m, k, n, dtype, dw_f32=True)), (m, k, n)
+
+
+def test_m_zero_dx_and_bias_grad(eng):
+    """M = 0: dX (no rows) writes nothing; the bias gradient is +0."""
+    k, n = 64, 136
+    dx = torch.full((1, k), 7.0, dtype=torch.bfloat16, device="cuda")
+    dy = torch.zeros(1, n, dtype=torch.bfloat16, device="cuda")
+    w = torch.zeros(k, n, dtype=torch.bfloat16, device="cuda")
+    for tc in (0, 1):
+        eng.backward_dx(dx, dy, w, 0, k, n, "bf16", None, tc)
+        db = torch.full((n,), 5.0, dtype=torch.float32, device="cuda")
+        eng.bias_grad(db, 1, dy, 0, n, "bf16")
+        eng.check()
+        assert torch.all(dx == 7.0)
+        assert torch.all(db == 0) and not torch.any(torch.signbit(db))
+
+
 def test_errors_are_reported(eng):
     h = eng.handle
     x = torch.zeros(16, 128, dtype=torch.bfloat16, device="cuda")
